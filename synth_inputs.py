@@ -1,0 +1,146 @@
+"""Seeded synthetic inputs for the W4A16 GEMM (shared by tests, bench and smoke check).
+
+This module only draws random numbers and lays them out in the canonical input format.
+It holds none of the method's arithmetic (no unpacking, dequantisation or products), so
+the oracle and the CUDA library can both be fed from it without sharing code.
+
+Canonical input format (the user-facing layout, before the library's repack):
+  A        activations, dtype bits uint16 [M, K], row-major.
+  qweight  uint32 [N, K/8]; nibble j (bits 4j..4j+3) of word w in row n is q[n, 8w+j].
+  scales   dtype bits uint16 [K/g, N].
+  qzeros   uint32 [K/g, N/8]; nibble j of word w in group row gi is z[gi, 8w+j];
+           None means symmetric weights, zero = 8.
+  cscale   optional per-channel factor, dtype bits uint16 [N].
+
+Recipe (one independent PCG64 stream per tensor, keyed by (seed, tensor id)):
+  A ~ N(0, 1) drawn in float64; optional outlier columns (a fraction of K, chosen
+  without replacement) are multiplied by a factor; then rounded to float32 and to the
+  dtype (numpy for fp16, torch for bf16; both round to nearest even).
+  q, z: uniform 32-bit words, i.e. eight independent uniform nibbles 0..15 per word.
+  scales ~ U[lo, hi] in float64, rounded to the dtype the same way.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+FP16 = 0
+BF16 = 1
+DTYPE_NAMES = {FP16: "fp16", BF16: "bf16"}
+
+_STREAM_A, _STREAM_Q, _STREAM_Z, _STREAM_S, _STREAM_OUT, _STREAM_C = 1, 2, 3, 4, 5, 6
+
+
+def _rng(seed: int, stream: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, stream])))
+
+
+def to_dtype_bits(x: np.ndarray, dtype: int) -> np.ndarray:
+    """float64 array -> fp16/bf16 bit patterns via the libraries' own RNE conversions."""
+    if dtype == FP16:
+        return np.ascontiguousarray(x.astype(np.float16).view(np.uint16))
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x.astype(np.float32))).to(torch.bfloat16)
+    return np.ascontiguousarray(t.view(torch.int16).numpy().view(np.uint16))
+
+
+@dataclass
+class Case:
+    M: int
+    N: int
+    K: int
+    group: int
+    dtype: int
+    A: np.ndarray
+    qweight: np.ndarray
+    scales: np.ndarray
+    qzeros: np.ndarray | None
+    cscale: np.ndarray | None = None
+    meta: dict = field(default_factory=dict)
+
+
+def make_case(M: int, N: int, K: int, group: int, dtype: int = FP16, seed: int = 0, *,
+              asym: bool = True, s_lo: float = 0.005, s_hi: float = 0.02,
+              outlier_frac: float = 0.0, outlier_gain: float = 20.0,
+              channel_scale: tuple[float, float] | None = None) -> Case:
+    assert K % group == 0 and K % 8 == 0 and N % 8 == 0
+    G = K // group
+    a = _rng(seed, _STREAM_A).standard_normal((M, K))
+    cols = np.zeros(0, dtype=np.int64)
+    if outlier_frac > 0.0:
+        n_out = int(round(outlier_frac * K))
+        cols = np.sort(_rng(seed, _STREAM_OUT).choice(K, size=n_out, replace=False))
+        a[:, cols] *= outlier_gain
+    A = to_dtype_bits(a, dtype)
+    qweight = _rng(seed, _STREAM_Q).integers(0, 1 << 32, size=(N, K // 8), dtype=np.uint32)
+    qzeros = None
+    if asym:
+        qzeros = _rng(seed, _STREAM_Z).integers(0, 1 << 32, size=(G, N // 8), dtype=np.uint32)
+    scales = to_dtype_bits(_rng(seed, _STREAM_S).uniform(s_lo, s_hi, size=(G, N)), dtype)
+    cscale = None
+    if channel_scale is not None:
+        cscale = to_dtype_bits(_rng(seed, _STREAM_C).uniform(*channel_scale, size=N), dtype)
+    return Case(M, N, K, group, dtype, A, qweight, scales, qzeros, cscale,
+                meta={"seed": seed, "outlier_cols": cols})
+
+
+# ---- the workloads -------------------------------------------------------------------
+# Each entry: name -> list of shapes; every shape is a dict of make_case arguments.
+
+def _decode_sweep():
+    out = []
+    for n in (4096, 11008):
+        for m in (1, 2, 4, 8, 16):
+            out.append(dict(M=m, N=n, K=4096, group=128, dtype=FP16, seed=1, asym=True,
+                            s_lo=0.005, s_hi=0.02))
+    return out
+
+
+def _ffn70b():
+    out = []
+    for (k, n) in ((8192, 28672), (28672, 8192)):
+        for m in (1, 8, 32):
+            out.append(dict(M=m, N=n, K=k, group=128, dtype=BF16, seed=2, asym=True,
+                            s_lo=0.002, s_hi=0.01, outlier_frac=0.001, outlier_gain=20.0))
+    return out
+
+
+def _transition():
+    out = []
+    for g in (32, 64, 128):
+        for m in (64, 128, 256):
+            out.append(dict(M=m, N=8192, K=8192, group=g, dtype=FP16, seed=3, asym=False,
+                            s_lo=0.005, s_hi=0.02))
+    return out
+
+
+WORKLOADS = {
+    # tiny single-token GEMM, seed 0
+    "tiny_m1_k512_n512_g128": [dict(M=1, N=512, K=512, group=128, dtype=FP16, seed=0,
+                                    asym=True, s_lo=0.005, s_hi=0.02)],
+    # decode sweep M in {1,2,4,8,16}, K=4096, N in {4096, 11008}
+    "decode_k4096_n4096_n11008": _decode_sweep(),
+    # 70B-shaped FFN decode, bf16 with 0.1% outlier columns x20
+    "ffn70b_decode_bf16": _ffn70b(),
+    # batch transition M in {64,128,256}, K=N=8192, g in {32,64,128}, symmetric
+    "transition_k8192_n8192": _transition(),
+    # prefill M=4096, K=4096, N=11008
+    "prefill_m4096_k4096_n11008": [dict(M=4096, N=11008, K=4096, group=128, dtype=FP16,
+                                        seed=4, asym=True, s_lo=0.005, s_hi=0.02)],
+}
+
+
+def shape_tag(p: dict) -> str:
+    return (f"M{p['M']}_N{p['N']}_K{p['K']}_g{p['group']}_{DTYPE_NAMES[p['dtype']]}"
+            f"{'' if p.get('asym', True) else '_sym'}")
+
+
+def algorithmic_bytes(M: int, N: int, K: int, group: int, asym: bool) -> int:
+    """Bytes the GEMM must move at least once: packed weights, scales, zeros, A and Y."""
+    G = K // group
+    return K * N // 2 + G * N * 2 + (G * N // 2 if asym else 0) + 2 * M * K + 2 * M * N
+
+
+def flops(M: int, N: int, K: int) -> int:
+    return 2 * M * N * K
