@@ -1,0 +1,176 @@
+/*
+ * w4a16.h -- C ABI of the W4A16 fused dequant-GEMM library for NVIDIA GB300 (sm_103a).
+ *
+ *   Y[M, N] = A[M, K] . W^T,   W[n, k] = s[k/g, n] * (q[n, k] - z[k/g, n])
+ *
+ * A is fp16 or bf16; W is stored as 4-bit nibbles q (8 per uint32), with one scale s
+ * (same dtype as A) and one 4-bit zero z per group of g = 32, 64 or 128 weights along K.
+ * The weights are dequantised only inside the GEMM kernel and are never written back
+ * to device memory.
+ *
+ * Sources (web pages, cited by title and section):
+ *   "W4A16 GEMM 算子浅析：INT4 权重反量化的计算流水线"
+ *       section "计算流水线的核心哲学"  -- HBM(4-bit) -> SMEM -> registers: unpack,
+ *           W = (W_int4 - Zero) * Scale, half2 -> tensor-core MMA with fp32 accumulate;
+ *       section "Marlin 与 CUTLASS 中的寄存器解包黑魔法" -- 8 nibbles per uint32 and the
+ *           0x6400 exponent-injection (magic bias) unpack.
+ *   "量化开销对比：各家方案的矩阵乘账本与省账手段"
+ *       §6.1-6.2 -- one launch, one pass over the weights, no materialised FP16 weights;
+ *           the group scale is applied to the weight operand inside the k loop, the
+ *           per-channel scale in the epilogue;
+ *       §6.4 -- offline repack of weights, scales and zeros into the kernel's tile order;
+ *       §6.5 -- weights stream from HBM exactly once, double-buffered with TMA.
+ *
+ * Conventions for every entry point:
+ *   - Every pointer named "device" is a CUDA device pointer on the CURRENT device
+ *     (cudaGetDevice()).  The caller owns every buffer; the library keeps no reference
+ *     after the call returns.
+ *   - "stream" is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *     Work is enqueued asynchronously on it; the call does not synchronise unless it
+ *     says so.
+ *   - Return values are w4a16_status codes (0 = success, negative = error).  Argument
+ *     errors are detected on the host before anything is launched.  Errors detected by
+ *     a kernel (packed-header mismatch, a pipeline wait that ran out) are recorded in a
+ *     per-device status word read by w4a16_get_device_status().
+ *   - Calls are thread-safe: the only library state is per-device, created on first use
+ *     under a lock.
+ */
+#ifndef W4A16_H_
+#define W4A16_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define W4A16_ABI_VERSION 1
+
+typedef enum w4a16_status {
+    W4A16_OK = 0,
+    W4A16_ERR_INVALID_ARG = -1,    /* null pointer, negative size, misaligned pointer  */
+    W4A16_ERR_UNSUPPORTED = -2,    /* shape or group the kernels do not handle         */
+    W4A16_ERR_CUDA = -3,           /* a CUDA runtime/driver call failed                */
+    W4A16_ERR_DEVICE_TIMEOUT = -4, /* a bounded in-kernel wait expired (device status) */
+    W4A16_ERR_FORMAT = -5          /* packed blob header does not match the arguments  */
+} w4a16_status;
+
+typedef enum w4a16_dtype {
+    W4A16_FP16 = 0,
+    W4A16_BF16 = 1
+} w4a16_dtype;
+
+/* Kernel selection for w4a16_gemm_ex (w4a16_gemm always uses W4A16_KERNEL_AUTO). */
+typedef enum w4a16_kernel {
+    W4A16_KERNEL_AUTO = 0,  /* choose by M                                            */
+    W4A16_KERNEL_TC = 1,    /* TMA ring -> dequant warps -> tcgen05.mma (swap-AB)      */
+    W4A16_KERNEL_SIMT = 2   /* CUDA-core FMA GEMV, M <= 8                             */
+} w4a16_kernel;
+
+typedef struct w4a16_gemm_config {
+    int kernel;       /* w4a16_kernel                                                   */
+    int split_k;      /* 0 = heuristic; else 1..8 K-slices reduced inside a CTA cluster  */
+    int tile_m;       /* 0 = heuristic; else 16, 32, 64, 128 or 256 rows of A per tile   */
+    int stages;       /* 0 = heuristic; else shared-memory ring depth (2..16)            */
+    int reserved[4];  /* must be zero                                                   */
+} w4a16_gemm_config;
+
+/* Library ABI version (W4A16_ABI_VERSION). */
+int w4a16_abi_version(void);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char* w4a16_status_string(int status);
+
+/*
+ * Size in bytes of the packed blob that w4a16_repack writes for these arguments, or 0
+ * if the shape is unsupported (see w4a16_repack).  The blob is
+ *     128-byte header
+ *   + K*N/2 bytes of nibbles
+ *   + (K/group)*N*2 bytes of scales
+ *   + (K/group)*N/2 bytes of zeros           (only if has_zeros)
+ *   + 4*N bytes of fp32 per-channel factors  (only if has_channel_scale)
+ * laid out in the kernel's tile order (128 output channels x 128 K per block, blocks of
+ * one channel tile contiguous along K; nibbles interleaved within each word so that
+ * one LOP3 per pair of halves unpacks them; the block's scales and zeros follow its
+ * nibbles so that they arrive with the weights).  The format is private to this
+ * library and versioned by the header.
+ */
+size_t w4a16_packed_bytes(int N, int K, int group, int has_zeros, int has_channel_scale);
+
+/*
+ * Offline repack ("量化开销对比" §6.4 / §6.7): reorder canonical quantised weights into
+ * the packed blob.  Runs once per weight matrix; asynchronous on `stream`.
+ *
+ *   qweight        device, uint32 [N][K/8], row-major.  Nibble j (bits 4j..4j+3) of word
+ *                  w in row n is q[n, 8w + j], an unsigned value 0..15.
+ *   scales         device, dtype [K/group][N], row-major: s[gi, n] for group gi.
+ *   qzeros         device, uint32 [K/group][N/8], row-major.  Nibble j of word w in row
+ *                  gi is z[gi, 8w + j].  NULL = symmetric weights, every zero is 8.
+ *   channel_scale  device, dtype [N]: optional factor c[n] applied to the fp32 result
+ *                  of output channel n in the epilogue.  NULL = none.
+ *   N, K, group    N % 128 == 0, K % 128 == 0, group in {32, 64, 128}; N, K > 0.
+ *   dtype          w4a16_dtype of scales and channel_scale (and of A/Y at GEMM time).
+ *   packed         device output, at least w4a16_packed_bytes(...) bytes, 16-byte
+ *                  aligned, must not overlap the inputs.
+ *   packed_bytes   capacity of `packed` in bytes.
+ * Errors: INVALID_ARG (null/misaligned pointer, capacity too small), UNSUPPORTED
+ * (shape/group/dtype), CUDA (launch failure).
+ */
+int w4a16_repack(const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                 const void* channel_scale, int N, int K, int group, int dtype,
+                 void* packed, size_t packed_bytes, void* stream);
+
+/*
+ * The fused W4A16 GEMM ("W4A16 GEMM 算子浅析" §"计算流水线的核心哲学"; "量化开销对比"
+ * §6.2): Y = A . W^T with W dequantised on the fly from `packed`; fp32 accumulation;
+ * the per-channel factor (if the blob has one) applied to the fp32 result; Y rounded to
+ * nearest-even into dtype.
+ *
+ *   A       device, dtype [M][K] row-major, 16-byte aligned.
+ *   packed  device, blob written by w4a16_repack with the same N, K, group, dtype.
+ *   M       rows of A and Y; M == 0 is a no-op that returns W4A16_OK.
+ *   N, K, group, dtype   as for w4a16_repack.
+ *   Y       device output, dtype [M][N] row-major, 16-byte aligned, must not overlap A
+ *           or packed.
+ * The kernel checks the blob header against (N, K, group, dtype); on a mismatch it
+ * writes nothing to Y and records W4A16_ERR_FORMAT in the device status word.
+ * Errors returned directly: INVALID_ARG, UNSUPPORTED, CUDA.
+ */
+int w4a16_gemm(const void* A, const void* packed, int M, int N, int K, int group, int dtype,
+               void* Y, void* stream);
+
+/* Same as w4a16_gemm with explicit kernel/tiling choices (cfg may be NULL = AUTO).
+ * Returns UNSUPPORTED for a combination the chosen kernel cannot run. */
+int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int group,
+                  int dtype, void* Y, const w4a16_gemm_config* cfg, void* stream);
+
+/*
+ * Debug / parity only: expand the packed blob to dtype W_out[N][K] (row-major, device)
+ * with exactly the unpack + dequant arithmetic the GEMM kernels use.  This is the
+ * materialised-weight path the pages warn against; it is never used by w4a16_gemm.
+ */
+int w4a16_dequant_debug(const void* packed, int N, int K, int group, int dtype,
+                        void* W_out, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's status word.
+ * Returns W4A16_OK, or the first error a kernel recorded since the last call
+ * (W4A16_ERR_FORMAT, W4A16_ERR_DEVICE_TIMEOUT), or W4A16_ERR_CUDA if the stream itself
+ * reports an error.
+ */
+int w4a16_get_device_status(void* stream);
+
+/*
+ * Failure-path check: launches one CTA that waits on an mbarrier nothing ever arrives
+ * on, with the same bounded wait the GEMM pipeline uses, limited to `timeout_us`
+ * microseconds (1..1000000).  The kernel records W4A16_ERR_DEVICE_TIMEOUT and returns;
+ * the GPU context stays usable.  Follow with w4a16_get_device_status().
+ */
+int w4a16_debug_timeout_probe(unsigned int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W4A16_H_ */

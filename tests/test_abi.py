@@ -1,0 +1,80 @@
+"""C-ABI library checks that need no GPU: it builds, loads, exports every function the
+header declares, and rejects bad arguments on the host before launching anything."""
+import ctypes
+
+import pytest
+
+import weight_only_int4_tma_gb300 as w4
+from weight_only_int4_tma_gb300 import build as w4build
+
+
+@pytest.fixture(scope="module")
+def L():
+    w4build.build()
+    return w4.lib()
+
+
+def test_exports_every_declared_function(L):
+    names = w4.header_functions()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(L, n), n
+
+
+def test_abi_version(L):
+    assert w4.w4a16_abi_version() == 1
+
+
+def test_status_strings(L):
+    for code in (0, -1, -2, -3, -4, -5):
+        assert w4.status_string(code)
+    assert w4.status_string(123) == "unknown status"
+
+
+@pytest.mark.parametrize("N,K,g,z,c", [(512, 512, 128, 1, 0), (4096, 4096, 128, 1, 0),
+                                       (8192, 8192, 32, 0, 0), (256, 384, 64, 1, 1)])
+def test_packed_bytes_formula(L, N, K, g, z, c):
+    want = 128 + K * N // 2 + (K // g) * N * 2 + (K // g) * N // 2 * z + 4 * N * c
+    assert w4.w4a16_packed_bytes(N, K, g, z, c) == want
+
+
+@pytest.mark.parametrize("N,K,g", [(100, 512, 128), (512, 500, 128), (512, 512, 16),
+                                   (512, 512, 96), (0, 512, 128), (512, 64, 32)])
+def test_packed_bytes_unsupported(L, N, K, g):
+    assert w4.w4a16_packed_bytes(N, K, g, 1, 0) == 0
+
+
+def test_repack_rejects_null_and_bad_shapes(L):
+    rc = L.w4a16_repack(None, None, None, None, 512, 512, 128, 0, None, 0, None)
+    assert rc == w4.W4A16_ERR_INVALID_ARG
+    fake = 1 << 20  # never dereferenced: the shape check fails first
+    assert L.w4a16_repack(fake, fake, None, None, 500, 512, 128, 0, fake, 1 << 30, None) \
+        == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_repack(fake, fake, None, None, 512, 512, 128, 7, fake, 1 << 30, None) \
+        == w4.W4A16_ERR_UNSUPPORTED
+    # capacity smaller than the blob
+    assert L.w4a16_repack(fake, fake, None, None, 512, 512, 128, 0, fake, 100, None) \
+        == w4.W4A16_ERR_INVALID_ARG
+    # misaligned qweight
+    assert L.w4a16_repack(fake + 4, fake, None, None, 512, 512, 128, 0, fake, 1 << 30, None) \
+        == w4.W4A16_ERR_INVALID_ARG
+
+
+def test_gemm_host_validation(L):
+    fake = 1 << 20
+    # M == 0 is a no-op that succeeds without touching the device
+    assert L.w4a16_gemm(None, None, 0, 512, 512, 128, 0, None, None) == w4.W4A16_OK
+    assert L.w4a16_gemm(fake, fake, -1, 512, 512, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_gemm(fake, fake, 4, 520, 512, 128, 0, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_gemm(fake, fake, 4, 512, 512, 48, 0, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_gemm(None, fake, 4, 512, 512, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_gemm(fake + 2, fake, 4, 512, 512, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_gemm(fake, fake, 4, 512, 512, 128, 0, fake + 8, None) == w4.W4A16_ERR_INVALID_ARG
+    cfg = w4.GemmConfig(0, 0, 0, 0)
+    cfg.reserved[0] = 0
+    assert L.w4a16_dequant_debug(None, 512, 512, 128, 0, None, None) == w4.W4A16_ERR_INVALID_ARG
+
+
+def test_timeout_probe_rejects_bad_limits(L):
+    assert L.w4a16_debug_timeout_probe(0, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a16_debug_timeout_probe(2_000_000, None) == w4.W4A16_ERR_INVALID_ARG

@@ -1,0 +1,226 @@
+// C-ABI entry points (include/w4a16.h): argument validation, per-device state, kernel
+// selection and the device status word.
+#include <cuda_runtime.h>
+
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/w4a16.h"
+#include "format.cuh"
+#include "launch.h"
+
+namespace w4g {
+
+// One status word per device (each device holds its own copy of a __device__ variable).
+__device__ int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::mutex g_ctx_mutex;
+DeviceCtx g_ctx[kMaxDevices];
+bool g_ctx_ready[kMaxDevices] = {};
+
+// Returns the current device's context, creating it on first use.
+int get_ctx(const DeviceCtx** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return W4A16_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_ctx_mutex);
+    if (!g_ctx_ready[dev]) {
+        DeviceCtx c{};
+        c.device = dev;
+        if (cudaDeviceGetAttribute(&c.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&c.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return W4A16_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return W4A16_ERR_CUDA;
+        c.status = static_cast<int*>(p);
+        uint64_t ms = 2000;
+        if (const char* e = std::getenv("W4A16_WAIT_TIMEOUT_MS")) {
+            const long v = std::strtol(e, nullptr, 10);
+            if (v > 0) ms = static_cast<uint64_t>(v);
+        }
+        c.timeout_ns = ms * 1000000ull;
+        g_ctx[dev] = c;
+        g_ctx_ready[dev] = true;
+    }
+    *out = &g_ctx[dev];
+    return W4A16_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_shape(int N, int K, int group, int dtype) {
+    if (N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
+    if (dtype != W4A16_FP16 && dtype != W4A16_BF16) return W4A16_ERR_UNSUPPORTED;
+    if (group != 32 && group != 64 && group != 128) return W4A16_ERR_UNSUPPORTED;
+    if (N % kTileN != 0 || K % kTileK != 0) return W4A16_ERR_UNSUPPORTED;
+    if (N / kTileN > 65535) return W4A16_ERR_UNSUPPORTED;  // grid.y limit
+    return W4A16_OK;
+}
+
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Kernel / tiling choice for a GEMM.
+int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
+              const w4a16_gemm_config* cfg, GemmPlan* plan) {
+    const int kernel = cfg ? cfg->kernel : W4A16_KERNEL_AUTO;
+    if (cfg) {
+        for (int i = 0; i < 4; ++i)
+            if (cfg->reserved[i] != 0) return W4A16_ERR_INVALID_ARG;
+    }
+    if (kernel == W4A16_KERNEL_SIMT) {
+        if (M > 8) return W4A16_ERR_UNSUPPORTED;
+        plan->kernel = W4A16_KERNEL_SIMT;
+        plan->tile_m = 0;
+        plan->split_k = 1;
+        plan->stages = 0;
+        return W4A16_OK;
+    }
+    if (kernel != W4A16_KERNEL_AUTO && kernel != W4A16_KERNEL_TC) return W4A16_ERR_INVALID_ARG;
+    plan->kernel = W4A16_KERNEL_TC;
+
+    int bm = cfg && cfg->tile_m ? cfg->tile_m : 0;
+    if (bm == 0) {
+        if (M <= 16) bm = 16;
+        else if (M <= 32) bm = 32;
+        else if (M <= 64) bm = 64;
+        else bm = 128;
+    }
+    if (bm != 16 && bm != 32 && bm != 64 && bm != 128 && bm != 256) return W4A16_ERR_UNSUPPORTED;
+    const int m_tiles = ceil_div(M, bm);
+    if (m_tiles > 65535) return W4A16_ERR_UNSUPPORTED;
+    const int kblocks = K / kTileK;
+    const int occ = bm <= 64 ? 2 : 1;  // CTAs per SM the ring depth below is sized for
+
+    int split = cfg && cfg->split_k ? cfg->split_k : 0;
+    if (split == 0) {
+        const int base = (N / kTileN) * m_tiles;
+        const int slots = ctx.num_sms * occ;
+        split = base >= slots ? 1 : slots / base;
+        if (split > 8) split = 8;
+        if (split > kblocks) split = kblocks;
+        if (split < 1) split = 1;
+    }
+    if (split < 1 || split > 8 || split > kblocks) return W4A16_ERR_UNSUPPORTED;
+
+    int stages = cfg && cfg->stages ? cfg->stages : 0;
+    const int smem_budget = occ == 2 ? 113 * 1024 : ctx.max_smem_optin;
+    const int max_st = tc_max_stages(bm, group, ctx.max_smem_optin);
+    if (stages == 0) {
+        stages = tc_max_stages(bm, group, smem_budget);
+        if (stages > 8) stages = 8;
+    }
+    if (stages < 2 || stages > max_st) return W4A16_ERR_UNSUPPORTED;
+    plan->tile_m = bm;
+    plan->split_k = split;
+    plan->stages = stages;
+    return W4A16_OK;
+}
+
+}  // namespace
+}  // namespace w4g
+
+using namespace w4g;
+
+extern "C" {
+
+int w4a16_abi_version(void) { return W4A16_ABI_VERSION; }
+
+const char* w4a16_status_string(int status) {
+    switch (status) {
+        case W4A16_OK: return "ok";
+        case W4A16_ERR_INVALID_ARG: return "invalid argument";
+        case W4A16_ERR_UNSUPPORTED: return "unsupported shape or option";
+        case W4A16_ERR_CUDA: return "CUDA error";
+        case W4A16_ERR_DEVICE_TIMEOUT: return "in-kernel wait timed out";
+        case W4A16_ERR_FORMAT: return "packed weight header does not match the arguments";
+        default: return "unknown status";
+    }
+}
+
+size_t w4a16_packed_bytes(int N, int K, int group, int has_zeros, int has_channel_scale) {
+    if (check_shape(N, K, group, W4A16_FP16) != W4A16_OK) return 0;
+    const size_t blocks = static_cast<size_t>(N / kTileN) * static_cast<size_t>(K / kTileK);
+    return kHeaderBytes + blocks * block_bytes(group, has_zeros != 0) +
+           (has_channel_scale ? 4ull * static_cast<size_t>(N) : 0ull);
+}
+
+int w4a16_repack(const uint32_t* qweight, const void* scales, const uint32_t* qzeros,
+                 const void* channel_scale, int N, int K, int group, int dtype, void* packed,
+                 size_t packed_bytes, void* stream) {
+    if (!qweight || !scales || !packed) return W4A16_ERR_INVALID_ARG;
+    int rc = check_shape(N, K, group, dtype);
+    if (rc != W4A16_OK) return rc;
+    if (!aligned(qweight, 16) || !aligned(scales, 2) || !aligned(packed, 16) ||
+        (qzeros && !aligned(qzeros, 4)) || (channel_scale && !aligned(channel_scale, 2)))
+        return W4A16_ERR_INVALID_ARG;
+    if (packed_bytes < w4a16_packed_bytes(N, K, group, qzeros != nullptr, channel_scale != nullptr))
+        return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
+    return launch_repack(*ctx, qweight, scales, qzeros, channel_scale, N, K, group, dtype,
+                         packed, static_cast<cudaStream_t>(stream));
+}
+
+int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int group, int dtype,
+                  void* Y, const w4a16_gemm_config* cfg, void* stream) {
+    if (M < 0) return W4A16_ERR_INVALID_ARG;
+    int rc = check_shape(N, K, group, dtype);
+    if (rc != W4A16_OK) return rc;
+    if (M == 0) return W4A16_OK;
+    if (!A || !packed || !Y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(Y, 16) || !aligned(packed, 16)) return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
+    GemmPlan plan{};
+    if ((rc = make_plan(*ctx, M, N, K, group, cfg, &plan)) != W4A16_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (plan.kernel == W4A16_KERNEL_SIMT)
+        return launch_simt_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, s);
+    return launch_tc_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, s);
+}
+
+int w4a16_gemm(const void* A, const void* packed, int M, int N, int K, int group, int dtype,
+               void* Y, void* stream) {
+    return w4a16_gemm_ex(A, packed, M, N, K, group, dtype, Y, nullptr, stream);
+}
+
+int w4a16_dequant_debug(const void* packed, int N, int K, int group, int dtype, void* W_out,
+                        void* stream) {
+    if (!packed || !W_out) return W4A16_ERR_INVALID_ARG;
+    int rc = check_shape(N, K, group, dtype);
+    if (rc != W4A16_OK) return rc;
+    if (!aligned(packed, 16) || !aligned(W_out, 16)) return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
+    return launch_dequant_debug(*ctx, packed, N, K, group, dtype, W_out,
+                                static_cast<cudaStream_t>(stream));
+}
+
+int w4a16_get_device_status(void* stream) {
+    const DeviceCtx* ctx = nullptr;
+    int rc = get_ctx(&ctx);
+    if (rc != W4A16_OK) return rc;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return W4A16_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyAsync(&v, ctx->status, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(ctx->status, 0, sizeof(int), s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return W4A16_ERR_CUDA;
+    return v;
+}
+
+int w4a16_debug_timeout_probe(unsigned int timeout_us, void* stream) {
+    if (timeout_us < 1 || timeout_us > 1000000) return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    int rc = get_ctx(&ctx);
+    if (rc != W4A16_OK) return rc;
+    return launch_timeout_probe(*ctx, static_cast<uint64_t>(timeout_us) * 1000ull,
+                                static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"

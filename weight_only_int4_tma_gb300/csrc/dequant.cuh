@@ -1,0 +1,86 @@
+// Register-level unpack + dequant of one packed word (8 weights) into four 16-bit pairs.
+//
+// "W4A16 GEMM 算子浅析" §"Marlin 与 CUTLASS 中的寄存器解包黑魔法": OR-ing a nibble into
+// the mantissa of the pattern 0x6400 (fp16 1024.0) gives the fp16 number 1024 + q with
+// no integer-to-float conversion.  The page's printed mask 0x0F0F0F0F would leave two
+// nibbles in one half; the per-half mask here is 0x000F000F, and the packed format puts
+// the pair (k_2i, k_2i+1) at nibble positions (i, i+4) so that (x >> 4i) & 0x000F000F
+// selects it.  bf16 uses 0x4300 (128.0), whose 7-bit mantissa also has unit spacing.
+//
+// The value must be ONE round-to-nearest-even of (q - z) * s ("计算流水线的核心哲学" step 2,
+// W = (W_int4 - Zero) * Scale).  A single fma with a pre-rounded -(1024 + z) * s constant
+// would round twice, so the pair is formed as
+//     t = (1024 + q) - (1024 + z)   exact: an integer in [-15, 15]
+//     w = t * s                     one rounding, to nearest even
+// with sub.rn / mul.rn on packed pairs: one LOP3 + one SUB + one MUL per pair of weights.
+#pragma once
+#include <cstdint>
+
+namespace w4g {
+
+template <int DT>
+struct Magic;
+template <>
+struct Magic<0> {  // fp16: 1024.0 in each half
+    static constexpr uint32_t kPair = 0x64006400u;
+};
+template <>
+struct Magic<1> {  // bf16: 128.0 in each half
+    static constexpr uint32_t kPair = 0x43004300u;
+};
+
+__device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;  // (a & b) | c
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t sub_pair(uint32_t a, uint32_t b) {
+    uint32_t d;
+    if constexpr (DT == 0) {
+        asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    } else {
+        asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    }
+    return d;
+}
+
+template <int DT>
+__device__ __forceinline__ uint32_t mul_pair(uint32_t a, uint32_t b) {
+    uint32_t d;
+    if constexpr (DT == 0) {
+        asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    } else {
+        asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    }
+    return d;
+}
+
+// Per-(group, row) constants: biased zero (1024 + z or 128 + z in both halves) and the
+// scale in both halves.
+template <int DT>
+__device__ __forceinline__ uint32_t zero_pair(uint32_t z) {
+    return Magic<DT>::kPair | (z * 0x00010001u);
+}
+__device__ __forceinline__ uint32_t scale_pair(uint32_t sbits) {
+    return sbits * 0x00010001u;
+}
+
+// x: one packed word (see format.cuh).  out[i] = (w[k_2i], w[k_2i+1]) as a 16-bit pair.
+template <int DT>
+__device__ __forceinline__ void dequant_word(uint32_t x, uint32_t zp, uint32_t sp,
+                                             uint32_t* out) {
+    constexpr uint32_t kMask = 0x000F000Fu;
+    constexpr uint32_t kM = Magic<DT>::kPair;
+    const uint32_t t0 = lop3_and_or(x, kMask, kM);
+    const uint32_t t1 = lop3_and_or(x >> 4, kMask, kM);
+    const uint32_t t2 = lop3_and_or(x >> 8, kMask, kM);
+    const uint32_t t3 = lop3_and_or(x >> 12, kMask, kM);
+    out[0] = mul_pair<DT>(sub_pair<DT>(t0, zp), sp);
+    out[1] = mul_pair<DT>(sub_pair<DT>(t1, zp), sp);
+    out[2] = mul_pair<DT>(sub_pair<DT>(t2, zp), sp);
+    out[3] = mul_pair<DT>(sub_pair<DT>(t3, zp), sp);
+}
+
+}  // namespace w4g

@@ -1,0 +1,48 @@
+// Internal host-side interface between the C-ABI layer (api.cu) and the kernel units.
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace w4g {
+
+// Per-device state, created once per device on first use.
+struct DeviceCtx {
+    int device;
+    int num_sms;
+    int max_smem_optin;     // bytes of dynamic shared memory a CTA may opt into
+    int* status;            // device address of this device's status word
+    uint64_t timeout_ns;    // limit of every bounded in-kernel wait
+};
+
+struct GemmPlan {
+    int kernel;   // 1 = tcgen05, 2 = SIMT
+    int tile_m;   // activation rows per tile (tcgen05 kernel)
+    int split_k;  // K slices (cluster size for the tcgen05 kernel)
+    int stages;   // shared-memory ring depth
+};
+
+// Launchers return a w4a16_status code.
+int launch_repack(const DeviceCtx& ctx, const uint32_t* qweight, const void* scales,
+                  const uint32_t* qzeros, const void* cscale, int N, int K, int group,
+                  int dtype, void* packed, cudaStream_t stream);
+
+int launch_dequant_debug(const DeviceCtx& ctx, const void* packed, int N, int K, int group,
+                         int dtype, void* W_out, cudaStream_t stream);
+
+int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
+                   int K, int group, int dtype, void* Y, const GemmPlan& plan,
+                   cudaStream_t stream);
+
+int launch_simt_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
+                     int K, int group, int dtype, void* Y, const GemmPlan& plan,
+                     cudaStream_t stream);
+
+int launch_timeout_probe(const DeviceCtx& ctx, uint64_t limit_ns, cudaStream_t stream);
+
+// Bytes of one stage of the tcgen05 ring for a tile of `tile_m` activation rows.
+uint32_t tc_stage_bytes(int tile_m, int group);
+// Largest ring depth that fits `smem_budget` bytes of dynamic shared memory.
+int tc_max_stages(int tile_m, int group, int smem_budget);
+
+}  // namespace w4g

@@ -1,0 +1,184 @@
+// Offline repack of canonical (qweight, scales, zeros, channel scale) into the packed
+// tile-ordered blob ("量化开销对比" §6.4: scales and zeros rearranged into the same
+// order as the weight tiles so that they arrive with them), and the debug-only
+// expansion of a blob back to dtype weights with the GEMM's own unpack arithmetic.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "dequant.cuh"
+#include "format.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+
+namespace w4g {
+namespace {
+
+// Permute the eight nibbles of a canonical word (nibble j holds K offset j) into the
+// packed order (K offset j at nibble position nibble_pos(j)).
+__device__ __forceinline__ uint32_t permute_nibbles(uint32_t w) {
+    uint32_t out = 0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) out |= ((w >> (4 * j)) & 0xFu) << (4 * nibble_pos(j));
+    return out;
+}
+
+__device__ __forceinline__ float decode_scale(uint16_t bits, int dtype) {
+    return dtype == 0 ? __half2float(__ushort_as_half(bits))
+                      : __bfloat162float(__ushort_as_bfloat16(bits));
+}
+
+// One CTA per (channel tile, K block); 512 threads.
+__global__ void __launch_bounds__(512) repack_kernel(
+    const uint32_t* __restrict__ qweight, const uint16_t* __restrict__ scales,
+    const uint32_t* __restrict__ qzeros, const uint16_t* __restrict__ cscale, int N, int K,
+    int group, int dtype, uint8_t* __restrict__ packed, uint32_t bb, uint64_t cs_off,
+    uint64_t total) {
+    const int kblocks = K / kTileK;
+    const int nt = blockIdx.x / kblocks;
+    const int kb = blockIdx.x % kblocks;
+    const int t = threadIdx.x;
+    uint8_t* blk = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * bb;
+    const int G = groups_per_block(group);
+
+    {   // nibbles: thread t -> chunk c = t / 128, row r = t % 128, four words
+        const int c = t >> 7, r = t & 127;
+        const int n = nt * kTileN + r;
+        const uint4 src = *reinterpret_cast<const uint4*>(
+            qweight + static_cast<size_t>(n) * (K / 8) + kb * (kTileK / 8) + c * 4);
+        uint4 dst;
+        dst.x = permute_nibbles(src.x);
+        dst.y = permute_nibbles(src.y);
+        dst.z = permute_nibbles(src.z);
+        dst.w = permute_nibbles(src.w);
+        *reinterpret_cast<uint4*>(blk + c * 2048 + r * 16) = dst;
+    }
+    const int gbase = kb * G;  // first global group index of this block
+    if (t < G * kTileN) {      // scales: [gi][r]
+        const int gi = t >> 7, r = t & 127;
+        const uint16_t s = scales[static_cast<size_t>(gbase + gi) * N + nt * kTileN + r];
+        reinterpret_cast<uint16_t*>(blk + kNibbleBytes)[gi * kTileN + r] = s;
+    }
+    if (qzeros != nullptr && t < G * (kTileN / 2)) {  // zeros: [gi][byte r/2]
+        const int gi = t / (kTileN / 2), b = t % (kTileN / 2);
+        const int n0 = nt * kTileN + 2 * b;
+        const uint32_t* zrow = qzeros + static_cast<size_t>(gbase + gi) * (N / 8);
+        const uint32_t z0 = (zrow[n0 / 8] >> (4 * (n0 % 8))) & 0xFu;
+        const uint32_t z1 = (zrow[(n0 + 1) / 8] >> (4 * ((n0 + 1) % 8))) & 0xFu;
+        blk[kNibbleBytes + scale_bytes(group) + gi * (kTileN / 2) + b] =
+            static_cast<uint8_t>(z0 | (z1 << 4));
+    }
+    if (blockIdx.x == 0) {
+        if (cscale != nullptr) {
+            float* cs = reinterpret_cast<float*>(packed + cs_off);
+            for (int n = t; n < N; n += blockDim.x) cs[n] = decode_scale(cscale[n], dtype);
+        }
+        if (t == 0) {
+            PackedHeader h{};
+            h.magic = kMagic;
+            h.version = kVersion;
+            h.N = N;
+            h.K = K;
+            h.group = group;
+            h.dtype = dtype;
+            h.flags = (qzeros ? kFlagZeros : 0u) | (cscale ? kFlagChannelScale : 0u);
+            h.block_bytes = bb;
+            h.body_offset = kHeaderBytes;
+            h.cscale_offset = cscale ? cs_off : 0;
+            h.total_bytes = total;
+            *reinterpret_cast<PackedHeader*>(packed) = h;
+        }
+    }
+}
+
+// One thread per (block, chunk, row): 32 weights -> 64 bytes of W_out.
+template <int DT>
+__global__ void __launch_bounds__(512) dequant_debug_kernel(const uint8_t* __restrict__ packed,
+                                                            int N, int K, int group,
+                                                            uint16_t* __restrict__ W,
+                                                            int* status) {
+    __shared__ int s_flags;
+    if (threadIdx.x == 0)
+        s_flags = check_header(reinterpret_cast<const PackedHeader*>(packed), N, K, group, DT);
+    __syncthreads();
+    const int flags = s_flags;
+    if (flags < 0) {
+        if (blockIdx.x == 0 && threadIdx.x == 0) record_status(status, kStatusFormat);
+        return;
+    }
+    const bool has_z = (flags & kFlagZeros) != 0;
+    const uint32_t bb = block_bytes(group, has_z);
+    const int kblocks = K / kTileK;
+    const int nt = blockIdx.x / kblocks, kb = blockIdx.x % kblocks;
+    const int c = threadIdx.x >> 7, r = threadIdx.x & 127;
+    const uint8_t* blk = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * bb;
+    const int gi = (c * kChunkK) / group;
+    const uint32_t sbits = reinterpret_cast<const uint16_t*>(blk + kNibbleBytes)[gi * kTileN + r];
+    uint32_t z = 8;
+    if (has_z) z = (blk[kNibbleBytes + scale_bytes(group) + gi * 64 + (r >> 1)] >> ((r & 1) * 4)) & 0xFu;
+    const uint32_t zp = zero_pair<DT>(z), sp = scale_pair(sbits);
+    const uint4 v = *reinterpret_cast<const uint4*>(blk + c * 2048 + r * 16);
+    uint32_t out[16];
+    dequant_word<DT>(v.x, zp, sp, out + 0);
+    dequant_word<DT>(v.y, zp, sp, out + 4);
+    dequant_word<DT>(v.z, zp, sp, out + 8);
+    dequant_word<DT>(v.w, zp, sp, out + 12);
+    const int n = nt * kTileN + r;
+    const int k0 = kb * kTileK + c * kChunkK;
+    uint4* dst = reinterpret_cast<uint4*>(W + static_cast<size_t>(n) * K + k0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
+}
+
+// Failure-path check: one CTA waits on an mbarrier that nothing arrives on.
+__global__ void timeout_probe_kernel(int* status, uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_addr(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        (void)mbar_wait_bounded(smem_addr(&bar), 0, &abort_flag, status, limit_ns);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+int launch_repack(const DeviceCtx& ctx, const uint32_t* qweight, const void* scales,
+                  const uint32_t* qzeros, const void* cscale, int N, int K, int group,
+                  int dtype, void* packed, cudaStream_t stream) {
+    (void)ctx;
+    const bool z = qzeros != nullptr;
+    const uint32_t bb = block_bytes(group, z);
+    const size_t blocks = static_cast<size_t>(N / kTileN) * (K / kTileK);
+    const uint64_t cs_off = kHeaderBytes + blocks * bb;
+    const uint64_t total = cs_off + (cscale ? 4ull * N : 0ull);
+    repack_kernel<<<static_cast<unsigned>(blocks), 512, 0, stream>>>(
+        qweight, static_cast<const uint16_t*>(scales), qzeros,
+        static_cast<const uint16_t*>(cscale), N, K, group, dtype,
+        static_cast<uint8_t*>(packed), bb, cs_off, total);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_dequant_debug(const DeviceCtx& ctx, const void* packed, int N, int K, int group,
+                         int dtype, void* W_out, cudaStream_t stream) {
+    const unsigned blocks = static_cast<unsigned>((N / kTileN) * (K / kTileK));
+    const uint8_t* p = static_cast<const uint8_t*>(packed);
+    uint16_t* w = static_cast<uint16_t*>(W_out);
+    if (dtype == 0)
+        dequant_debug_kernel<0><<<blocks, 512, 0, stream>>>(p, N, K, group, w, ctx.status);
+    else
+        dequant_debug_kernel<1><<<blocks, 512, 0, stream>>>(p, N, K, group, w, ctx.status);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+int launch_timeout_probe(const DeviceCtx& ctx, uint64_t limit_ns, cudaStream_t stream) {
+    timeout_probe_kernel<<<1, 32, 0, stream>>>(ctx.status, limit_ns);
+    return cudaGetLastError() == cudaSuccess ? 0 : -3;
+}
+
+}  // namespace w4g
