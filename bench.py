@@ -1,0 +1,491 @@
+"""Benchmark of the W4A16 fused dequant-GEMM on GB300.
+
+One step = one pass of the decode sweep: the fused GEMM for M in {1,2,4,8,16},
+K = 4096, N in {4096, 11008}, group 128, fp16 activations, asymmetric int4 weights
+(10 launches).  The repack is offline and not timed.  The headline metric is achieved
+HBM TB/s over algorithmic bytes (packed weights + scales + zeros + A + Y).
+
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead.
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth_inputs as si  # noqa: E402
+
+DEFAULT_WORKLOAD = "decode_k4096_n4096_n11008"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(si.WORKLOADS))
+    ap.add_argument("--graph-steps", type=int, default=10,
+                    help="steps captured per CUDA graph (replayed to reach --steps)")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", type=int, default=0, help="0 auto, 1 tcgen05, 2 SIMT")
+    ap.add_argument("--split-k", type=int, default=0)
+    ap.add_argument("--tile-m", type=int, default=0)
+    ap.add_argument("--stages", type=int, default=0)
+    return ap.parse_args()
+
+
+# ---- distributed plumbing (one process per GPU; replicas, no data-path collective) ---
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    ws, rank, _ = dist_info()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend, rank=rank, world_size=ws)
+    return ws, rank
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---- measured peaks, clocks, profile traffic ------------------------------------------
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append((time.time(), ln.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=2)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            if self.t is not None:
+                self.t.join(timeout=2)
+
+    def summary(self, t0=None, t1=None):
+        rows = []
+        for ts, ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((ts, float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sel = [r for r in rows if t0 is None or (t0 - 0.25 <= r[0] <= t1 + 0.25)] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[3]) if v == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in sel),
+                "sm_max_mhz": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel)}
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "weight_only_int4_tma_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
+        if p.endswith((".cu", ".cuh", ".h")):
+            h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernels are unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(workload)
+    if not d or d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---- the reference arm: the CPU oracle ----------------------------------------------
+
+def oracle_slice(orc, c, n0, nc):
+    """Oracle dequant + GEMM for output channels [n0, n0 + nc) of a case."""
+    G = c.K // c.group
+    qw = c.qweight[n0:n0 + nc]
+    sc = np.ascontiguousarray(c.scales[:, n0:n0 + nc])
+    qz = None if c.qzeros is None else np.ascontiguousarray(c.qzeros[:, n0 // 8:(n0 + nc) // 8])
+    wd = orc.dequant(qw, sc, qz, nc, c.K, c.group, c.dtype)
+    orc.gemm(c.A, wd, c.M, nc, c.K, c.dtype)
+    _ = G
+
+
+def shape_bytes(p):
+    return si.algorithmic_bytes(p["M"], p["N"], p["K"], p["group"], p.get("asym", True))
+
+
+def cpu_oracle_rate(cases, shapes, budget_s):
+    """Times the oracle over slices of the workload's shapes for about budget_s seconds.
+    Returns (bytes/s, sample description, threads)."""
+    import oracle as orc
+    orc.build()
+    total_bytes = 0.0
+    t_used = 0.0
+    done = []
+    nc = 256
+    i = 0
+    while t_used < budget_s and i < 10 * len(cases):
+        c, p = cases[i % len(cases)], shapes[i % len(cases)]
+        n0 = (i // len(cases)) * nc % c.N
+        t0 = time.perf_counter()
+        oracle_slice(orc, c, n0, nc)
+        dt = time.perf_counter() - t0
+        t_used += dt
+        total_bytes += shape_bytes(p) * nc / c.N
+        done.append(f"{si.shape_tag(p)}[n {n0}:{n0 + nc}]")
+        i += 1
+    desc = (f"{len(done)} slices of {nc} output channels (dequant + fp64 GEMM), e.g. "
+            + ", ".join(done[:3]))
+    return total_bytes / t_used, desc, orc.num_threads(), t_used
+
+
+def run_reference(a):
+    ws, rank, _ = dist_info()
+    if ws > 1:
+        dist_init("gloo")
+        if rank != 0:
+            return
+    shapes = si.WORKLOADS[a.workload]
+    cases = [si.make_case(**p) for p in shapes]
+    step_bytes = sum(shape_bytes(p) for p in shapes)
+    import oracle as orc
+    orc.build()
+    # Each step: one slice of output channels of one shape, sized so that the whole run
+    # stays within about two minutes.
+    budget = 120.0 / max(1, a.steps + a.warmup)
+    probe_c, probe_p = cases[0], shapes[0]
+    t0 = time.perf_counter()
+    oracle_slice(orc, probe_c, 0, 8)
+    per_ch = (time.perf_counter() - t0) / 8
+    nc = int(max(8, min(probe_c.N, (budget / max(per_ch, 1e-9)) // 8 * 8)))
+    for i in range(a.warmup):
+        c = cases[i % len(cases)]
+        oracle_slice(orc, c, 0, min(nc, c.N))
+    tot_b = 0.0
+    t0 = time.perf_counter()
+    for i in range(a.steps):
+        c, p = cases[i % len(cases)], shapes[i % len(cases)]
+        n = min(nc, c.N)
+        n0 = (i * n) % c.N
+        n = min(n, c.N - n0)
+        oracle_slice(orc, c, n0, n)
+        tot_b += shape_bytes(p) * n / c.N
+    el = time.perf_counter() - t0
+    v = tot_b / el / 1e12
+    sample = f"per step: {nc} output channels of one decode shape (dequant + fp64 GEMM)"
+    line = {
+        "impl": "reference", "metric": "W4A16 GEMM achieved HBM TB/s (decode sweep)",
+        "value": v, "unit": "TB/s", "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": el / max(1, a.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": a.workload, "step_bytes_full": step_bytes},
+        "cpu_baseline": {"value": v, "unit": "TB/s", "cores": orc.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---- our arm ------------------------------------------------------------------------
+
+def run_ours(a):
+    import torch
+
+    ws, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        dist_init("nccl")
+
+    from weight_only_int4_tma_gb300 import build as w4build
+    w4build.build()
+    import weight_only_int4_tma_gb300 as w4
+
+    shapes = si.WORKLOADS[a.workload]
+    cases = [si.make_case(**p) for p in shapes]
+    step_bytes = sum(shape_bytes(p) for p in shapes)
+    step_flops = sum(si.flops(p["M"], p["N"], p["K"]) for p in shapes)
+
+    def dev(x):
+        if x is None:
+            return None
+        v = x.view(np.int16) if x.dtype == np.uint16 else x.view(np.int32)
+        return torch.from_numpy(np.ascontiguousarray(v)).to(device)
+
+    # Weights rotate over enough copies that each launch reads them from HBM, not L2.
+    packed_per_step = sum(w4.w4a16_packed_bytes(c.N, c.K, c.group, c.qzeros is not None)
+                          for c in cases)
+    copies = max(2, -(-3 * L2_BYTES // max(1, packed_per_step)))
+    bufs = []
+    for c in cases:
+        first = w4.repack(dev(c.qweight), dev(c.scales), dev(c.qzeros), c.N, c.K, c.group,
+                          c.dtype)
+        reps = [first] + [first.clone() for _ in range(copies - 1)]
+        A = dev(c.A)
+        Y = torch.empty((c.M, c.N), dtype=torch.int16, device=device)
+        bufs.append((c, reps, A, Y))
+    torch.cuda.synchronize()
+    ex = dict(kernel=a.kernel, split_k=a.split_k, tile_m=a.tile_m, stages=a.stages)
+
+    stream = torch.cuda.Stream(device=device)
+
+    def launch_step(step_idx, evs=None):
+        for j, (c, reps, A, Y) in enumerate(bufs):
+            if evs is not None:
+                evs[j][0].record(stream)
+            w4.w4a16_gemm_ex(A, reps[step_idx % copies], c.M, c.N, c.K, c.group, c.dtype, Y,
+                             stream=stream, **ex)
+            if evs is not None:
+                evs[j][1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, a.warmup)):
+            launch_step(i)
+    stream.synchronize()
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status after warm-up: {w4.status_string(st)}")
+
+    # Capture G steps (with an event pair around every GEMM) into one CUDA graph.
+    G = max(1, min(a.graph_steps, a.steps))
+    def timing_event():
+        try:   # recorded as a real event node when captured into a graph
+            return torch.cuda.Event(enable_timing=True, external=True)
+        except TypeError:
+            return None
+
+    evs = [[[timing_event(), timing_event()] for _ in bufs] for _ in range(G)]
+    if any(e is None for row in evs for pair in row for e in pair):
+        evs = None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for g in range(G):
+                launch_step(g, evs[g] if evs is not None else None)
+    stream.synchronize()
+    replays = -(-a.steps // G)
+    tail = replays * G - a.steps      # steps to run eagerly instead (keep exactly K)
+    full_replays = replays - (1 if tail else 0)
+    eager_tail = (a.steps - full_replays * G)
+
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            graph.replay()
+    stream.synchronize()
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(full_replays):
+            graph.replay()
+        for i in range(eager_tail):
+            launch_step(i)
+        e1.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize(device)
+    barrier(device)
+    t_wall1 = time.time()
+    time.sleep(0.3)
+    sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"device status after timed region: {w4.status_string(st)}")
+    elapsed_ms = max_over_ranks(elapsed_ms, device)
+
+    # Per-launch kernel durations (last replay inside the timed region), per shape.
+    per_shape_ms = []
+    if evs is not None:
+        for j in range(len(bufs)):
+            per_shape_ms.append(statistics.mean(evs[g][j][0].elapsed_time(evs[g][j][1])
+                                                for g in range(G)))
+    else:  # no external graph events: time an eager pass queued behind a sleep kernel
+        ev2 = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+                for _ in bufs] for _ in range(G)]
+        with torch.cuda.stream(stream):
+            torch.cuda._sleep(50_000_000)
+            for g in range(G):
+                launch_step(g, ev2[g])
+        stream.synchronize()
+        for j in range(len(bufs)):
+            per_shape_ms.append(statistics.mean(ev2[g][j][0].elapsed_time(ev2[g][j][1])
+                                                for g in range(G)))
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    launch_bytes = [shape_bytes(p) for p in shapes]
+    achieved_gbs = sum(launch_bytes) / (sum(per_shape_ms) * 1e-3) / 1e9
+    traffic = profiled_traffic(a.workload)
+    value = step_bytes * a.steps * ws / (elapsed_ms * 1e-3) / 1e12
+
+    # End to end through the public API: pinned host A in, Y out, every step.
+    e2e_steps = max(1, min(a.e2e_steps, a.steps))
+    hostA = [torch.from_numpy(np.ascontiguousarray(c.A.view(np.int16))).pin_memory()
+             for c, _, _, _ in bufs]
+    hostY = [torch.empty((c.M, c.N), dtype=torch.int16).pin_memory() for c, _, _, _ in bufs]
+    h2d = sum(2 * c.M * c.K for c in cases)
+    d2h = sum(2 * c.M * c.N for c in cases)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            for j, (c, reps, A, Y) in enumerate(bufs):
+                A.copy_(hostA[j], non_blocking=True)
+                w4.w4a16_gemm(A, reps[i % copies], c.M, c.N, c.K, c.group, c.dtype, Y, stream)
+                hostY[j].copy_(Y, non_blocking=True)
+    stream.synchronize()
+    barrier(device)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        f0.record(stream)
+        for i in range(e2e_steps):
+            for j, (c, reps, A, Y) in enumerate(bufs):
+                A.copy_(hostA[j], non_blocking=True)
+                w4.w4a16_gemm(A, reps[i % copies], c.M, c.N, c.K, c.group, c.dtype, Y, stream)
+                hostY[j].copy_(Y, non_blocking=True)
+        f1.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), device)
+    e2e_val = step_bytes * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and ws == 1 and not a.no_cpu_baseline:
+        rate, desc, cores, used = cpu_oracle_rate(cases, shapes, budget_s=12.0)
+        cpu = {"value": rate / 1e12, "unit": "TB/s", "cores": cores, "kind": "oracle",
+               "sample": f"{desc}; {used:.1f} s of CPU time"}
+
+    if rank != 0:
+        return
+    per_shape = []
+    for p, ms, b in zip(shapes, per_shape_ms, launch_bytes):
+        per_shape.append({"shape": si.shape_tag(p), "us": round(ms * 1e3, 3),
+                          "gbs": round(b / (ms * 1e-3) / 1e9, 1),
+                          "frac": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4)})
+    clocks = sampler.summary(t_wall0, t_wall1)
+    line = {
+        "metric": "W4A16 GEMM achieved HBM TB/s (decode sweep, M<=16)",
+        "value": value, "unit": "TB/s", "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": elapsed_ms / a.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": a.workload, "shapes": len(shapes), "step_bytes": step_bytes,
+                   "step_flops": step_flops,
+                   "l2": f"inputs larger than L2: {copies} rotating copies of the packed "
+                         f"weights ({copies * packed_per_step / 2**20:.0f} MiB per rotation)",
+                   "timing": f"CUDA graph of {G} steps replayed; CUDA events on the launch "
+                             f"stream", "parallelism": f"replicas{ws}",
+                   "kernel": a.kernel, "split_k": a.split_k, "tile_m": a.tile_m,
+                   "stages": a.stages},
+        "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved_gbs / hbm_peak,
+                     "traffic": traffic, "peak_kind": peak_kind,
+                     "algorithmic_bytes_per_launch": sum(launch_bytes) / len(launch_bytes),
+                     "kernel": "w4a16_tc_kernel" if a.kernel != 2 else "w4a16_simt_kernel"},
+        "per_shape": per_shape,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_val, "unit": "TB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "note": "public C-ABI call per shape with pinned host A in and Y out; packed "
+                        "weights resident (uploaded once, as in serving)"},
+        "gpu_launches": a.steps * len(shapes),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

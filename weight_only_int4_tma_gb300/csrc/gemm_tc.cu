@@ -357,9 +357,19 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
 
     const size_t smem = static_cast<size_t>(plan.stages) * args.stage_bytes + kCtrlBytes + 1024;
     auto kern = w4a16_tc_kernel<BM, NWG, DT>;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-        return -3;
+    {   // raise the dynamic shared-memory limit once per device (not a stream operation,
+        // but kept out of the steady state so that launches can be graph-captured cheaply)
+        static std::mutex mu;
+        static size_t configured[64] = {};
+        std::lock_guard<std::mutex> lock(mu);
+        const int d = ctx.device < 64 ? ctx.device : 63;
+        if (configured[d] < smem) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     static_cast<int>(smem)) != cudaSuccess)
+                return -3;
+            configured[d] = smem;
+        }
+    }
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.split_k), static_cast<unsigned>(N / kTileN),
