@@ -38,6 +38,25 @@ namespace {
 constexpr int kMaxStages = 16;
 constexpr int kCtrlBytes = 1024;
 
+#ifdef W4A16_TRACE
+// Development-only timeline (built with -DW4A16_TRACE, never in the product library):
+// globaltimer stamps per CTA for the first kTraceCtas CTAs.
+constexpr int kTraceCtas = 1024;
+constexpr int kTraceSlots = 64;
+__device__ unsigned long long g_w4a16_trace[kTraceCtas * kTraceSlots];
+#define W4G_TRACE(slot, value)                                                         \
+    do {                                                                              \
+        const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z); \
+        const int slot_ = (slot);                                                     \
+        if (cta_ < kTraceCtas && slot_ >= 0 && slot_ < kTraceSlots)                   \
+            g_w4a16_trace[cta_ * kTraceSlots + slot_] = (value);                      \
+    } while (0)
+#define W4G_NOW() globaltimer_ns()
+#else
+#define W4G_TRACE(slot, value) do { } while (0)
+#define W4G_NOW() 0ull
+#endif
+
 struct TcArgs {
     const uint8_t* packed;
     void* Y;
@@ -97,6 +116,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const int nkb = kb_per + (split < kb_rem ? 1 : 0);
 
     if (threadIdx.x == 0) {
+        W4G_TRACE(0, W4G_NOW());
         const PackedHeader* h = reinterpret_cast<const PackedHeader*>(args.packed);
         const int flags = check_header(h, args.N, args.K, args.group, DT);
         info[0] = flags;
@@ -128,6 +148,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     tc_fence_after();
 
     const uint32_t tmem = *tmem_slot;
+#ifdef W4A16_TRACE
+    if (threadIdx.x == 0) {
+        W4G_TRACE(1, W4G_NOW());
+        unsigned smid_;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid_));
+        W4G_TRACE(56, smid_);
+    }
+#endif
     const int flags = info[0];
     const bool run = flags >= 0 && nkb > 0;
     const bool has_z = flags >= 0 && (flags & kFlagZeros) != 0;
@@ -157,6 +185,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 const int kc = (kb0 + i) * kTileK;
                 tma_tensor_2d_g2s(st, &tmap_a, kc, m0, fb, pol_a);
                 tma_tensor_2d_g2s(st + S::kABoxBytes, &tmap_a, kc + 64, m0, fb, pol_a);
+                W4G_TRACE(2 + (i < 16 ? i : 15), W4G_NOW());
                 ++issued;
             }
             if (issued < nkb || *abort_flag) {
@@ -183,6 +212,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 ok = mbar_wait_bounded(full0 + 8 * s, ph, abort_flag, args.status, tlim) &&
                      mbar_wait_bounded(tfull0 + 8 * t, tph, abort_flag, args.status, tlim);
                 if (!ok) break;
+                if (i < 6) W4G_TRACE(57 + i, W4G_NOW());
                 tc_fence_after();
                 const uint32_t st = base + static_cast<uint32_t>(s) * args.stage_bytes;
 #pragma unroll
@@ -195,6 +225,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 tc_commit(tempty0 + 8 * t);
             }
             tc_commit(accum_bar);
+            W4G_TRACE(50, W4G_NOW());
             if (!ok) {  // make sure no MMA is still reading TMEM/SMEM when the CTA exits
                 int dummy = 0;
                 (void)mbar_wait_bounded(accum_bar, 0, &dummy, nullptr, tlim);
@@ -213,6 +244,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             const int t = i % kTBuf;
             const uint32_t tph = static_cast<uint32_t>(i / kTBuf) & 1u;
             if (!mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim)) break;
+            if (warp == 2 && lane == 0 && i < 16) W4G_TRACE(18 + i, W4G_NOW());
             if (i >= kTBuf &&
                 !mbar_wait_warp(tempty0 + 8 * t, tph ^ 1u, abort_flag, args.status, tlim))
                 break;
@@ -237,10 +269,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tfull0 + 8 * t);
+            if (warp == 2 && lane == 0 && i < 16) W4G_TRACE(34 + i, W4G_NOW());
         }
 
         // ---------------- epilogue ----------------
         if (mbar_wait_warp(accum_bar, 0, abort_flag, args.status, tlim)) {
+            if (warp == 2 && lane == 0) W4G_TRACE(51, W4G_NOW());
             tc_fence_after();
             const int n = n_tile * kTileN + r;
             const float cs = cscale ? cscale[n] : 1.0f;
@@ -269,8 +303,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
 
     // ---------------- split-K reduction across the cluster ----------------
     __syncwarp();
+    if (warp == 2 && lane == 0) W4G_TRACE(52, W4G_NOW());
     if (args.splits > 1) {
         cluster_sync_all();
+        if (threadIdx.x == 0) W4G_TRACE(53, W4G_NOW());
         if (run && !*abort_flag) {
             const uint32_t rank = cluster_ctarank();
             const int S_ = args.splits;
@@ -292,8 +328,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 Y[static_cast<size_t>(m_tile * BM + ml) * args.N + n] = f32_to_dtype<DT>(acc);
             }
         }
+        if (threadIdx.x == 0) W4G_TRACE(54, W4G_NOW());
         cluster_sync_all();
     }
+    if (threadIdx.x == 0) W4G_TRACE(55, W4G_NOW());
 
     tc_fence_before();
     __syncthreads();
@@ -393,6 +431,18 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
 }
 
 }  // namespace
+
+#ifdef W4A16_TRACE
+extern "C" int w4a16_trace_read(void* host, size_t bytes) {
+    if (bytes > sizeof(g_w4a16_trace)) bytes = sizeof(g_w4a16_trace);
+    return cudaMemcpyFromSymbol(host, g_w4a16_trace, bytes) == cudaSuccess ? 0 : -3;
+}
+extern "C" int w4a16_trace_clear(void) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_w4a16_trace) != cudaSuccess) return -3;
+    return cudaMemset(p, 0, sizeof(g_w4a16_trace)) == cudaSuccess ? 0 : -3;
+}
+#endif
 
 uint32_t tc_stage_bytes(int tile_m, int group) {
     const uint32_t raw = static_cast<uint32_t>(tile_m) * 256u + block_bytes(group, true);
