@@ -68,12 +68,25 @@ typedef enum w4a16_kernel {
     W4A16_KERNEL_SIMT = 2   /* CUDA-core FMA GEMV, M <= 8                             */
 } w4a16_kernel;
 
+/* Flags for w4a16_gemm_config.flags. */
+/* Launch without programmatic dependent launch (the kernel then starts only after the
+ * previous work in the stream has finished). */
+#define W4A16_GEMM_NO_PDL 1
+/* Read the packed blob only after the previous kernel in the stream has finished.  By
+ * default the tensor-core kernel reads the blob header and its first weight stages
+ * while that kernel is still running (weights are static between repacks), and reads A
+ * and writes Y only after it has finished.  Set this flag if the kernel that runs right
+ * before the GEMM in the same stream writes the packed blob itself; w4a16_repack needs
+ * no flag (it ends with a launch that later kernels cannot overlap). */
+#define W4A16_GEMM_NO_WEIGHT_PREFETCH 2
+
 typedef struct w4a16_gemm_config {
     int kernel;       /* w4a16_kernel                                                   */
     int split_k;      /* 0 = heuristic; else 1..8 K-slices reduced inside a CTA cluster  */
     int tile_m;       /* 0 = heuristic; else 16, 32, 64, 128 or 256 rows of A per tile   */
     int stages;       /* 0 = heuristic; else shared-memory ring depth (2..16)            */
-    int reserved[4];  /* must be zero                                                   */
+    int flags;        /* W4A16_GEMM_* bits; 0 = defaults                                 */
+    int reserved[3];  /* must be zero                                                   */
 } w4a16_gemm_config;
 
 /* Library ABI version (W4A16_ABI_VERSION). */
@@ -141,7 +154,9 @@ int w4a16_gemm(const void* A, const void* packed, int M, int N, int K, int group
                void* Y, void* stream);
 
 /* Same as w4a16_gemm with explicit kernel/tiling choices (cfg may be NULL = AUTO).
- * Returns UNSUPPORTED for a combination the chosen kernel cannot run. */
+ * Returns UNSUPPORTED for a combination the chosen kernel cannot run.  w4a16_gemm is
+ * w4a16_gemm_ex with cfg = NULL: programmatic dependent launch and weight prefetch on
+ * (see W4A16_GEMM_NO_WEIGHT_PREFETCH for the one case that needs them off). */
 int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int group,
                   int dtype, void* Y, const w4a16_gemm_config* cfg, void* stream);
 

@@ -113,13 +113,47 @@ def test_gemm_small_auto(shape):
 
 
 @pytest.mark.parametrize("tile_m", [16, 32, 64, 128, 256])
-@pytest.mark.parametrize("split_k", [1, 2, 3, 8])
+@pytest.mark.parametrize("split_k", [1, 2, 3, 5, 8])
 def test_gemm_tc_tilings(tile_m, split_k):
     M = {16: 13, 32: 30, 64: 64, 128: 129, 256: 200}[tile_m]
     c = si.make_case(M, 256, 1024, 128, FP16, seed=tile_m + split_k)
     packed = repack_case(c)
+    if tile_m == 256 and split_k > 1:
+        # the split-K receive area of a 256-row tile does not fit beside its ring
+        with pytest.raises(w4.W4A16Error) as e:
+            run_gemm(c, packed, kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m, split_k=split_k)
+        assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
+        return
     Y = run_gemm(c, packed, kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m, split_k=split_k)
     assert_parity_full(c, Y)
+
+
+@pytest.mark.parametrize("flags", [0, w4.W4A16_GEMM_NO_PDL, w4.W4A16_GEMM_NO_WEIGHT_PREFETCH,
+                                   w4.W4A16_GEMM_NO_PDL | w4.W4A16_GEMM_NO_WEIGHT_PREFETCH])
+@pytest.mark.parametrize("split_k", [1, 4, 7])
+def test_gemm_tc_launch_flags(flags, split_k):
+    c = si.make_case(3, 384, 1792, 128, BF16, seed=flags + 10 * split_k)
+    packed = repack_case(c)
+    Y = run_gemm(c, packed, kernel=w4.W4A16_KERNEL_TC, split_k=split_k, flags=flags)
+    assert_parity_full(c, Y)
+
+
+def test_back_to_back_gemms_share_nothing():
+    """Consecutive launches overlap under programmatic dependent launch: the second
+    GEMM reads the first one's output as its A, so a missing dependency wait would
+    show up as a mismatch."""
+    c1 = si.make_case(4, 512, 512, 128, FP16, seed=31)
+    c2 = si.make_case(4, 256, 512, 128, FP16, seed=32)
+    p1, p2 = repack_case(c1), repack_case(c2)
+    A = to_dev(c1.A)
+    Y1 = torch.empty((4, 512), dtype=torch.int16, device="cuda")
+    Y2 = torch.empty((4, 256), dtype=torch.int16, device="cuda")
+    for _ in range(3):
+        w4.w4a16_gemm(A, p1, 4, 512, 512, 128, FP16, Y1)
+        w4.w4a16_gemm(Y1, p2, 4, 256, 512, 128, FP16, Y2)
+    assert w4.w4a16_get_device_status() == 0
+    c2.A = to_host_u16(Y1)
+    assert_parity_full(c2, to_host_u16(Y2))
 
 
 @pytest.mark.parametrize("stages", [2, 3, 5])

@@ -31,6 +31,9 @@ W4A16_KERNEL_AUTO = 0
 W4A16_KERNEL_TC = 1
 W4A16_KERNEL_SIMT = 2
 
+W4A16_GEMM_NO_PDL = 1
+W4A16_GEMM_NO_WEIGHT_PREFETCH = 2
+
 _lock = threading.Lock()
 _lib = None
 
@@ -43,7 +46,8 @@ class W4A16Error(RuntimeError):
 
 class GemmConfig(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("split_k", ctypes.c_int), ("tile_m", ctypes.c_int),
-                ("stages", ctypes.c_int), ("reserved", ctypes.c_int * 4)]
+                ("stages", ctypes.c_int), ("flags", ctypes.c_int),
+                ("reserved", ctypes.c_int * 3)]
 
 
 def lib() -> ctypes.CDLL:
@@ -138,8 +142,8 @@ def w4a16_gemm(A, packed, M: int, N: int, K: int, group: int, dtype: int, Y,
 
 def w4a16_gemm_ex(A, packed, M: int, N: int, K: int, group: int, dtype: int, Y, *,
                   kernel: int = W4A16_KERNEL_AUTO, split_k: int = 0, tile_m: int = 0,
-                  stages: int = 0, stream=None) -> None:
-    cfg = GemmConfig(kernel, split_k, tile_m, stages)
+                  stages: int = 0, flags: int = 0, stream=None) -> None:
+    cfg = GemmConfig(kernel, split_k, tile_m, stages, flags)
     _check(lib().w4a16_gemm_ex(_ptr(A), _ptr(packed), M, N, K, group, dtype, _ptr(Y),
                                ctypes.byref(cfg), _stream(stream)), "w4a16_gemm_ex")
 

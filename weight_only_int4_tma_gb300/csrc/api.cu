@@ -5,7 +5,7 @@
 #include <cstdlib>
 #include <mutex>
 
-#include "../../include/w4a16.h"
+#include "w4a16.h"
 #include "format.cuh"
 #include "launch.h"
 
@@ -67,10 +67,16 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
               const w4a16_gemm_config* cfg, GemmPlan* plan) {
     const int kernel = cfg ? cfg->kernel : W4A16_KERNEL_AUTO;
+    int flags = 0;
     if (cfg) {
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 3; ++i)
             if (cfg->reserved[i] != 0) return W4A16_ERR_INVALID_ARG;
+        if (cfg->flags & ~(W4A16_GEMM_NO_PDL | W4A16_GEMM_NO_WEIGHT_PREFETCH))
+            return W4A16_ERR_INVALID_ARG;
+        flags = cfg->flags;
     }
+    plan->pdl = (flags & W4A16_GEMM_NO_PDL) == 0;
+    plan->prefetch_weights = plan->pdl && (flags & W4A16_GEMM_NO_WEIGHT_PREFETCH) == 0;
     if (kernel == W4A16_KERNEL_SIMT) {
         if (M > 8) return W4A16_ERR_UNSUPPORTED;
         plan->kernel = W4A16_KERNEL_SIMT;
@@ -107,10 +113,12 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     if (split < 1 || split > 8 || split > kblocks) return W4A16_ERR_UNSUPPORTED;
 
     int stages = cfg && cfg->stages ? cfg->stages : 0;
-    const int smem_budget = occ == 2 ? 113 * 1024 : ctx.max_smem_optin;
-    const int max_st = tc_max_stages(bm, group, ctx.max_smem_optin);
+    // split-K receive area (fp32 partials of the other cluster ranks), outside the ring
+    const int recv = split > 1 ? split * bm * ceil_div(kTileN, split) * 4 : 0;
+    const int smem_budget = (occ == 2 ? 113 * 1024 : ctx.max_smem_optin) - recv;
+    const int max_st = tc_max_stages(bm, M, group, ctx.max_smem_optin - recv);
     if (stages == 0) {
-        stages = tc_max_stages(bm, group, smem_budget);
+        stages = tc_max_stages(bm, M, group, smem_budget);
         if (stages > 8) stages = 8;
     }
     if (stages < 2 || stages > max_st) return W4A16_ERR_UNSUPPORTED;

@@ -83,4 +83,39 @@ __device__ __forceinline__ void dequant_word(uint32_t x, uint32_t zp, uint32_t s
     out[3] = mul_pair<DT>(sub_pair<DT>(t3, zp), sp);
 }
 
+// fp16 only, two shifts fewer per word: the pairs at nibble positions (1,5) and (3,7)
+// are masked in place (0x00F000F0), which puts q in mantissa bits 4..7, i.e. the fp16
+// number 1024 + 16 q.  Then (1024 + 16q) - (1024 + 16z) = 16 (q - z) exactly, and
+// multiplying by s/16 rounds once to rn((q - z) s) -- provided s/16 is itself exact
+// (checked per group by the caller with f16_div16_exact()).
+__device__ __forceinline__ void dequant_word_f16_x16(uint32_t x, uint32_t zp, uint32_t sp,
+                                                     uint32_t zp16, uint32_t sp16,
+                                                     uint32_t* out) {
+    constexpr uint32_t kM = Magic<0>::kPair;
+    const uint32_t y = x >> 8;
+    const uint32_t t0 = lop3_and_or(x, 0x000F000Fu, kM);
+    const uint32_t t1 = lop3_and_or(x, 0x00F000F0u, kM);
+    const uint32_t t2 = lop3_and_or(y, 0x000F000Fu, kM);
+    const uint32_t t3 = lop3_and_or(y, 0x00F000F0u, kM);
+    out[0] = mul_pair<0>(sub_pair<0>(t0, zp), sp);
+    out[1] = mul_pair<0>(sub_pair<0>(t1, zp16), sp16);
+    out[2] = mul_pair<0>(sub_pair<0>(t2, zp), sp);
+    out[3] = mul_pair<0>(sub_pair<0>(t3, zp16), sp16);
+}
+
+// (1024 + 16 z) in both fp16 halves.
+__device__ __forceinline__ uint32_t zero_pair_x16(uint32_t z) {
+    return Magic<0>::kPair | ((z << 4) * 0x00010001u);
+}
+
+// s/16 in both halves (a power-of-two scaling: exact unless it leaves the normal range).
+__device__ __forceinline__ uint32_t scale_pair_div16(uint32_t sp) {
+    return mul_pair<0>(sp, 0x2C002C00u);  // x 0.0625
+}
+
+// True when s/16 * 16 == s bit for bit, i.e. the division by 16 lost nothing.
+__device__ __forceinline__ bool f16_div16_exact(uint32_t sp, uint32_t sp16) {
+    return mul_pair<0>(sp16, 0x4C004C00u) == sp;  // x 16
+}
+
 }  // namespace w4g

@@ -2,7 +2,7 @@
 //
 // One CTA computes a 128-channel x BM-row tile of Y^T = W . A^T over a K slice:
 //
-//   HBM --TMA bulk copy--> SMEM ring stage: [A tile BM x 128 (128B swizzle) | packed block]
+//   HBM --TMA bulk copy--> SMEM ring stage: [A tile (128B swizzle) | packed 128x128 block]
 //        (weights stream once, evict-first; "量化开销对比" §6.5; "W4A16 GEMM 算子浅析"
 //         §"计算流水线的核心哲学", the HBM -> SMEM step)
 //   SMEM --dequant warps: LOP3 magic-bias unpack, sub/mul per pair--> TMEM (A operand)
@@ -11,15 +11,21 @@
 //   tcgen05.mma.kind::f16 D[128 x BM] (fp32, TMEM) += W_tile[128 x 16] (TMEM) . A[BM x 16]^T
 //        (the FP16 x FP16 -> FP32 MMA of the pipeline diagram; weights are the 128-row M
 //         operand so that a decode batch of 1..16 tokens only pads the narrow N side)
-//   epilogue: tcgen05.ld -> (split-K: partials reduced over the CTA cluster through
-//        distributed shared memory) -> x per-channel factor -> round to dtype -> Y
-//        ("量化开销对比" §6.2 "最后：累加器 × s_x → +bias → 写出", §6.7 folding)
+//   epilogue: tcgen05.ld -> (split-K: each CTA of the cluster owns a slice of the 128
+//        channels; the others push their fp32 partials for it into its shared memory
+//        with bulk DSMEM copies; the owner sums them in rank order) -> x per-channel
+//        factor -> round to dtype -> Y  ("量化开销对比" §6.2 "最后：累加器 × s_x → +bias →
+//        写出", §6.7 folding)
 //
 // Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator + single-thread MMA issuer,
 // warps 2.. = dequant warps (4 per warpgroup; warp w may only touch TMEM lanes
 // 32*(w%4)..+31, so each warpgroup covers all 128 lanes) which also run the epilogue.
-// Every mbarrier wait is bounded; on expiry the CTA records a timeout, drains what it
-// issued and exits.
+//
+// Programmatic dependent launch: the prologue (barriers, TMEM, descriptor prefetch and,
+// unless disabled, the header check and the first ring stages of packed weights) runs
+// while the previous kernel in the stream finishes; A is read and Y written only after
+// griddepcontrol.wait.  Every mbarrier wait is bounded; on expiry the CTA records a
+// timeout, drains what it issued and exits.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -57,23 +63,37 @@ __device__ unsigned long long g_w4a16_trace[kTraceCtas * kTraceSlots];
 #define W4G_NOW() 0ull
 #endif
 
+#ifndef W4A16_SMALL_TILE_WG
+#define W4A16_SMALL_TILE_WG 2  // dequant warpgroups for 16- and 32-row tiles
+#endif
+
+constexpr int kFlagPrefetchW = 1;   // read header + first stages before the dependency wait
+
 struct TcArgs {
     const uint8_t* packed;
     void* Y;
     int* status;
     int M, N, K, group;
-    int kblocks;        // K / 128
-    int splits;         // K slices = cluster size along x
-    int stages;         // ring depth
+    int kblocks;          // K / 128
+    int splits;           // K slices = cluster size along x
+    int stages;           // ring depth
+    int a_rows;           // rows per A chunk in shared memory (8, 16 or BM)
+    int kps;              // 128-K blocks per ring stage (1 or 2)
+    int slice_rows;       // channels owned per cluster rank (ceil(128 / splits))
+    int flags;
     uint32_t stage_bytes;
+    uint32_t recv_off;    // offset of the split-K receive area from the ring base
     uint64_t timeout_ns;
 };
 
 template <int BM>
 struct TcShape {
-    static constexpr int kABoxBytes = BM * 128;            // BM rows x 64 K (128 bytes)
-    static constexpr int kATileBytes = 2 * kABoxBytes;     // 128 K per stage
-    static constexpr int kTBuf = BM >= 256 ? 2 : (BM >= 128 ? 2 : 3);  // TMEM W buffers
+    // MMA-issuing threads (one per warp).  A 128-row K=16 tcgen05.mma costs its issuing
+    // thread tens of cycles whatever N is, so narrow decode tiles (N = 16 or 32) split
+    // the blocks over two issuers, even blocks into accumulator 0, odd into 1.
+    static constexpr int kNMI = BM <= 32 ? 2 : 1;
+    static constexpr int kDq0 = 1 + kNMI;                  // first dequant warp
+    static constexpr int kTBuf = BM >= 128 ? 2 : 3;        // TMEM W buffers
     static constexpr int kACol0 = BM < 64 ? 64 : BM;       // first W staging column
     static constexpr int kColsUsed = kACol0 + kTBuf * 64;
     static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64
@@ -86,24 +106,35 @@ __device__ __forceinline__ uint16_t f32_to_dtype(float v) {
     else return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 template <int BM, int NWG, int DT>
-__global__ void __launch_bounds__(64 + 128 * NWG, 1)
+__global__ void __launch_bounds__(32 * (1 + TcShape<BM>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     using S = TcShape<BM>;
     constexpr int kTBuf = S::kTBuf;
+    constexpr uint32_t kEpiThreads = 128 * NWG;
+    constexpr int kNMI = S::kNMI;
+    static_assert(S::kACol0 >= kNMI * BM, "accumulators overlap the W staging columns");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
     const uint32_t ring_bytes = static_cast<uint32_t>(args.stages) * args.stage_bytes;
-    const uint32_t ctrl = base + ring_bytes;
-    uint8_t* ctrl_ptr = base_ptr + ring_bytes;
-    // control block: full[16] empty[16] tfull[4] tempty[4] accum, then scalars
+    const uint32_t ctrl_off = args.splits > 1
+        ? args.recv_off + static_cast<uint32_t>(args.splits * BM * args.slice_rows * 4)
+        : ring_bytes;
+    const uint32_t ctrl = base + ctrl_off;
+    uint8_t* ctrl_ptr = base_ptr + ctrl_off;
+    // control block: full[16] empty[16] tfull[4] tempty[4] accum recv, then scalars
     const uint32_t full0 = ctrl, empty0 = ctrl + 128, tfull0 = ctrl + 256, tempty0 = ctrl + 288;
     const uint32_t accum_bar = ctrl + 320;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl_ptr + 328);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl_ptr + 332);
-    int* info = reinterpret_cast<int*>(ctrl_ptr + 336);  // [0] flags or -1, [1] block bytes
+    const uint32_t recv_bar = ctrl + 328;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl_ptr + 336);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl_ptr + 340);
+    int* info = reinterpret_cast<int*>(ctrl_ptr + 344);  // [0] flags or -1, [1] block bytes
     const float** cs_slot = reinterpret_cast<const float**>(ctrl_ptr + 352);
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -114,9 +145,27 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const int kb_per = args.kblocks / args.splits, kb_rem = args.kblocks % args.splits;
     const int kb0 = split * kb_per + (split < kb_rem ? split : kb_rem);
     const int nkb = kb_per + (split < kb_rem ? 1 : 0);
+    const bool prefetch_w = (args.flags & kFlagPrefetchW) != 0;
+    const uint32_t slice_bytes = static_cast<uint32_t>(BM * args.slice_rows * 4);
 
     if (threadIdx.x == 0) {
         W4G_TRACE(0, W4G_NOW());
+        *abort_flag = 0;
+        for (int s = 0; s < args.stages; ++s) {
+            mbar_init(full0 + 8 * s, 1);
+            // a stage is free once every issuer that read it has committed
+            mbar_init(empty0 + 8 * s, (kNMI == 2 && args.kps == 2) ? 2 : 1);
+        }
+        for (int t = 0; t < kTBuf; ++t) {
+            mbar_init(tfull0 + 8 * t, 4 * NWG);
+            mbar_init(tempty0 + 8 * t, 1);
+        }
+        mbar_init(accum_bar, kNMI);
+        mbar_init(recv_bar, 1);
+        fence_mbar_init();
+        if (args.splits > 1)  // partials of the other ranks for this rank's slice
+            mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(args.splits - 1) * slice_bytes);
+        if (!prefetch_w) grid_dep_wait();
         const PackedHeader* h = reinterpret_cast<const PackedHeader*>(args.packed);
         const int flags = check_header(h, args.N, args.K, args.group, DT);
         info[0] = flags;
@@ -126,19 +175,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                        : nullptr;
         if (flags < 0 && split == 0 && n_tile == 0 && m_tile == 0)
             record_status(args.status, kStatusFormat);
-        *abort_flag = 0;
-        for (int s = 0; s < args.stages; ++s) {
-            mbar_init(full0 + 8 * s, 1);
-            mbar_init(empty0 + 8 * s, 1);
-        }
-        for (int t = 0; t < kTBuf; ++t) {
-            mbar_init(tfull0 + 8 * t, 4 * NWG);
-            mbar_init(tempty0 + 8 * t, 1);
-        }
-        mbar_init(accum_bar, 1);
-        fence_mbar_init();
+        prefetch_tensormap(&tmap_a);
     }
-    if (warp == 0 && lane == 0) prefetch_tensormap(&tmap_a);
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), S::kTmemCols);
         tmem_relinquish();
@@ -146,6 +184,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (args.splits > 1) cluster_arrive_release();  // peers may now target our barriers
+    if (threadIdx.x == 0) grid_dep_launch();
 
     const uint32_t tmem = *tmem_slot;
 #ifdef W4A16_TRACE
@@ -162,33 +202,59 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const uint32_t bb = static_cast<uint32_t>(info[1]);
     const float* cscale = *cs_slot;
     const uint64_t tlim = args.timeout_ns;
+    const int kps = args.kps;
+    const uint32_t a_chunk = static_cast<uint32_t>(args.a_rows) * 128u;   // one 64-K chunk of A
+    const uint32_t a_bytes = 2u * static_cast<uint32_t>(kps) * a_chunk;  // A part of a stage
+    const int nst = (nkb + kps - 1) / kps;                                // ring stages to stream
 
-    if (run && warp == 0) {
+    if (warp == 0) {
         // ---------------- TMA producer ----------------
-        if (lane == 0) {
+        if (lane == 0 && run) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_a = policy_evict_last();
             const uint8_t* src = args.packed + kHeaderBytes +
                                  (static_cast<size_t>(n_tile) * args.kblocks + kb0) * bb;
             const int m0 = m_tile * BM;
-            int issued = 0;
-            for (int i = 0; i < nkb; ++i) {
-                const int s = i % args.stages;
-                const uint32_t ph = static_cast<uint32_t>(i / args.stages) & 1u;
+            // stage i: blocks [i*kps, i*kps + nblk) as ONE bulk copy + ONE 3-D A box
+            const int pre = prefetch_w ? (nst < args.stages ? nst : args.stages) : 0;
+            for (int i = 0; i < pre; ++i) {  // weights do not depend on the previous grid
+                const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
+                const int nblk = min(kps, nkb - i * kps);
+                mbar_arrive_expect_tx(full0 + 8 * i, nblk * bb + a_bytes);
+                tma_bulk_g2s(st + a_bytes, src + static_cast<size_t>(i) * kps * bb, nblk * bb,
+                             full0 + 8 * i, pol_w);
+            }
+            if (prefetch_w) grid_dep_wait();
+            for (int i = 0; i < pre; ++i) {
+                const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
+                tma_tensor_3d_g2s(st, &tmap_a, 0, m0, (kb0 + i * kps) * 2, full0 + 8 * i, pol_a);
+                if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
+            }
+            int issued = pre;
+            int s = pre;              // ring slot of stage i, and the parity of its use
+            uint32_t ph = 0;
+            if (s == args.stages) { s = 0; ph = 1; }
+            const uint8_t* wsrc = src + static_cast<size_t>(pre) * kps * bb;
+            int kchunk = (kb0 + pre * kps) * 2;  // first 64-K chunk of A for stage i
+            int left = nkb - pre * kps;          // blocks not yet issued
+            for (int i = pre; i < nst; ++i) {
                 if (i >= args.stages &&
                     !mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, args.status, tlim))
                     break;
                 const uint32_t st = base + static_cast<uint32_t>(s) * args.stage_bytes;
                 const uint32_t fb = full0 + 8 * s;
-                mbar_arrive_expect_tx(fb, bb + S::kATileBytes);
-                tma_bulk_g2s(st + S::kATileBytes, src + static_cast<size_t>(i) * bb, bb, fb, pol_w);
-                const int kc = (kb0 + i) * kTileK;
-                tma_tensor_2d_g2s(st, &tmap_a, kc, m0, fb, pol_a);
-                tma_tensor_2d_g2s(st + S::kABoxBytes, &tmap_a, kc + 64, m0, fb, pol_a);
-                W4G_TRACE(2 + (i < 16 ? i : 15), W4G_NOW());
+                const int nblk = left < kps ? left : kps;
+                mbar_arrive_expect_tx(fb, nblk * bb + a_bytes);
+                tma_bulk_g2s(st + a_bytes, wsrc, nblk * bb, fb, pol_w);
+                tma_tensor_3d_g2s(st, &tmap_a, 0, m0, kchunk, fb, pol_a);
+                if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
                 ++issued;
+                left -= kps;
+                wsrc += static_cast<size_t>(kps) * bb;
+                kchunk += 2 * kps;
+                if (++s == args.stages) { s = 0; ph ^= 1u; }
             }
-            if (issued < nkb || *abort_flag) {
+            if (issued < nst || *abort_flag) {
                 // Drain: every issued copy must land before the CTA may exit.
                 const int first = issued > args.stages ? issued - args.stages : 0;
                 for (int i = first; i < issued; ++i) {
@@ -199,30 +265,53 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 }
             }
         }
-    } else if (run && warp == 1) {
-        // ---------------- MMA issuer (one thread) ----------------
-        if (lane == 0) {
+        __syncwarp();
+        if (args.splits > 1) cluster_wait_acquire();
+    } else if (warp <= kNMI) {
+        // ---------------- MMA issuers (one thread per warp) ----------------
+        const int k = warp - 1;  // issuer index: blocks k, k + kNMI, ...
+        if (lane == 0 && run) {
             constexpr uint32_t idesc = idesc_f16(DT, 128, BM);
+            // Descriptor of chunk c, 16-K step q of the A tile in a stage = descriptor of
+            // the stage base + (c * a_chunk + 32 q) / 16; only the start address moves.
+            const uint64_t chunk16 = a_chunk >> 4;
+            const uint32_t dacc = tmem + static_cast<uint32_t>(k * BM);  // this issuer's D
             bool ok = true;
-            for (int i = 0; i < nkb && ok; ++i) {
-                const int s = i % args.stages;
-                const uint32_t ph = static_cast<uint32_t>(i / args.stages) & 1u;
-                const int t = i % kTBuf;
-                const uint32_t tph = static_cast<uint32_t>(i / kTBuf) & 1u;
-                ok = mbar_wait_bounded(full0 + 8 * s, ph, abort_flag, args.status, tlim) &&
-                     mbar_wait_bounded(tfull0 + 8 * t, tph, abort_flag, args.status, tlim);
+            // kNMI == 2 implies two blocks per stage: issuer k owns block b = k of every
+            // stage, so the stage advances once per issued block.
+            int s = 0, b = kNMI == 2 ? k : 0, t = k;
+            uint32_t ph = 0, tph = 0;
+            for (int i = k; i < nkb; i += kNMI) {   // i: 128-K block
+                ok = ((kNMI == 1 && b != 0) ||
+                      mbar_wait_spin(full0 + 8 * s, ph, abort_flag, args.status, tlim)) &&
+                     mbar_wait_spin(tfull0 + 8 * t, tph, abort_flag, args.status, tlim);
                 if (!ok) break;
-                if (i < 6) W4G_TRACE(57 + i, W4G_NOW());
+                if (i < 8) W4G_TRACE(34 + i, W4G_NOW());
                 tc_fence_after();
-                const uint32_t st = base + static_cast<uint32_t>(s) * args.stage_bytes;
-#pragma unroll
-                for (int j = 0; j < kTileK / 16; ++j) {
-                    const uint32_t a_t = tmem + S::kACol0 + t * 64 + j * 8;
-                    const uint64_t bd = sw128_desc(st + (j >> 2) * S::kABoxBytes + (j & 3) * 32);
-                    tc_mma_ts(tmem, a_t, bd, idesc, (i | j) != 0 ? 1u : 0u);
-                }
-                tc_commit(empty0 + 8 * s);
+                const uint64_t d0 = sw128_desc(base + static_cast<uint32_t>(s) * args.stage_bytes) +
+                                    static_cast<uint64_t>(2 * b) * chunk16;
+                const uint64_t d1 = d0 + chunk16;
+                const uint32_t a0 = tmem + S::kACol0 + t * 64;
+                tc_mma_ts(dacc, a0, d0, idesc, i >= kNMI ? 1u : 0u);
+                tc_mma_ts(dacc, a0 + 8, d0 + 2, idesc, 1u);
+                tc_mma_ts(dacc, a0 + 16, d0 + 4, idesc, 1u);
+                tc_mma_ts(dacc, a0 + 24, d0 + 6, idesc, 1u);
+                tc_mma_ts(dacc, a0 + 32, d1, idesc, 1u);
+                tc_mma_ts(dacc, a0 + 40, d1 + 2, idesc, 1u);
+                tc_mma_ts(dacc, a0 + 48, d1 + 4, idesc, 1u);
+                tc_mma_ts(dacc, a0 + 56, d1 + 6, idesc, 1u);
                 tc_commit(tempty0 + 8 * t);
+                if (i < 8) W4G_TRACE(42 + i, W4G_NOW());
+                t += kNMI;
+                if (t >= kTBuf) { t -= kTBuf; tph ^= 1u; }
+                if (kNMI == 2) {
+                    tc_commit(empty0 + 8 * s);
+                    if (++s == args.stages) { s = 0; ph ^= 1u; }
+                } else if (++b == kps || i == nkb - 1) {
+                    tc_commit(empty0 + 8 * s);
+                    b = 0;
+                    if (++s == args.stages) { s = 0; ph ^= 1u; }
+                }
             }
             tc_commit(accum_bar);
             W4G_TRACE(50, W4G_NOW());
@@ -230,61 +319,105 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 int dummy = 0;
                 (void)mbar_wait_bounded(accum_bar, 0, &dummy, nullptr, tlim);
             }
+        } else if (lane == 0) {
+            tc_commit(accum_bar);  // no MMAs to track: arrive at once
         }
-    } else if (run) {
+        __syncwarp();
+        if (args.splits > 1) cluster_wait_acquire();
+    } else {
         // ---------------- dequant warps ----------------
         const int q = warp & 3;                 // TMEM lane quarter of this warp
-        const int wg = (warp - 2) >> 2;         // dequant warpgroup
+        const int wg = (warp - S::kDq0) >> 2;   // dequant warpgroup
         const int r = q * 32 + lane;            // weight row of the tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
         const uint32_t zoff = kNibbleBytes + scale_bytes(args.group);
-        for (int i = 0; i < nkb; ++i) {
-            const int s = i % args.stages;
-            const uint32_t ph = static_cast<uint32_t>(i / args.stages) & 1u;
-            const int t = i % kTBuf;
-            const uint32_t tph = static_cast<uint32_t>(i / kTBuf) & 1u;
-            if (!mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim)) break;
-            if (warp == 2 && lane == 0 && i < 16) W4G_TRACE(18 + i, W4G_NOW());
-            if (i >= kTBuf &&
-                !mbar_wait_warp(tempty0 + 8 * t, tph ^ 1u, abort_flag, args.status, tlim))
-                break;
-            const uint8_t* wb = base_ptr + static_cast<size_t>(s) * args.stage_bytes + S::kATileBytes;
+        bool ok = run;
+        const int gshift = args.group == 128 ? 2 : (args.group == 64 ? 1 : 0);  // chunk -> group
+        int s = 0, b = 0, t = 0;
+        uint32_t ph = 0, tph = 0;
+        const uint8_t* stage_ptr = base_ptr + a_bytes;
+        for (int i = 0; i < nkb && ok; ++i) {   // i: 128-K block
+            if (b == 0) ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
+            if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(10 + i, W4G_NOW());
+            if (ok && i >= kTBuf)
+                ok = mbar_wait_warp(tempty0 + 8 * t, tph ^ 1u, abort_flag, args.status, tlim);
+            if (!ok) break;
+            if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(18 + i, W4G_NOW());
+            const uint8_t* wb = stage_ptr + static_cast<size_t>(b) * bb;
+            int cur_g = -1;
+            uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
+            bool x16 = false;
 #pragma unroll
             for (int c = wg; c < 4; c += NWG) {
-                const int gi = (c * kChunkK) / args.group;
-                const uint32_t sbits =
-                    reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[gi * kTileN + r];
-                uint32_t z = 8;
-                if (has_z) z = (wb[zoff + gi * (kTileN / 2) + (r >> 1)] >> ((r & 1) * 4)) & 0xFu;
-                const uint32_t zp = zero_pair<DT>(z), sp = scale_pair(sbits);
+                const int gi = c >> gshift;
+                if (gi != cur_g) {  // per-(group, row) constants
+                    cur_g = gi;
+                    const uint32_t sbits =
+                        reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[gi * kTileN + r];
+                    uint32_t z = 8;
+                    if (has_z) z = (wb[zoff + gi * (kTileN / 2) + (r >> 1)] >> ((r & 1) * 4)) & 0xFu;
+                    zp = zero_pair<DT>(z);
+                    sp = scale_pair(sbits);
+                    if constexpr (DT == 0) {
+                        zp16 = zero_pair_x16(z);
+                        sp16 = scale_pair_div16(sp);
+                        x16 = __all_sync(0xffffffffu, f16_div16_exact(sp, sp16));
+                    }
+                }
                 const uint4 v = *reinterpret_cast<const uint4*>(wb + c * 2048 + r * 16);
                 uint32_t out[16];
-                dequant_word<DT>(v.x, zp, sp, out + 0);
-                dequant_word<DT>(v.y, zp, sp, out + 4);
-                dequant_word<DT>(v.z, zp, sp, out + 8);
-                dequant_word<DT>(v.w, zp, sp, out + 12);
+                if (DT == 0 && x16) {
+                    dequant_word_f16_x16(v.x, zp, sp, zp16, sp16, out + 0);
+                    dequant_word_f16_x16(v.y, zp, sp, zp16, sp16, out + 4);
+                    dequant_word_f16_x16(v.z, zp, sp, zp16, sp16, out + 8);
+                    dequant_word_f16_x16(v.w, zp, sp, zp16, sp16, out + 12);
+                } else {
+                    dequant_word<DT>(v.x, zp, sp, out + 0);
+                    dequant_word<DT>(v.y, zp, sp, out + 4);
+                    dequant_word<DT>(v.z, zp, sp, out + 8);
+                    dequant_word<DT>(v.w, zp, sp, out + 12);
+                }
                 tmem_st16(tmem + lane_base + S::kACol0 + t * 64 + c * 16, out);
             }
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tfull0 + 8 * t);
-            if (warp == 2 && lane == 0 && i < 16) W4G_TRACE(34 + i, W4G_NOW());
+            if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(26 + i, W4G_NOW());
+            if (++t == kTBuf) { t = 0; tph ^= 1u; }
+            if (++b == kps) {
+                b = 0;
+                stage_ptr += args.stage_bytes;
+                if (++s == args.stages) { s = 0; ph ^= 1u; stage_ptr = base_ptr + a_bytes; }
+            }
         }
 
         // ---------------- epilogue ----------------
-        if (mbar_wait_warp(accum_bar, 0, abort_flag, args.status, tlim)) {
-            if (warp == 2 && lane == 0) W4G_TRACE(51, W4G_NOW());
+        const int R = args.slice_rows;
+        float* part = reinterpret_cast<float*>(base_ptr);  // [slice][BM][R] when split
+        ok = ok && mbar_wait_warp(accum_bar, 0, abort_flag, args.status, tlim);
+        if (ok) {
+            if (warp == S::kDq0 && lane == 0) W4G_TRACE(51, W4G_NOW());
             tc_fence_after();
             const int n = n_tile * kTileN + r;
-            const float cs = cscale ? cscale[n] : 1.0f;
             uint16_t* Y = static_cast<uint16_t*>(args.Y);
-            float* part = reinterpret_cast<float*>(base_ptr);  // [BM][128] when split
+            if (args.splits == 1) grid_dep_wait();  // Y may still be in use upstream
+            const float cs = (args.splits == 1 && cscale) ? cscale[n] : 1.0f;
+            const int pslice = r / R, prow = r - pslice * R;
 #pragma unroll 1
             for (int e = wg; e < BM / 16; e += NWG) {
                 uint32_t v[16];
                 tmem_ld16(tmem + lane_base + e * 16, v);
-                tmem_wait_ld();
+                if (kNMI == 2 && nkb > 1) {  // add the odd-block accumulator
+                    uint32_t v1[16];
+                    tmem_ld16(tmem + lane_base + BM + e * 16, v1);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __uint_as_float(v1[j]));
+                } else {
+                    tmem_wait_ld();
+                }
                 if (args.splits == 1) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
@@ -295,41 +428,57 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     }
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) part[(e * 16 + j) * kTileN + r] = __uint_as_float(v[j]);
+                    for (int j = 0; j < 16; ++j)
+                        part[(pslice * BM + e * 16 + j) * R + prow] = __uint_as_float(v[j]);
                 }
             }
         }
-    }
-
-    // ---------------- split-K reduction across the cluster ----------------
-    __syncwarp();
-    if (warp == 2 && lane == 0) W4G_TRACE(52, W4G_NOW());
-    if (args.splits > 1) {
-        cluster_sync_all();
-        if (threadIdx.x == 0) W4G_TRACE(53, W4G_NOW());
-        if (run && !*abort_flag) {
+        if (warp == S::kDq0 && lane == 0) W4G_TRACE(52, W4G_NOW());
+        if (args.splits > 1) {
+            // Push our partial of every other rank's slice into that rank's receive area.
+            fence_proxy_async_smem();
+            named_bar_sync(1, kEpiThreads);
+            cluster_wait_acquire();  // every peer has initialised its receive barrier
             const uint32_t rank = cluster_ctarank();
-            const int S_ = args.splits;
-            const int rows_per = (kTileN + S_ - 1) / S_;
-            const int r0 = static_cast<int>(rank) * rows_per;
-            const int r1 = min(kTileN, r0 + rows_per);
-            const int nr = r1 - r0;
-            const int mvalid = min(BM, args.M - m_tile * BM);
-            uint16_t* Y = static_cast<uint16_t*>(args.Y);
-            for (int e = static_cast<int>(threadIdx.x); nr > 0 && e < nr * mvalid;
-                 e += static_cast<int>(blockDim.x)) {
-                const int ml = e / nr;
-                const int rl = r0 + e % nr;
-                const uint32_t off = base + static_cast<uint32_t>((ml * kTileN + rl) * 4);
-                float acc = 0.0f;
-                for (int p = 0; p < S_; ++p) acc += ld_dsmem_f32(map_to_rank(off, p));
-                const int n = n_tile * kTileN + rl;
-                if (cscale) acc *= cscale[n];
-                Y[static_cast<size_t>(m_tile * BM + ml) * args.N + n] = f32_to_dtype<DT>(acc);
+            if (warp == S::kDq0 && lane == 0) {
+                W4G_TRACE(53, W4G_NOW());
+                const uint32_t recv = base + args.recv_off;
+                for (int p = 0; p < args.splits; ++p) {
+                    if (p == static_cast<int>(rank)) continue;
+                    const uint32_t src = base + static_cast<uint32_t>(p) * slice_bytes;
+                    const uint32_t dst = map_to_rank(recv + rank * slice_bytes, p);
+                    bulk_s2cluster(dst, src, slice_bytes, map_to_rank(recv_bar, p));
+                }
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+            // Sum this rank's slice over all ranks, in rank order, and store it.
+            const bool got = mbar_wait_warp(recv_bar, 0, abort_flag, args.status, tlim);
+            if (ok && got) {
+                if (warp == S::kDq0 && lane == 0) W4G_TRACE(54, W4G_NOW());
+                grid_dep_wait();
+                const int r0 = static_cast<int>(rank) * R;
+                const int nr = min(kTileN, r0 + R) - r0;
+                const int mvalid = min(BM, args.M - m_tile * BM);
+                const float* recvp = reinterpret_cast<const float*>(base_ptr + args.recv_off);
+                uint16_t* Y = static_cast<uint16_t*>(args.Y);
+                const int tid = static_cast<int>(threadIdx.x) - 32 * S::kDq0;
+                for (int e = tid; nr > 0 && e < nr * mvalid; e += static_cast<int>(kEpiThreads)) {
+                    const int ml = e / nr;
+                    const int j = e - ml * nr;
+                    float acc = 0.0f;
+                    for (int p = 0; p < args.splits; ++p) {
+                        const float* src = p == static_cast<int>(rank)
+                                               ? part + (static_cast<int>(rank) * BM + ml) * R
+                                               : recvp + (p * BM + ml) * R;
+                        acc += src[j];
+                    }
+                    const int n = n_tile * kTileN + r0 + j;
+                    if (cscale) acc *= cscale[n];
+                    Y[static_cast<size_t>(m_tile * BM + ml) * args.N + n] = f32_to_dtype<DT>(acc);
+                }
             }
         }
-        if (threadIdx.x == 0) W4G_TRACE(54, W4G_NOW());
-        cluster_sync_all();
     }
     if (threadIdx.x == 0) W4G_TRACE(55, W4G_NOW());
 
@@ -368,13 +517,17 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
                        int K, int group, void* Y, const GemmPlan& plan, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return -3;
+    const int a_rows = tc_a_rows(BM, M);
+    const int kps = tc_blocks_per_stage(BM);
+    // A viewed as [K/64][M][64]: one box = 2*kps chunks of 64 K x a_rows rows, landing in
+    // shared memory chunk-major, each chunk a run of 128-byte-swizzled 8-row atoms.
     CUtensorMap map;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(BM)};
-    const cuuint32_t estr[2] = {1, 1};
+    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(a_rows), static_cast<cuuint32_t>(2 * kps)};
+    const cuuint32_t estr[3] = {1, 1, 1};
     CUresult cr = enc(&map, DT == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      2, const_cast<void*>(A), dims, strides, box, estr,
+                      3, const_cast<void*>(A), dims, strides, box, estr,
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (cr != CUDA_SUCCESS) return -3;
@@ -390,10 +543,20 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     args.kblocks = K / kTileK;
     args.splits = plan.split_k;
     args.stages = plan.stages;
-    args.stage_bytes = tc_stage_bytes(BM, group);
+    args.a_rows = a_rows;
+    args.kps = kps;
+    args.slice_rows = (kTileN + plan.split_k - 1) / plan.split_k;
+    args.flags = plan.prefetch_weights ? kFlagPrefetchW : 0;
+    args.stage_bytes = tc_stage_bytes(BM, M, group);
+    const uint32_t ring = static_cast<uint32_t>(plan.stages) * args.stage_bytes;
+    const uint32_t recv_bytes = plan.split_k > 1
+        ? static_cast<uint32_t>(plan.split_k * BM * args.slice_rows * 4) : 0u;
+    if (plan.split_k > 1 && recv_bytes > ring) return -2;  // partials are staged in the ring
+    args.recv_off = ring;
     args.timeout_ns = ctx.timeout_ns;
 
-    const size_t smem = static_cast<size_t>(plan.stages) * args.stage_bytes + kCtrlBytes + 1024;
+    const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;
+    if (smem > static_cast<size_t>(ctx.max_smem_optin)) return -2;
     auto kern = w4a16_tc_kernel<BM, NWG, DT>;
     {   // raise the dynamic shared-memory limit once per device (not a stream operation,
         // but kept out of the steady state so that launches can be graph-captured cheaply)
@@ -412,17 +575,22 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.split_k), static_cast<unsigned>(N / kTileN),
                        static_cast<unsigned>((M + BM - 1) / BM));
-    cfg.blockDim = dim3(64 + 128 * NWG, 1, 1);
+    cfg.blockDim = dim3(32 * TcShape<BM>::kDq0 + 128 * NWG, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     int nattr = 0;
     if (plan.split_k > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = static_cast<unsigned>(plan.split_k);
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        nattr = 1;
+        attr[nattr].id = cudaLaunchAttributeClusterDimension;
+        attr[nattr].val.clusterDim.x = static_cast<unsigned>(plan.split_k);
+        attr[nattr].val.clusterDim.y = 1;
+        attr[nattr].val.clusterDim.z = 1;
+        ++nattr;
+    }
+    if (plan.pdl) {
+        attr[nattr].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[nattr].val.programmaticStreamSerializationAllowed = 1;
+        ++nattr;
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
@@ -444,14 +612,23 @@ extern "C" int w4a16_trace_clear(void) {
 }
 #endif
 
-uint32_t tc_stage_bytes(int tile_m, int group) {
-    const uint32_t raw = static_cast<uint32_t>(tile_m) * 256u + block_bytes(group, true);
+int tc_a_rows(int tile_m, int M) {
+    if (tile_m > 16) return tile_m;
+    return M <= 8 ? 8 : 16;  // rows past M are zero-filled by the TMA
+}
+
+int tc_blocks_per_stage(int tile_m) { return tile_m <= 32 ? 2 : 1; }
+
+uint32_t tc_stage_bytes(int tile_m, int M, int group) {
+    const int kps = tc_blocks_per_stage(tile_m);
+    const uint32_t raw = static_cast<uint32_t>(2 * kps * tc_a_rows(tile_m, M)) * 128u +
+                         static_cast<uint32_t>(kps) * block_bytes(group, true);
     return (raw + 1023u) & ~1023u;
 }
 
-int tc_max_stages(int tile_m, int group, int smem_budget) {
+int tc_max_stages(int tile_m, int M, int group, int smem_budget) {
     const int avail = smem_budget - kCtrlBytes - 1024;
-    int s = avail / static_cast<int>(tc_stage_bytes(tile_m, group));
+    int s = avail / static_cast<int>(tc_stage_bytes(tile_m, M, group));
     return s > kMaxStages ? kMaxStages : s;
 }
 
@@ -466,8 +643,8 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
                    : launch_tc_instance<BMV, NWGV, 1>(ctx, A, packed, M, N, K, group, Y, \
                                                       plan, stream);
     switch (plan.tile_m) {
-        W4G_TC_CASE(16, 2)
-        W4G_TC_CASE(32, 2)
+        W4G_TC_CASE(16, W4A16_SMALL_TILE_WG)
+        W4G_TC_CASE(32, W4A16_SMALL_TILE_WG)
         W4G_TC_CASE(64, 2)
         W4G_TC_CASE(128, 2)
         W4G_TC_CASE(256, 1)

@@ -20,6 +20,8 @@ struct GemmPlan {
     int tile_m;   // activation rows per tile (tcgen05 kernel)
     int split_k;  // K slices (cluster size for the tcgen05 kernel)
     int stages;   // shared-memory ring depth
+    bool pdl;               // launch with programmatic dependent launch
+    bool prefetch_weights;  // read the packed blob before the dependency wait
 };
 
 // Launchers return a w4a16_status code.
@@ -40,9 +42,13 @@ int launch_simt_gemm(const DeviceCtx& ctx, const void* A, const void* packed, in
 
 int launch_timeout_probe(const DeviceCtx& ctx, uint64_t limit_ns, cudaStream_t stream);
 
+// Rows of A staged per 64-K chunk (8 or 16 for decode tiles, else the tile height).
+int tc_a_rows(int tile_m, int M);
+// 128-K weight blocks per ring stage (one bulk copy each stage).
+int tc_blocks_per_stage(int tile_m);
 // Bytes of one stage of the tcgen05 ring for a tile of `tile_m` activation rows.
-uint32_t tc_stage_bytes(int tile_m, int group);
+uint32_t tc_stage_bytes(int tile_m, int M, int group);
 // Largest ring depth that fits `smem_budget` bytes of dynamic shared memory.
-int tc_max_stages(int tile_m, int group, int smem_budget);
+int tc_max_stages(int tile_m, int M, int group, int smem_budget);
 
 }  // namespace w4g

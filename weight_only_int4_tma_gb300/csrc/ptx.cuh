@@ -62,16 +62,32 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Same, but the thread may sleep in hardware (up to kSuspendNs) until the phase
+// completes, instead of re-issuing the test: waiting warps then take no issue slots.
+constexpr uint32_t kSuspendNs = 20000;
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity), "n"(kSuspendNs)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete.  Gives up when the
 // CTA-wide abort flag is raised or after `limit_ns` of wall time; the first waiter to
 // time out raises the abort flag and records kStatusTimeout.  Returns true on success.
+template <bool kSleep>
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                             volatile int* abort_flag, int* status,
                                             uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0u) {
+        if (kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return true;
+        if ((it & 3u) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
@@ -86,7 +102,15 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, int* status,
                                                   uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity, abort_flag, status, limit_ns);
+    return mbar_wait_slow<true>(bar, parity, abort_flag, status, limit_ns);
+}
+
+// Same bound, but never sleeps: for the single latency-critical MMA-issuing thread.
+__device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
+                                               volatile int* abort_flag, int* status,
+                                               uint64_t limit_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow<false>(bar, parity, abort_flag, status, limit_ns);
 }
 
 // Warp-uniform form: every lane waits, and the warp proceeds only if all lanes succeeded,
@@ -130,6 +154,18 @@ __device__ __forceinline__ void tma_tensor_2d_g2s(uint32_t dst, const CUtensorMa
         ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;"
         ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar),
           "l"(policy)
+        : "memory");
+}
+
+// 3-D tiled tensor copy global -> shared; coordinates {c0 (innermost), c1, c2}.
+__device__ __forceinline__ void tma_tensor_3d_g2s(uint32_t dst, const CUtensorMap* map,
+                                                  int c0, int c1, int c2, uint32_t bar,
+                                                  uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2),
+          "r"(bar), "l"(policy)
         : "memory");
 }
 
@@ -243,6 +279,38 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t caddr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(caddr) : "memory");
     return v;
+}
+
+// Cluster barrier in two halves, so that the arrive can be issued early and the wait
+// late (all threads of every CTA of the cluster take part in both).
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Generic-proxy shared-memory writes -> visible to the async proxy (TMA / bulk copies).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Bulk copy from this CTA's shared memory into a peer CTA's shared memory; completes
+// `bytes` of transaction count on the peer's mbarrier (both cluster addresses).
+__device__ __forceinline__ void bulk_s2cluster(uint32_t dst_cluster, uint32_t src_cta,
+                                               uint32_t bytes, uint32_t bar_cluster) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes"
+        " [%0], [%1], %2, [%3];"
+        ::"r"(dst_cluster), "r"(src_cta), "r"(bytes), "r"(bar_cluster)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Wait until the source side of every committed bulk copy has been read.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // ---- programmatic dependent launch ---------------------------------------------------

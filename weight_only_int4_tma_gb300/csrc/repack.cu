@@ -130,6 +130,12 @@ __global__ void __launch_bounds__(512) dequant_debug_kernel(const uint8_t* __res
         dst[i] = make_uint4(out[4 * i], out[4 * i + 1], out[4 * i + 2], out[4 * i + 3]);
 }
 
+// Launched (without programmatic dependent launch) right after the repack: a GEMM that
+// follows in the stream may start early only relative to this kernel, which itself
+// starts after the repack has completed, so the GEMM's early reads of the packed blob
+// always see the finished blob.
+__global__ void repack_fence_kernel() {}
+
 // Failure-path check: one CTA waits on an mbarrier that nothing arrives on.
 __global__ void timeout_probe_kernel(int* status, uint64_t limit_ns) {
     __shared__ __align__(8) uint64_t bar;
@@ -161,6 +167,8 @@ int launch_repack(const DeviceCtx& ctx, const uint32_t* qweight, const void* sca
         qweight, static_cast<const uint16_t*>(scales), qzeros,
         static_cast<const uint16_t*>(cscale), N, K, group, dtype,
         static_cast<uint8_t*>(packed), bb, cs_off, total);
+    if (cudaGetLastError() != cudaSuccess) return -3;
+    repack_fence_kernel<<<1, 32, 0, stream>>>();
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
 
