@@ -88,27 +88,36 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     if (kernel != W4A16_KERNEL_AUTO && kernel != W4A16_KERNEL_TC) return W4A16_ERR_INVALID_ARG;
     plan->kernel = W4A16_KERNEL_TC;
 
+    const int n_tiles = N / kTileN;
+    const int kblocks = K / kTileK;
     int bm = cfg && cfg->tile_m ? cfg->tile_m : 0;
     if (bm == 0) {
         if (M <= 16) bm = 16;
         else if (M <= 32) bm = 32;
         else if (M <= 64) bm = 64;
+        else if (M >= 256 && n_tiles * ceil_div(M, 256) >= ctx.num_sms) bm = 256;
         else bm = 128;
     }
     if (bm != 16 && bm != 32 && bm != 64 && bm != 128 && bm != 256) return W4A16_ERR_UNSUPPORTED;
     const int m_tiles = ceil_div(M, bm);
     if (m_tiles > 65535) return W4A16_ERR_UNSUPPORTED;
-    const int kblocks = K / kTileK;
-    const int occ = bm <= 64 ? 2 : 1;  // CTAs per SM the ring depth below is sized for
+    const int base = n_tiles * m_tiles;
+    // CTAs per SM the ring is sized for: decode tiles always pair up; 128-row tiles pair
+    // up (2-stage rings) when there are enough tiles to fill two per SM.
+    const int occ = bm <= 64 ? 2 : (bm == 128 && base >= 2 * ctx.num_sms ? 2 : 1);
 
     int split = cfg && cfg->split_k ? cfg->split_k : 0;
     if (split == 0) {
-        const int base = (N / kTileN) * m_tiles;
         const int slots = ctx.num_sms * occ;
         split = base >= slots ? 1 : slots / base;
         if (split > 8) split = 8;
         if (split > kblocks) split = kblocks;
         if (split < 1) split = 1;
+        // the split-K receive area must leave room for a ring of at least two stages
+        while (split > 1 &&
+               tc_max_stages(bm, M, group, ctx.max_smem_optin -
+                             split * bm * ceil_div(kTileN, split) * 4) < 2)
+            --split;
     }
     if (split < 1 || split > 8 || split > kblocks) return W4A16_ERR_UNSUPPORTED;
 

@@ -63,6 +63,9 @@ __device__ unsigned long long g_w4a16_trace[kTraceCtas * kTraceSlots];
 #define W4G_NOW() 0ull
 #endif
 
+#ifndef W4A16_BIG_TILE_WG
+#define W4A16_BIG_TILE_WG 2    // dequant warpgroups for 256-row tiles
+#endif
 #ifndef W4A16_SMALL_TILE_WG
 #define W4A16_SMALL_TILE_WG 2  // dequant warpgroups for 16- and 32-row tiles
 #endif
@@ -647,7 +650,7 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
         W4G_TC_CASE(32, W4A16_SMALL_TILE_WG)
         W4G_TC_CASE(64, 2)
         W4G_TC_CASE(128, 2)
-        W4G_TC_CASE(256, 1)
+        W4G_TC_CASE(256, W4A16_BIG_TILE_WG)
         default:
             return -2;
     }
