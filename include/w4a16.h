@@ -63,9 +63,9 @@ typedef enum w4a16_dtype {
 
 /* Kernel selection for w4a16_gemm_ex (w4a16_gemm always uses W4A16_KERNEL_AUTO). */
 typedef enum w4a16_kernel {
-    W4A16_KERNEL_AUTO = 0,  /* choose by M                                            */
+    W4A16_KERNEL_AUTO = 0,  /* M == 1 and K <= 16384: SIMT; otherwise TC               */
     W4A16_KERNEL_TC = 1,    /* TMA ring -> dequant warps -> tcgen05.mma (swap-AB)      */
-    W4A16_KERNEL_SIMT = 2   /* CUDA-core FMA GEMV, M <= 8                             */
+    W4A16_KERNEL_SIMT = 2   /* CUDA-core FMA GEMV (cp.async ring), M <= 8              */
 } w4a16_kernel;
 
 /* Flags for w4a16_gemm_config.flags. */
@@ -81,10 +81,14 @@ typedef enum w4a16_kernel {
 #define W4A16_GEMM_NO_WEIGHT_PREFETCH 2
 
 typedef struct w4a16_gemm_config {
-    int kernel;       /* w4a16_kernel                                                   */
-    int split_k;      /* 0 = heuristic; else 1..8 K-slices reduced inside a CTA cluster  */
-    int tile_m;       /* 0 = heuristic; else 16, 32, 64, 128 or 256 rows of A per tile   */
-    int stages;       /* 0 = heuristic; else shared-memory ring depth (2..16)            */
+    int kernel;       /* w4a16_kernel; AUTO picks SIMT only if the three fields below
+                         are all 0                                                       */
+    int split_k;      /* TC: 0 = heuristic; else 1..8 K-slices reduced inside a CTA
+                         cluster.  SIMT: 0 or 1                                          */
+    int tile_m;       /* TC: 0 = heuristic; else 16, 32, 64, 128 or 256 rows of A per
+                         tile.  SIMT: 0, 16 or 32 output channels per work unit          */
+    int stages;       /* TC: 0 = heuristic; else shared-memory ring depth (2..16).
+                         SIMT: must be 0 (fixed 4-stage cp.async ring)                   */
     int flags;        /* W4A16_GEMM_* bits; 0 = defaults                                 */
     int reserved[3];  /* must be zero                                                   */
 } w4a16_gemm_config;
@@ -159,6 +163,16 @@ int w4a16_gemm(const void* A, const void* packed, int M, int N, int K, int group
  * (see W4A16_GEMM_NO_WEIGHT_PREFETCH for the one case that needs them off). */
 int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int group,
                   int dtype, void* Y, const w4a16_gemm_config* cfg, void* stream);
+
+/*
+ * The kernel and tiling that w4a16_gemm_ex(..., cfg, ...) would launch for this shape on
+ * the current device (cfg may be NULL = AUTO), written to *out with every field resolved
+ * (kernel TC or SIMT; split_k, tile_m, stages as used; flags as applied).  Host-side
+ * only: launches nothing, reads no device memory.  Errors: INVALID_ARG (M < 1, out NULL,
+ * bad cfg fields), UNSUPPORTED, CUDA (no usable device).
+ */
+int w4a16_gemm_plan(int M, int N, int K, int group, int dtype, const w4a16_gemm_config* cfg,
+                    w4a16_gemm_config* out);
 
 /*
  * Debug / parity only: expand the packed blob to dtype W_out[N][K] (row-major, device)

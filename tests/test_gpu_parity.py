@@ -173,6 +173,42 @@ def test_gemm_simt(M, dtype):
     assert_parity_full(c, Y)
 
 
+# CUDA-core GEMV work split: units of 16 or 32 channels over a persistent grid (several
+# units per CTA once N / rows exceeds the CTAs that fit), K blocks dealt to 8 or 16 slots
+# (ragged and idle slots when K / 128 is not a multiple), 1, 2 or 4 groups per block.
+SIMT_SPLITS = [
+    # (M, N, K, group, dtype, asym, rows)
+    (1, 8192, 1024, 128, FP16, True, 16),    # 512 units > resident CTAs: 2 per CTA
+    (1, 12288, 640, 64, BF16, True, 32),     # 384 units; 5 blocks over 8 slots
+    (2, 8192, 384, 32, FP16, False, 16),     # 3 blocks over 16 slots, symmetric
+    (1, 256, 2944, 32, BF16, True, 16),      # 23 blocks: uneven slots, odd counts
+    (3, 6016, 1152, 64, FP16, True, 32),     # 47 tiles' worth of rows, 9 blocks
+]
+
+
+@pytest.mark.parametrize("shape", SIMT_SPLITS, ids=lambda s: "M{}_N{}_K{}_g{}_{}{}_r{}".format(
+    s[0], s[1], s[2], s[3], "bf16" if s[4] else "fp16", "" if s[5] else "_sym", s[6]))
+def test_gemm_simt_work_split(shape):
+    M, N, K, g, dt, asym, rows = shape
+    c = si.make_case(M, N, K, g, dt, seed=N + K, asym=asym)
+    packed = repack_case(c)
+    Y = run_gemm(c, packed, kernel=w4.W4A16_KERNEL_SIMT, tile_m=rows)
+    assert_parity_sampled(c, Y, count=6000, seed=rows)
+
+
+def test_auto_routes_single_row_by_k():
+    """M == 1 goes to the GEMV up to K = 16384 and to the tensor-core kernel beyond; both
+    routes agree with the oracle."""
+    for K in (16384, 16512):
+        c = si.make_case(1, 256, K, 128, FP16, seed=K)
+        packed = repack_case(c)
+        assert_parity_full(c, run_gemm(c, packed))
+    with pytest.raises(w4.W4A16Error) as e:  # the GEMV has no ring depth or split to set
+        c = si.make_case(1, 256, 512, 128, FP16, seed=1)
+        run_gemm(c, repack_case(c), kernel=w4.W4A16_KERNEL_SIMT, stages=3)
+    assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
+
+
 @pytest.mark.parametrize("kernel", [w4.W4A16_KERNEL_TC, w4.W4A16_KERNEL_SIMT])
 def test_channel_scale(kernel):
     c = si.make_case(4, 256, 512, 128, BF16, seed=3, channel_scale=(0.25, 4.0))

@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
             L.w4a16_gemm.restype = I
             L.w4a16_gemm_ex.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(GemmConfig), P]
             L.w4a16_gemm_ex.restype = I
+            L.w4a16_gemm_plan.argtypes = [I, I, I, I, I, ctypes.POINTER(GemmConfig),
+                                          ctypes.POINTER(GemmConfig)]
+            L.w4a16_gemm_plan.restype = I
             L.w4a16_dequant_debug.argtypes = [P, I, I, I, I, P, P]
             L.w4a16_dequant_debug.restype = I
             L.w4a16_get_device_status.argtypes = [P]
@@ -146,6 +149,18 @@ def w4a16_gemm_ex(A, packed, M: int, N: int, K: int, group: int, dtype: int, Y, 
     cfg = GemmConfig(kernel, split_k, tile_m, stages, flags)
     _check(lib().w4a16_gemm_ex(_ptr(A), _ptr(packed), M, N, K, group, dtype, _ptr(Y),
                                ctypes.byref(cfg), _stream(stream)), "w4a16_gemm_ex")
+
+
+def w4a16_gemm_plan(M: int, N: int, K: int, group: int, dtype: int, *,
+                    kernel: int = W4A16_KERNEL_AUTO, split_k: int = 0, tile_m: int = 0,
+                    stages: int = 0, flags: int = 0) -> dict:
+    """The resolved launch choice of w4a16_gemm_ex for these arguments (no launch)."""
+    cfg = GemmConfig(kernel, split_k, tile_m, stages, flags)
+    out = GemmConfig()
+    _check(lib().w4a16_gemm_plan(M, N, K, group, dtype, ctypes.byref(cfg), ctypes.byref(out)),
+           "w4a16_gemm_plan")
+    return {"kernel": out.kernel, "split_k": out.split_k, "tile_m": out.tile_m,
+            "stages": out.stages, "flags": out.flags}
 
 
 def w4a16_dequant_debug(packed, N: int, K: int, group: int, dtype: int, W_out,

@@ -66,7 +66,13 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 // Kernel / tiling choice for a GEMM.
 int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
               const w4a16_gemm_config* cfg, GemmPlan* plan) {
-    const int kernel = cfg ? cfg->kernel : W4A16_KERNEL_AUTO;
+    int kernel = cfg ? cfg->kernel : W4A16_KERNEL_AUTO;
+    // Single-row decode with K up to 16384: the CUDA-core GEMV beats the tensor-core
+    // kernel there (the MMA's fixed issue cost and the TMEM round trip of the unpacked
+    // tile dominate at one row); longer K favours the tensor-core kernel's split-K.
+    if (kernel == W4A16_KERNEL_AUTO && M == 1 && K <= 16384 &&
+        !(cfg && (cfg->tile_m || cfg->split_k || cfg->stages)))
+        kernel = W4A16_KERNEL_SIMT;
     int flags = 0;
     if (cfg) {
         for (int i = 0; i < 3; ++i)
@@ -79,8 +85,12 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     plan->prefetch_weights = plan->pdl && (flags & W4A16_GEMM_NO_WEIGHT_PREFETCH) == 0;
     if (kernel == W4A16_KERNEL_SIMT) {
         if (M > 8) return W4A16_ERR_UNSUPPORTED;
+        if (cfg && (cfg->split_k > 1 || cfg->stages != 0)) return W4A16_ERR_UNSUPPORTED;
+        int rows = cfg && cfg->tile_m ? cfg->tile_m : 0;
+        if (rows == 0) rows = 16;  // channels per unit (measured best or equal everywhere)
+        if (rows != 16 && rows != 32) return W4A16_ERR_UNSUPPORTED;
         plan->kernel = W4A16_KERNEL_SIMT;
-        plan->tile_m = 0;
+        plan->tile_m = rows;
         plan->split_k = 1;
         plan->stages = 0;
         return W4A16_OK;
@@ -126,11 +136,13 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     const int recv = split > 1 ? split * bm * ceil_div(kTileN, split) * 4 : 0;
     const int smem_budget = (occ == 2 ? 113 * 1024 : ctx.max_smem_optin) - recv;
     const int max_st = tc_max_stages(bm, M, group, ctx.max_smem_optin - recv);
+    const int mult = tc_stage_multiple(bm);
     if (stages == 0) {
         stages = tc_max_stages(bm, M, group, smem_budget);
         if (stages > 8) stages = 8;
+        stages -= stages % mult;
     }
-    if (stages < 2 || stages > max_st) return W4A16_ERR_UNSUPPORTED;
+    if (stages < 2 || stages > max_st || stages % mult != 0) return W4A16_ERR_UNSUPPORTED;
     plan->tile_m = bm;
     plan->split_k = split;
     plan->stages = stages;
@@ -198,6 +210,26 @@ int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int gr
     if (plan.kernel == W4A16_KERNEL_SIMT)
         return launch_simt_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, s);
     return launch_tc_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, s);
+}
+
+int w4a16_gemm_plan(int M, int N, int K, int group, int dtype, const w4a16_gemm_config* cfg,
+                    w4a16_gemm_config* out) {
+    if (M < 1 || !out) return W4A16_ERR_INVALID_ARG;
+    int rc = check_shape(N, K, group, dtype);
+    if (rc != W4A16_OK) return rc;
+    const DeviceCtx* ctx = nullptr;
+    if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
+    GemmPlan plan{};
+    if ((rc = make_plan(*ctx, M, N, K, group, cfg, &plan)) != W4A16_OK) return rc;
+    w4a16_gemm_config r{};
+    r.kernel = plan.kernel;
+    r.split_k = plan.split_k;
+    r.tile_m = plan.tile_m;
+    r.stages = plan.stages;
+    r.flags = (plan.pdl ? 0 : W4A16_GEMM_NO_PDL) |
+              (plan.prefetch_weights ? 0 : W4A16_GEMM_NO_WEIGHT_PREFETCH);
+    *out = r;
+    return W4A16_OK;
 }
 
 int w4a16_gemm(const void* A, const void* packed, int M, int N, int K, int group, int dtype,

@@ -96,6 +96,10 @@ struct TcShape {
     // the blocks over two issuers, even blocks into accumulator 0, odd into 1.
     static constexpr int kNMI = BM <= 32 ? 2 : 1;
     static constexpr int kDq0 = 1 + kNMI;                  // first dequant warp
+    // Decode tiles: each dequant warpgroup unpacks whole blocks (wg, wg + NWG, ...).
+    // Larger tiles: every warpgroup takes its chunks of every block, so that each block
+    // is ready sooner for the longer MMAs.
+    static constexpr bool kInterleave = BM <= 32;
     static constexpr int kTBuf = BM >= 128 ? 2 : 3;        // TMEM W buffers
     static constexpr int kACol0 = BM < 64 ? 64 : BM;       // first W staging column
     static constexpr int kColsUsed = kACol0 + kTBuf * 64;
@@ -121,6 +125,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     constexpr uint32_t kEpiThreads = 128 * NWG;
     constexpr int kNMI = S::kNMI;
     static_assert(S::kACol0 >= kNMI * BM, "accumulators overlap the W staging columns");
+    static_assert(kNMI * kTBuf <= 8 && NWG * kTBuf <= 16, "control block barrier slots");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -131,14 +136,15 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         : ring_bytes;
     const uint32_t ctrl = base + ctrl_off;
     uint8_t* ctrl_ptr = base_ptr + ctrl_off;
-    // control block: full[16] empty[16] tfull[4] tempty[4] accum recv, then scalars
-    const uint32_t full0 = ctrl, empty0 = ctrl + 128, tfull0 = ctrl + 256, tempty0 = ctrl + 288;
-    const uint32_t accum_bar = ctrl + 320;
-    const uint32_t recv_bar = ctrl + 328;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl_ptr + 336);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl_ptr + 340);
-    int* info = reinterpret_cast<int*>(ctrl_ptr + 344);  // [0] flags or -1, [1] block bytes
-    const float** cs_slot = reinterpret_cast<const float**>(ctrl_ptr + 352);
+    // control block: full[16] empty[16] tfull[issuer][W buffer] (8)
+    // tempty[warpgroup][W buffer] (16) accum recv, then scalars
+    const uint32_t full0 = ctrl, empty0 = ctrl + 128, tfull0 = ctrl + 256, tempty0 = ctrl + 320;
+    const uint32_t accum_bar = ctrl + 448;
+    const uint32_t recv_bar = ctrl + 456;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl_ptr + 464);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctrl_ptr + 468);
+    int* info = reinterpret_cast<int*>(ctrl_ptr + 472);  // [0] flags or -1, [1] block bytes
+    const float** cs_slot = reinterpret_cast<const float**>(ctrl_ptr + 480);
 
     const int warp = static_cast<int>(threadIdx.x >> 5);
     const int lane = static_cast<int>(threadIdx.x & 31);
@@ -159,10 +165,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             // a stage is free once every issuer that read it has committed
             mbar_init(empty0 + 8 * s, (kNMI == 2 && args.kps == 2) ? 2 : 1);
         }
-        for (int t = 0; t < kTBuf; ++t) {
-            mbar_init(tfull0 + 8 * t, 4 * NWG);
-            mbar_init(tempty0 + 8 * t, 1);
-        }
+        for (int t = 0; t < kNMI * kTBuf; ++t)  // the warps that write a block's W tile
+            mbar_init(tfull0 + 8 * t, S::kInterleave ? 4 : 4 * NWG);
+        for (int t = 0; t < NWG * kTBuf; ++t)
+            mbar_init(tempty0 + 8 * t, 1);  // one MMA commit
         mbar_init(accum_bar, kNMI);
         mbar_init(recv_bar, 1);
         fence_mbar_init();
@@ -283,11 +289,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             // kNMI == 2 implies two blocks per stage: issuer k owns block b = k of every
             // stage, so the stage advances once per issued block.
             int s = 0, b = kNMI == 2 ? k : 0, t = k;
-            uint32_t ph = 0, tph = 0;
+            uint32_t ph = 0;
+            uint32_t fpar = 0;  // bit t: parity of this issuer's next wait on tfull[k][t]
             for (int i = k; i < nkb; i += kNMI) {   // i: 128-K block
-                ok = ((kNMI == 1 && b != 0) ||
-                      mbar_wait_spin(full0 + 8 * s, ph, abort_flag, args.status, tlim)) &&
-                     mbar_wait_spin(tfull0 + 8 * t, tph, abort_flag, args.status, tlim);
+                ok = (kNMI == 1 && b != 0) ||
+                     mbar_wait_spin(full0 + 8 * s, ph, abort_flag, args.status, tlim);
+                ok = ok && mbar_wait_spin(tfull0 + 8 * (k * kTBuf + t), (fpar >> t) & 1u,
+                                          abort_flag, args.status, tlim);
+                fpar ^= 1u << t;
                 if (!ok) break;
                 if (i < 8) W4G_TRACE(34 + i, W4G_NOW());
                 tc_fence_after();
@@ -303,10 +312,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 tc_mma_ts(dacc, a0 + 40, d1 + 2, idesc, 1u);
                 tc_mma_ts(dacc, a0 + 48, d1 + 4, idesc, 1u);
                 tc_mma_ts(dacc, a0 + 56, d1 + 6, idesc, 1u);
-                tc_commit(tempty0 + 8 * t);
+                // the W buffer is free for its next block, i + kTBuf (unpacked by warpgroup
+                // (i + kTBuf) % NWG when warpgroups take whole blocks, else by all)
+                tc_commit(tempty0 + 8 * ((S::kInterleave ? (i + kTBuf) % NWG : 0) * kTBuf + t));
                 if (i < 8) W4G_TRACE(42 + i, W4G_NOW());
                 t += kNMI;
-                if (t >= kTBuf) { t -= kTBuf; tph ^= 1u; }
+                if (t >= kTBuf) t -= kTBuf;
                 if (kNMI == 2) {
                     tc_commit(empty0 + 8 * s);
                     if (++s == args.stages) { s = 0; ph ^= 1u; }
@@ -336,22 +347,57 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         const uint32_t zoff = kNibbleBytes + scale_bytes(args.group);
         bool ok = run;
         const int gshift = args.group == 128 ? 2 : (args.group == 64 ? 1 : 0);  // chunk -> group
-        int s = 0, b = 0, t = 0;
-        uint32_t ph = 0, tph = 0;
-        const uint8_t* stage_ptr = base_ptr + a_bytes;
-        for (int i = 0; i < nkb && ok; ++i) {   // i: 128-K block
-            if (b == 0) ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
+        // Decode tiles: warpgroup wg unpacks whole 128-K blocks wg, wg + NWG, ..., so one
+        // group's TMEM stores drain while another unpacks.  Larger tiles: every warpgroup
+        // unpacks chunks wg, wg + NWG, ... of every block.  A parity wait is only
+        // meaningful for the current or the immediately preceding phase of an mbarrier,
+        // so every barrier has a single waiting party that takes part in each of its
+        // phases: issuer k waits on tfull[k][t] (its own blocks in W buffer t), warpgroup
+        // w on tempty[w][t] (the MMA of the block before its own next use of buffer t;
+        // one shared party when all groups unpack every block), and each warpgroup passes
+        // every phase of the ring slots it reads (the host keeps the ring depth a
+        // multiple of NWG / blocks-per-stage when groups take whole blocks).
+        constexpr int kBStep = S::kInterleave ? NWG : 1;         // block stride of a group
+        constexpr int kCpw = S::kInterleave ? 4 : (4 + NWG - 1) / NWG;  // chunks per block
+        const int tw = S::kInterleave ? wg : 0;                  // tempty party
+        int cur_p = 0, s = 0;   // a ring stage, its slot and the parity of that use
+        uint32_t ph = 0;
+        bool waited = false;    // stage cur_p's full barrier already passed
+        int b = 0, t = 0;       // block i's place in its stage, its W buffer
+        uint32_t epar = 0;      // bit t: parity of this warp's next wait on tempty[tw][t]
+        for (int i = S::kInterleave ? wg : 0; i < nkb && ok; i += kBStep) {   // 128-K block
+            if constexpr (S::kInterleave) {
+                const int p = args.kps == 2 ? (i >> 1) : i;  // ring stage of block i
+                b = i - p * args.kps;
+                t = i % kTBuf;
+                if (p != cur_p || !waited) {
+                    while (cur_p < p) {
+                        ++cur_p;
+                        if (++s == args.stages) { s = 0; ph ^= 1u; }
+                    }
+                    ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
+                    waited = true;
+                }
+            } else if (b == 0) {  // every block, in order: (s, b, t) advance at the loop end
+                ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
+            }
             if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(10 + i, W4G_NOW());
-            if (ok && i >= kTBuf)
-                ok = mbar_wait_warp(tempty0 + 8 * t, tph ^ 1u, abort_flag, args.status, tlim);
+            if (ok && i >= kTBuf) {
+                ok = mbar_wait_warp(tempty0 + 8 * (tw * kTBuf + t), (epar >> t) & 1u, abort_flag,
+                                    args.status, tlim);
+                epar ^= 1u << t;
+            }
             if (!ok) break;
             if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(18 + i, W4G_NOW());
-            const uint8_t* wb = stage_ptr + static_cast<size_t>(b) * bb;
+            const uint8_t* wb = base_ptr + a_bytes + static_cast<size_t>(s) * args.stage_bytes +
+                                static_cast<size_t>(b) * bb;
             int cur_g = -1;
             uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
             bool x16 = false;
 #pragma unroll
-            for (int c = wg; c < 4; c += NWG) {
+            for (int j = 0; j < kCpw; ++j) {
+                const int c = S::kInterleave ? j : wg + j * NWG;  // 32-K chunk
+                if (!S::kInterleave && c >= 4) break;
                 const int gi = c >> gshift;
                 if (gi != cur_g) {  // per-(group, row) constants
                     cur_g = gi;
@@ -385,13 +431,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tfull0 + 8 * t);
+            if (lane == 0) mbar_arrive(tfull0 + 8 * ((i % kNMI) * kTBuf + t));
             if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(26 + i, W4G_NOW());
-            if (++t == kTBuf) { t = 0; tph ^= 1u; }
-            if (++b == kps) {
-                b = 0;
-                stage_ptr += args.stage_bytes;
-                if (++s == args.stages) { s = 0; ph ^= 1u; stage_ptr = base_ptr + a_bytes; }
+            if constexpr (!S::kInterleave) {
+                if (++t == kTBuf) t = 0;
+                if (++b == args.kps) {
+                    b = 0;
+                    if (++s == args.stages) { s = 0; ph ^= 1u; }
+                }
             }
         }
 
@@ -627,6 +674,13 @@ uint32_t tc_stage_bytes(int tile_m, int M, int group) {
     const uint32_t raw = static_cast<uint32_t>(2 * kps * tc_a_rows(tile_m, M)) * 128u +
                          static_cast<uint32_t>(kps) * block_bytes(group, true);
     return (raw + 1023u) & ~1023u;
+}
+
+int tc_stage_multiple(int tile_m) {
+    if (tile_m > 32) return 1;  // every warpgroup reads every stage
+    const int nwg = W4A16_SMALL_TILE_WG;
+    const int kps = tc_blocks_per_stage(tile_m);
+    return nwg > kps ? nwg / kps : 1;
 }
 
 int tc_max_stages(int tile_m, int M, int group, int smem_budget) {

@@ -17,7 +17,7 @@ struct DeviceCtx {
 
 struct GemmPlan {
     int kernel;   // 1 = tcgen05, 2 = SIMT
-    int tile_m;   // activation rows per tile (tcgen05 kernel)
+    int tile_m;   // activation rows per tile (tcgen05 kernel); channels per unit (SIMT)
     int split_k;  // K slices (cluster size for the tcgen05 kernel)
     int stages;   // shared-memory ring depth
     bool pdl;               // launch with programmatic dependent launch
@@ -48,6 +48,9 @@ int tc_a_rows(int tile_m, int M);
 int tc_blocks_per_stage(int tile_m);
 // Bytes of one stage of the tcgen05 ring for a tile of `tile_m` activation rows.
 uint32_t tc_stage_bytes(int tile_m, int M, int group);
+// The ring depth must be a multiple of this (each dequant warpgroup then reads a fixed
+// subset of the ring slots and passes every phase of their barriers).
+int tc_stage_multiple(int tile_m);
 // Largest ring depth that fits `smem_budget` bytes of dynamic shared memory.
 int tc_max_stages(int tile_m, int M, int group, int smem_budget);
 

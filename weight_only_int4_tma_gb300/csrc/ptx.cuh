@@ -4,6 +4,10 @@
 #include <cstdint>
 #include <cuda.h>
 
+#ifndef W4A16_SPIN_MODE
+#define W4A16_SPIN_MODE 0  // MMA issuers: 0 = try_wait, 2 = test_wait polling
+#endif
+
 namespace w4g {
 
 // ---- status word -----------------------------------------------------------------
@@ -30,6 +34,29 @@ __device__ __forceinline__ uint32_t lane_id() {
     uint32_t l;
     asm volatile("mov.u32 %0, %%laneid;" : "=r"(l));
     return l;
+}
+
+// ---- explicit shared-memory loads (32-bit shared addresses) -------------------------
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u16(uint32_t a) {
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t lds_u8(uint32_t a) {
+    uint32_t v;
+    asm volatile("ld.shared.u8 %0, [%1];" : "=r"(v) : "r"(a));
+    return v;
 }
 
 // ---- mbarrier ----------------------------------------------------------------------
@@ -62,6 +89,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test: returns at once (no hardware suspension window).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Same, but the thread may sleep in hardware (up to kSuspendNs) until the phase
 // completes, instead of re-issuing the test: waiting warps then take no issue slots.
 constexpr uint32_t kSuspendNs = 20000;
@@ -80,14 +120,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
 // Bounded wait for the phase with the given parity to complete.  Gives up when the
 // CTA-wide abort flag is raised or after `limit_ns` of wall time; the first waiter to
 // time out raises the abort flag and records kStatusTimeout.  Returns true on success.
-template <bool kSleep>
+template <int kMode>  // 0: try_wait, 1: try_wait with sleep hint, 2: test_wait polling
 static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity,
                                             volatile int* abort_flag, int* status,
                                             uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (kSleep ? mbar_try_wait_sleep(bar, parity) : mbar_try_wait(bar, parity)) return true;
-        if ((it & 3u) == 0u) {
+        const bool done = kMode == 1 ? mbar_try_wait_sleep(bar, parity)
+                        : kMode == 2 ? mbar_test_wait(bar, parity)
+                                     : mbar_try_wait(bar, parity);
+        if (done) return true;
+        if ((it & (kMode == 2 ? 255u : 3u)) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > limit_ns) {
                 *abort_flag = 1;
@@ -98,19 +141,22 @@ static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity
     }
 }
 
+#ifndef W4A16_WAIT_MODE
+#define W4A16_WAIT_MODE 1  // other waiters: 1 = try_wait with a sleep hint, 2 = test_wait polling
+#endif
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort_flag, int* status,
                                                   uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow<true>(bar, parity, abort_flag, status, limit_ns);
+    return mbar_wait_slow<W4A16_WAIT_MODE>(bar, parity, abort_flag, status, limit_ns);
 }
 
-// Same bound, but never sleeps: for the single latency-critical MMA-issuing thread.
+// Same bound, but never sleeps: for the latency-critical MMA-issuing threads.
 __device__ __forceinline__ bool mbar_wait_spin(uint32_t bar, uint32_t parity,
                                                volatile int* abort_flag, int* status,
                                                uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_slow<false>(bar, parity, abort_flag, status, limit_ns);
+    return mbar_wait_slow<W4A16_SPIN_MODE>(bar, parity, abort_flag, status, limit_ns);
 }
 
 // Warp-uniform form: every lane waits, and the warp proceeds only if all lanes succeeded,
