@@ -1,0 +1,191 @@
+"""Model check of the tensor-core kernel's mbarrier protocol on the CPU.
+
+The kernel's warps wait on mbarriers with parity waits, which only distinguish the
+current phase from the one before it.  This discrete-event model replays the kernel's
+protocol (producer, MMA issuers, dequant warpgroups, asynchronous copy and MMA
+completions with random latencies; one issuer's MMAs complete in order, the two
+issuers' independently) and flags any wait whose intended phase is not the barrier's
+current or immediately preceding phase, and any deadlock.
+
+Layout modelled (as in csrc/gemm_tc.cu): ring slots full[s] / empty[s]; W buffers t
+with tfull[issuer][t] (count: the warps that write the tile) and
+tempty[warpgroup][t] (one MMA commit).  Decode tiles: warpgroup w unpacks blocks
+w, w + NWG, ...; larger tiles: every warpgroup unpacks every block.
+"""
+import heapq
+import itertools
+import random
+
+import pytest
+
+
+class Bar:
+    def __init__(self, count):
+        self.count = count
+        self.pending = count
+        self.ph = 0  # completed phases
+
+    def arrive(self):
+        self.pending -= 1
+        assert self.pending >= 0
+        if self.pending == 0:
+            self.ph += 1
+            self.pending = self.count
+
+
+def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
+    nst = (nkb + kps - 1) // kps
+    full = [Bar(1) for _ in range(S)]
+    empty = [Bar(2 if (kNMI == 2 and kps == 2) else 1) for _ in range(S)]
+    n_tparty = kNMI if per_party else 1
+    n_eparty = (NWG if interleave else 1) if per_party else 1
+    tfull = [[Bar(4 if interleave else 4 * NWG) for _ in range(T)] for _ in range(n_tparty)]
+    tempty = [[Bar(1) for _ in range(T)] for _ in range(n_eparty)]
+    events, cnt, errors = [], itertools.count(), []
+
+    def at(t, f):
+        heapq.heappush(events, (t, next(cnt), f))
+
+    def producer():
+        for p in range(nst):
+            if p >= S:
+                yield ("wait", empty[p % S], p // S - 1)
+            yield ("async", rng.uniform(0.2, 3.0), full[p % S])
+
+    mma_free = [0.0] * kNMI  # MMAs of one issuer complete in order; issuers independently
+
+    def issuer(k):
+        seen = [0] * T
+        last_p = -1
+        for i in range(k, nkb, kNMI):
+            p = i // kps
+            if p != last_p:
+                yield ("wait", full[p % S], p // S)
+                last_p = p
+            t = i % T
+            party = k if per_party else 0
+            q = seen[t] if per_party else i // T
+            yield ("wait", tfull[party][t], q)
+            seen[t] += 1
+            yield ("delay", rng.uniform(0.01, 0.1))
+            yield ("mma", k, i, p, kNMI == 2 or i % kps == kps - 1 or i == nkb - 1)
+
+    def warp(w):
+        seen = [0] * T
+        last_p = -1
+        blocks = range(w, nkb, NWG) if interleave else range(nkb)
+        for i in blocks:
+            p = i // kps
+            if p != last_p:
+                yield ("wait", full[p % S], p // S)
+                last_p = p
+            t = i % T
+            if i >= T:
+                party = (w if interleave else 0) if per_party else 0
+                q = seen[t] if per_party else i // T - 1
+                yield ("wait", tempty[party][t], q)
+                seen[t] += 1
+            yield ("delay", rng.uniform(0.05, 0.8))
+            yield ("arrive", tfull[(i % kNMI) if per_party else 0][t])
+
+    agents = [producer()] + [issuer(k) for k in range(kNMI)]
+    agents += [warp(w) for w in range(NWG) for _ in range(4)]
+    waiting, finished = {}, set()
+
+    def wake(now):
+        for ai, (bar, q) in list(waiting.items()):
+            if bar.ph > q:
+                del waiting[ai]
+                at(now, lambda n, ai=ai: step(ai, n))
+
+    def step(ai, now):
+        g = agents[ai]
+        while True:
+            try:
+                act = next(g)
+            except StopIteration:
+                finished.add(ai)
+                return
+            kind = act[0]
+            if kind == "wait":
+                bar, q = act[1], act[2]
+                if not (bar.ph - 1 <= q <= bar.ph):
+                    errors.append(f"parity alias: wants phase {q}, barrier at {bar.ph}")
+                    finished.add(ai)
+                    return
+                if bar.ph > q:
+                    continue
+                waiting[ai] = (bar, q)
+                return
+            if kind == "delay":
+                at(now + act[1], lambda n, ai=ai: step(ai, n))
+                return
+            if kind == "arrive":
+                act[1].arrive()
+                wake(now)
+                continue
+            if kind == "async":
+                bar = act[2]
+                at(now + act[1], lambda n, bar=bar: (bar.arrive(), wake(n)))
+                continue
+            if kind == "mma":
+                k, i, p, release = act[1], act[2], act[3], act[4]
+                fin = max(now, mma_free[k]) + rng.uniform(0.05, 0.8)
+                mma_free[k] = fin
+
+                def done(n, i=i, p=p, release=release):
+                    party = ((i + T) % NWG if interleave else 0) if per_party else 0
+                    tempty[party][i % T].arrive()
+                    if release:
+                        empty[p % S].arrive()
+                    wake(n)
+                at(fin, done)
+                continue
+
+    for ai in range(len(agents)):
+        at(rng.uniform(0, 0.5), lambda n, ai=ai: step(ai, n))
+    while events and not errors:
+        _, _, f = heapq.heappop(events)
+        f(_)
+    if errors:
+        return errors[0]
+    if len(finished) != len(agents) or waiting:
+        return "deadlock"
+    return None
+
+
+def configs(interleave):
+    for kNMI, kps in ((2, 2), (1, 1), (1, 2)):
+        for T in (2, 3):
+            for NWG in (1, 2, 4):
+                for S in (2, 3, 4, 5, 6):
+                    # host rule: with whole blocks per group, the ring depth is a multiple
+                    # of groups per stage
+                    if interleave and NWG > kps and S % (NWG // kps):
+                        continue
+                    for nkb in (1, 2, 3, 5, 7, 11, 16):
+                        yield kNMI, NWG, T, kps, S, nkb
+
+
+@pytest.mark.parametrize("interleave", [True, False], ids=["whole_blocks", "all_chunks"])
+def test_per_party_barriers_never_alias_or_deadlock(interleave):
+    bad = []
+    for cfg in configs(interleave):
+        for trial in range(4):
+            rng = random.Random(hash((cfg, trial, interleave)))
+            e = simulate(*cfg, rng, interleave)
+            if e:
+                bad.append((cfg, e))
+                break
+    assert not bad, bad[:3]
+
+
+def test_model_catches_a_ring_depth_that_breaks_the_rule():
+    """Sensitivity of the model: four warpgroups taking whole blocks, one block per stage,
+    and a ring depth (3 or 2) that is not a multiple of 4: each group skips phases of
+    slots it shares with the others; the host forbids those depths, and the model must
+    flag them."""
+    for S in (3, 2):
+        hits = sum(1 for trial in range(20)
+                   if simulate(1, 4, 2, 1, S, 16, random.Random(trial), interleave=True))
+        assert hits > 0, S

@@ -196,9 +196,19 @@ def test_gemm_simt_work_split(shape):
     assert_parity_sampled(c, Y, count=6000, seed=rows)
 
 
-def test_auto_routes_single_row_by_k():
-    """M == 1 goes to the GEMV up to K = 16384 and to the tensor-core kernel beyond; both
-    routes agree with the oracle."""
+def test_auto_routes_single_row():
+    """M == 1 goes to the GEMV up to K = 16384 (and one 128-channel tile per SM at most),
+    otherwise to the tensor-core kernel; both routes agree with the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = lambda M, N, K: w4.w4a16_gemm_plan(M, N, K, 128, FP16)["kernel"]
+    assert plan(1, 256, 16384) == w4.W4A16_KERNEL_SIMT
+    assert plan(1, 256, 16512) == w4.W4A16_KERNEL_TC
+    assert plan(1, 128 * sms, 4096) == w4.W4A16_KERNEL_SIMT
+    assert plan(1, 128 * (sms + 1), 4096) == w4.W4A16_KERNEL_TC
+    assert plan(2, 256, 4096) == w4.W4A16_KERNEL_TC
+    # between one and two decode tiles per SM: two K slices balance the SMs
+    p = w4.w4a16_gemm_plan(8, 128 * (sms + 8), 8192, 128, BF16)
+    assert (p["kernel"], p["tile_m"], p["split_k"]) == (w4.W4A16_KERNEL_TC, 16, 2)
     for K in (16384, 16512):
         c = si.make_case(1, 256, K, 128, FP16, seed=K)
         packed = repack_case(c)

@@ -67,10 +67,11 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
               const w4a16_gemm_config* cfg, GemmPlan* plan) {
     int kernel = cfg ? cfg->kernel : W4A16_KERNEL_AUTO;
-    // Single-row decode with K up to 16384: the CUDA-core GEMV beats the tensor-core
-    // kernel there (the MMA's fixed issue cost and the TMEM round trip of the unpacked
-    // tile dominate at one row); longer K favours the tensor-core kernel's split-K.
-    if (kernel == W4A16_KERNEL_AUTO && M == 1 && K <= 16384 &&
+    // Single-row decode with K up to 16384 and at most one 128-channel tile per SM: the
+    // CUDA-core GEMV beats the tensor-core kernel there (the MMA's fixed issue cost and
+    // the TMEM round trip of the unpacked tile dominate at one row, and the GEMV needs no
+    // split-K reduction); longer K or more tiles favour the tensor-core kernel.
+    if (kernel == W4A16_KERNEL_AUTO && M == 1 && K <= 16384 && N / kTileN <= ctx.num_sms &&
         !(cfg && (cfg->tile_m || cfg->split_k || cfg->stages)))
         kernel = W4A16_KERNEL_SIMT;
     int flags = 0;
@@ -119,7 +120,13 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     int split = cfg && cfg->split_k ? cfg->split_k : 0;
     if (split == 0) {
         const int slots = ctx.num_sms * occ;
-        split = base >= slots ? 1 : slots / base;
+        if (base >= slots) split = 1;
+        // 16-row tiles, more tiles than SMs but fewer than slots: one wave would give
+        // some SMs two tiles and others one; two half-length waves balance the SMs
+        // (measured: 37.7 vs 44.2 us at N = 28672, K = 8192; with 32-row tiles the
+        // receive area costs a ring stage and the split loses).
+        else if (bm == 16 && base > ctx.num_sms) split = 2;
+        else split = slots / base;
         if (split > 8) split = 8;
         if (split > kblocks) split = kblocks;
         if (split < 1) split = 1;
