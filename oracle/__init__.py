@@ -82,6 +82,8 @@ def _load():
         lib.w4o_gemm_sampled.restype = i32
         lib.w4o_check.argtypes = [P, P, P, i64, i32, f64, P, P]
         lib.w4o_check.restype = i64
+        lib.w4o_epilogue.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P]
+        lib.w4o_epilogue.restype = i32
         _lib = lib
         return lib
 
@@ -186,6 +188,27 @@ def gemm_sampled(A, qweight, scales, qzeros, M: int, N: int, K: int, group: int,
                                   _ptr(yr))
     assert rc == 0, rc
     return yd, bb, yr
+
+
+ACT_NONE, ACT_RELU, ACT_SILU = 0, 1, 2
+
+
+def epilogue(Yd, Babs, bias, residual, act: int, M: int, N: int, dtype: int):
+    """Fused epilogue on the GEMM's fp64 result: out = act(Yd + bias[n]) + residual[m, n].
+    Returns (out fp64 [M,N], magnitude bound fp64 [M,N], RNE dtype bits [M,N])."""
+    yd = np.ascontiguousarray(Yd, dtype=np.float64).reshape(M, N)
+    bb = np.ascontiguousarray(Babs, dtype=np.float64).reshape(M, N)
+    b = None if bias is None else _u16(bias)
+    r = None if residual is None else _u16(residual)
+    assert b is None or b.size == N
+    assert r is None or r.size == M * N
+    out = np.empty((M, N), dtype=np.float64)
+    bo = np.empty((M, N), dtype=np.float64)
+    yr = np.empty((M, N), dtype=np.uint16)
+    rc = _load().w4o_epilogue(_ptr(yd), _ptr(bb), _ptr(b), _ptr(r), act, M, N, dtype,
+                              _ptr(out), _ptr(bo), _ptr(yr))
+    assert rc == 0, rc
+    return out, bo, yr
 
 
 def check(Y_bits, Yd, Babs, dtype: int, rel_tol: float = REL_TOL):

@@ -15,6 +15,9 @@
 //          weight operand; per-channel scales commute with the k-sum and go to the end.
 //        - §6.4: group sizes 128 / 64 / 32.
 //        - §6.7: per-channel scale folded into the epilogue.
+//        - §6.2 (end of the tile pipeline: accumulator x scale -> + bias -> store) and
+//          §6.6 (dequant + GEMM + scale + bias, + residual / activation, in one kernel):
+//          the fused epilogue below.
 //
 // Readings where the pages are silent (each is listed in the design notes):
 //   * nibble j of word w of a row is bits 4j..4j+3 and holds k = 8w + j (the pages
@@ -299,6 +302,41 @@ int64_t w4o_check(const uint16_t* Y, const double* Yd, const double* Babs, int64
     if (first_bad) *first_bad = first;
     if (worst) *worst = wr;
     return bad;
+}
+
+// Fused epilogue ("量化开销对比" §6.2, §6.6).  From the GEMM's fp64 result Yd (per-channel
+// factor included) and its magnitude Babs, per element (m, n):
+//     pre  = Yd + bias[n]                      (bias optional)
+//     post = act(pre)                          0: identity, 1: max(pre, 0),
+//                                              2: SiLU, pre / (1 + exp(-pre))
+//     out  = post + residual[m, n]             (residual optional)
+// all in fp64 (the pages fix no order between residual and activation; the activation
+// is applied to the biased GEMM result and the residual added after it).  Also
+//     Bout = L * Babs + |bias| + |residual|     L = 1 (identity, ReLU) or 1.1 (SiLU,
+//                                               whose slope lies in [-0.1, 1.1])
+// the magnitude that scales the fused result's error bound, and Yref = RNE_dtype(out).
+int w4o_epilogue(const double* Yd, const double* Babs, const uint16_t* bias,
+                 const uint16_t* residual, int act, int M, int N, int dtype, double* Yout,
+                 double* Bout, uint16_t* Yref) {
+    if (M <= 0 || N <= 0 || act < 0 || act > 2) return -1;
+    const Fmt& F = fmt_of(dtype);
+    const double L = act == 2 ? 1.1 : 1.0;
+    for (int m = 0; m < M; ++m) {
+        for (int n = 0; n < N; ++n) {
+            const size_t o = static_cast<size_t>(m) * N + n;
+            const double b = bias ? decode(bias[n], F) : 0.0;
+            const double r = residual ? decode(residual[o], F) : 0.0;
+            const double pre = Yd[o] + b;
+            double post = pre;
+            if (act == 1) post = pre > 0.0 ? pre : 0.0;
+            if (act == 2) post = pre / (1.0 + std::exp(-pre));
+            const double out = post + r;
+            if (Yout) Yout[o] = out;
+            if (Bout) Bout[o] = L * Babs[o] + std::fabs(b) + std::fabs(r);
+            if (Yref) Yref[o] = encode(out, F);
+        }
+    }
+    return 0;
 }
 
 }  // extern "C"
