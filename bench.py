@@ -48,6 +48,10 @@ def parse():
     ap.add_argument("--split-k", type=int, default=0)
     ap.add_argument("--tile-m", type=int, default=0)
     ap.add_argument("--stages", type=int, default=0)
+    ap.add_argument("--epilogue", default="none",
+                    choices=["none", "bias", "bias_relu", "bias_silu", "bias_residual",
+                             "bias_silu_residual"],
+                    help="fuse a bias / activation / residual epilogue into every GEMM")
     ap.add_argument("--shape", action="append", default=[],
                     help="restrict the workload to this shape tag (repeatable; profiling)")
     return ap.parse_args()
@@ -201,8 +205,13 @@ def oracle_slice(orc, c, n0, nc):
     _ = G
 
 
-def shape_bytes(p):
-    return si.algorithmic_bytes(p["M"], p["N"], p["K"], p["group"], p.get("asym", True))
+def shape_bytes(p, epilogue="none"):
+    b = si.algorithmic_bytes(p["M"], p["N"], p["K"], p["group"], p.get("asym", True))
+    if epilogue != "none":
+        b += 2 * p["N"]             # bias
+    if epilogue.endswith("residual"):
+        b += 2 * p["M"] * p["N"]    # residual read
+    return b
 
 
 def cpu_oracle_rate(cases, shapes, budget_s):
@@ -296,7 +305,7 @@ def run_ours(a):
 
     shapes = workload_shapes(a)
     cases = [si.make_case(**p) for p in shapes]
-    step_bytes = sum(shape_bytes(p) for p in shapes)
+    step_bytes = sum(shape_bytes(p, a.epilogue) for p in shapes)
     step_flops = sum(si.flops(p["M"], p["N"], p["K"]) for p in shapes)
 
     def dev(x):
@@ -319,6 +328,33 @@ def run_ours(a):
         bufs.append((c, reps, A, Y))
     torch.cuda.synchronize()
     ex = dict(kernel=a.kernel, split_k=a.split_k, tile_m=a.tile_m, stages=a.stages)
+    # optional fused epilogue: a seeded bias per shape (resident, like the weights) and a
+    # device-resident residual (the previous layer's output in a real forward pass)
+    act = {"relu": w4.W4A16_ACT_RELU, "silu": w4.W4A16_ACT_SILU}
+    epi_act = next((v for k, v in act.items() if k in a.epilogue), w4.W4A16_ACT_NONE)
+    epi = []
+    for c, _, _, _ in bufs:
+        tdt = torch.float16 if c.dtype == 0 else torch.bfloat16
+        g = torch.Generator().manual_seed(c.M * 100003 + c.N)
+        bias = (torch.randn(c.N, generator=g).to(tdt).view(torch.int16).to(device)
+                if a.epilogue != "none" else None)
+        res = (torch.randn((c.M, c.N), generator=g).to(tdt).view(torch.int16).to(device)
+               if a.epilogue.endswith("residual") else None)
+        epi.append((bias, res))
+
+    def gemm_call(j, A, packed, Y, stream_, public=False):
+        c = bufs[j][0]
+        if a.epilogue == "none":
+            if public:
+                w4.w4a16_gemm(A, packed, c.M, c.N, c.K, c.group, c.dtype, Y, stream_)
+            else:
+                w4.w4a16_gemm_ex(A, packed, c.M, c.N, c.K, c.group, c.dtype, Y, stream=stream_,
+                                 **ex)
+        else:
+            bias, res = epi[j]
+            w4.w4a16_gemm_epilogue(A, packed, c.M, c.N, c.K, c.group, c.dtype, bias, res,
+                                   epi_act, Y, stream=stream_, **({} if public else ex))
+
     # which of the two kernels each shape runs on (the library's own launch choice)
     kname = {w4.W4A16_KERNEL_TC: "w4a16_tc_kernel", w4.W4A16_KERNEL_SIMT: "w4a16_gemv_kernel"}
     shape_kernel = [kname[w4.w4a16_gemm_plan(c.M, c.N, c.K, c.group, c.dtype, **ex)["kernel"]]
@@ -327,9 +363,8 @@ def run_ours(a):
     stream = torch.cuda.Stream(device=device)
 
     def launch_step(step_idx):
-        for c, reps, A, Y in bufs:
-            w4.w4a16_gemm_ex(A, reps[step_idx % copies], c.M, c.N, c.K, c.group, c.dtype, Y,
-                             stream=stream, **ex)
+        for j, (c, reps, A, Y) in enumerate(bufs):
+            gemm_call(j, A, reps[step_idx % copies], Y, stream)
 
     with torch.cuda.stream(stream):
         for i in range(max(3, a.warmup)):
@@ -390,8 +425,7 @@ def run_ours(a):
         with torch.cuda.stream(stream):
             with torch.cuda.graph(gj, stream=stream):
                 for i in range(nl):
-                    w4.w4a16_gemm_ex(A, reps[i % copies], c.M, c.N, c.K, c.group, c.dtype, Y,
-                                     stream=stream, **ex)
+                    gemm_call(j, A, reps[i % copies], Y, stream)
             gj.replay()
             f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             f0.record(stream)
@@ -403,7 +437,7 @@ def run_ours(a):
         del gj
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
-    launch_bytes = [shape_bytes(p) for p in shapes]
+    launch_bytes = [shape_bytes(p, a.epilogue) for p in shapes]
     # The roofline is that of the dominant kernel (the one most launches of a step run
     # on): its algorithmic bytes per launch over its average launch duration, both over
     # its own shapes, the durations from the per-shape pass (CUDA events on the launch
@@ -471,8 +505,7 @@ def run_ours(a):
         if i >= 2:
             stream.wait_event(out_done[b])  # step i-2's outputs have left devY[b]
         for j, c in enumerate(cases):
-            w4.w4a16_gemm(a_ptr[b][j], p_ptr[j][i % copies], c.M, c.N, c.K, c.group, c.dtype,
-                          y_ptr[b][j], s_ptr)
+            gemm_call(j, a_ptr[b][j], p_ptr[j][i % copies], y_ptr[b][j], s_ptr, public=True)
         gemm_done[b].record(stream)
         with torch.cuda.stream(out_stream):
             out_stream.wait_event(gemm_done[b])
@@ -527,6 +560,7 @@ def run_ours(a):
         "ms_per_step": elapsed_ms / a.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": a.workload, "shapes": len(shapes),
+                   **({"epilogue": a.epilogue} if a.epilogue != "none" else {}),
                    **({"shape_subset": a.shape} if a.shape else {}),
                    "step_bytes": step_bytes,
                    "step_flops": step_flops,

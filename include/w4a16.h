@@ -164,6 +164,31 @@ int w4a16_gemm(const void* A, const void* packed, int M, int N, int K, int group
 int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int group,
                   int dtype, void* Y, const w4a16_gemm_config* cfg, void* stream);
 
+/* Activation of the fused epilogue (w4a16_gemm_epilogue). */
+typedef enum w4a16_act {
+    W4A16_ACT_NONE = 0,
+    W4A16_ACT_RELU = 1,  /* max(x, 0)                                                 */
+    W4A16_ACT_SILU = 2   /* x / (1 + exp(-x))                                         */
+} w4a16_act;
+
+/*
+ * The fused GEMM with a bias / activation / residual epilogue ("量化开销对比" §6.2: the
+ * accumulator times the per-channel scale, plus bias, then the store; §6.6: bias and
+ * residual / activation fused into the same kernel).  Per output element, in fp32 after
+ * the fp32 k-sum and the per-channel factor c[n]:
+ *     Y[m,n] = RNE_dtype( act( c[n] * sum_k A[m,k] W[n,k] + bias[n] ) + residual[m,n] )
+ *   bias      device, dtype [N], 2-byte aligned, or NULL (no bias).
+ *   residual  device, dtype [M][N] row-major, 2-byte aligned, or NULL.  It may be Y
+ *             itself (in-place residual add: each element is read and then written by the
+ *             same thread); any other overlap with Y, A or packed is not allowed.
+ *   act       w4a16_act.
+ * Everything else (arguments, kernel choice through cfg, header check, errors) as for
+ * w4a16_gemm_ex; INVALID_ARG also for an unknown act or a misaligned bias / residual.
+ */
+int w4a16_gemm_epilogue(const void* A, const void* packed, int M, int N, int K, int group,
+                        int dtype, const void* bias, const void* residual, int act, void* Y,
+                        const w4a16_gemm_config* cfg, void* stream);
+
 /*
  * The kernel and tiling that w4a16_gemm_ex(..., cfg, ...) would launch for this shape on
  * the current device (cfg may be NULL = AUTO), written to *out with every field resolved

@@ -31,6 +31,10 @@ W4A16_KERNEL_AUTO = 0
 W4A16_KERNEL_TC = 1
 W4A16_KERNEL_SIMT = 2
 
+W4A16_ACT_NONE = 0
+W4A16_ACT_RELU = 1
+W4A16_ACT_SILU = 2
+
 W4A16_GEMM_NO_PDL = 1
 W4A16_GEMM_NO_WEIGHT_PREFETCH = 2
 
@@ -71,6 +75,9 @@ def lib() -> ctypes.CDLL:
             L.w4a16_gemm.restype = I
             L.w4a16_gemm_ex.argtypes = [P, P, I, I, I, I, I, P, ctypes.POINTER(GemmConfig), P]
             L.w4a16_gemm_ex.restype = I
+            L.w4a16_gemm_epilogue.argtypes = [P, P, I, I, I, I, I, P, P, I, P,
+                                              ctypes.POINTER(GemmConfig), P]
+            L.w4a16_gemm_epilogue.restype = I
             L.w4a16_gemm_plan.argtypes = [I, I, I, I, I, ctypes.POINTER(GemmConfig),
                                           ctypes.POINTER(GemmConfig)]
             L.w4a16_gemm_plan.restype = I
@@ -149,6 +156,16 @@ def w4a16_gemm_ex(A, packed, M: int, N: int, K: int, group: int, dtype: int, Y, 
     cfg = GemmConfig(kernel, split_k, tile_m, stages, flags)
     _check(lib().w4a16_gemm_ex(_ptr(A), _ptr(packed), M, N, K, group, dtype, _ptr(Y),
                                ctypes.byref(cfg), _stream(stream)), "w4a16_gemm_ex")
+
+
+def w4a16_gemm_epilogue(A, packed, M: int, N: int, K: int, group: int, dtype: int, bias,
+                        residual, act: int, Y, *, kernel: int = W4A16_KERNEL_AUTO,
+                        split_k: int = 0, tile_m: int = 0, stages: int = 0, flags: int = 0,
+                        stream=None) -> None:
+    cfg = GemmConfig(kernel, split_k, tile_m, stages, flags)
+    _check(lib().w4a16_gemm_epilogue(_ptr(A), _ptr(packed), M, N, K, group, dtype, _ptr(bias),
+                                     _ptr(residual), act, _ptr(Y), ctypes.byref(cfg),
+                                     _stream(stream)), "w4a16_gemm_epilogue")
 
 
 def w4a16_gemm_plan(M: int, N: int, K: int, group: int, dtype: int, *,

@@ -201,8 +201,9 @@ int w4a16_repack(const uint32_t* qweight, const void* scales, const uint32_t* qz
                          packed, static_cast<cudaStream_t>(stream));
 }
 
-int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int group, int dtype,
-                  void* Y, const w4a16_gemm_config* cfg, void* stream) {
+namespace {
+int gemm_common(const void* A, const void* packed, int M, int N, int K, int group, int dtype,
+                void* Y, const w4a16_gemm_config* cfg, const EpilogueArgs& epi, void* stream) {
     if (M < 0) return W4A16_ERR_INVALID_ARG;
     int rc = check_shape(N, K, group, dtype);
     if (rc != W4A16_OK) return rc;
@@ -215,8 +216,26 @@ int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int gr
     if ((rc = make_plan(*ctx, M, N, K, group, cfg, &plan)) != W4A16_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan.kernel == W4A16_KERNEL_SIMT)
-        return launch_simt_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, s);
-    return launch_tc_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, s);
+        return launch_simt_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, epi, s);
+    return launch_tc_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, epi, s);
+}
+}  // namespace
+
+int w4a16_gemm_ex(const void* A, const void* packed, int M, int N, int K, int group, int dtype,
+                  void* Y, const w4a16_gemm_config* cfg, void* stream) {
+    const EpilogueArgs none{nullptr, nullptr, kActNone};
+    return gemm_common(A, packed, M, N, K, group, dtype, Y, cfg, none, stream);
+}
+
+int w4a16_gemm_epilogue(const void* A, const void* packed, int M, int N, int K, int group,
+                        int dtype, const void* bias, const void* residual, int act, void* Y,
+                        const w4a16_gemm_config* cfg, void* stream) {
+    if (act != W4A16_ACT_NONE && act != W4A16_ACT_RELU && act != W4A16_ACT_SILU)
+        return W4A16_ERR_INVALID_ARG;
+    if (!aligned(bias, 2) || !aligned(residual, 2)) return W4A16_ERR_INVALID_ARG;
+    const EpilogueArgs epi{static_cast<const uint16_t*>(bias),
+                           static_cast<const uint16_t*>(residual), act};
+    return gemm_common(A, packed, M, N, K, group, dtype, Y, cfg, epi, stream);
 }
 
 int w4a16_gemm_plan(int M, int N, int K, int group, int dtype, const w4a16_gemm_config* cfg,

@@ -33,6 +33,7 @@
 #include <mutex>
 
 #include "dequant.cuh"
+#include "epilogue.cuh"
 #include "format.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -46,16 +47,18 @@ constexpr int kCtrlBytes = 1024;
 
 #ifdef W4A16_TRACE
 // Development-only timeline (built with -DW4A16_TRACE, never in the product library):
-// globaltimer stamps per CTA for the first kTraceCtas CTAs.
-constexpr int kTraceCtas = 1024;
+// every CTA claims one record (in start order, across launches) and stamps globaltimer
+// values into its slots; slots 57..59 identify the launch and the CTA.
+constexpr int kTraceRecs = 8192;
 constexpr int kTraceSlots = 64;
-__device__ unsigned long long g_w4a16_trace[kTraceCtas * kTraceSlots];
+__device__ unsigned long long g_w4a16_trace[kTraceRecs * kTraceSlots];
+__device__ unsigned int g_w4a16_trace_next;
 #define W4G_TRACE(slot, value)                                                         \
     do {                                                                              \
-        const unsigned cta_ = blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z); \
         const int slot_ = (slot);                                                     \
-        if (cta_ < kTraceCtas && slot_ >= 0 && slot_ < kTraceSlots)                   \
-            g_w4a16_trace[cta_ * kTraceSlots + slot_] = (value);                      \
+        if (trace_rec < static_cast<unsigned>(kTraceRecs) && slot_ >= 0 &&            \
+            slot_ < kTraceSlots)                                                      \
+            g_w4a16_trace[trace_rec * kTraceSlots + slot_] = (value);                 \
     } while (0)
 #define W4G_NOW() globaltimer_ns()
 #else
@@ -87,6 +90,7 @@ struct TcArgs {
     uint32_t stage_bytes;
     uint32_t recv_off;    // offset of the split-K receive area from the ring base
     uint64_t timeout_ns;
+    EpilogueArgs epi;     // bias / activation / residual applied to the fp32 result
 };
 
 template <int BM>
@@ -157,6 +161,21 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const bool prefetch_w = (args.flags & kFlagPrefetchW) != 0;
     const uint32_t slice_bytes = static_cast<uint32_t>(BM * args.slice_rows * 4);
 
+#ifdef W4A16_TRACE
+    unsigned trace_rec = 0xFFFFFFFFu;
+    if (threadIdx.x == 0) {
+        trace_rec = atomicAdd(&g_w4a16_trace_next, 1u);
+        *reinterpret_cast<unsigned*>(ctrl_ptr + 488) = trace_rec;
+        W4G_TRACE(57, static_cast<unsigned long long>(args.M) |
+                          (static_cast<unsigned long long>(args.N) << 16) |
+                          (static_cast<unsigned long long>(args.K) << 32));
+        W4G_TRACE(58, blockIdx.x | (static_cast<unsigned long long>(blockIdx.y) << 16) |
+                          (static_cast<unsigned long long>(blockIdx.z) << 32));
+        unsigned smid_;
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid_));
+        W4G_TRACE(59, smid_);
+    }
+#endif
     if (threadIdx.x == 0) {
         W4G_TRACE(0, W4G_NOW());
         *abort_flag = 0;
@@ -198,12 +217,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
 
     const uint32_t tmem = *tmem_slot;
 #ifdef W4A16_TRACE
-    if (threadIdx.x == 0) {
-        W4G_TRACE(1, W4G_NOW());
-        unsigned smid_;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid_));
-        W4G_TRACE(56, smid_);
-    }
+    trace_rec = *reinterpret_cast<const unsigned*>(ctrl_ptr + 488);
+    if (threadIdx.x == 0) W4G_TRACE(1, W4G_NOW());
 #endif
     const int flags = info[0];
     const bool run = flags >= 0 && nkb > 0;
@@ -453,10 +468,11 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             uint16_t* Y = static_cast<uint16_t*>(args.Y);
             if (args.splits == 1) grid_dep_wait();  // Y may still be in use upstream
             const float cs = (args.splits == 1 && cscale) ? cscale[n] : 1.0f;
+            const float bias_n =
+                (args.splits == 1 && args.epi.bias) ? dtype_to_f32<DT>(args.epi.bias[n]) : 0.0f;
             const int pslice = r / R, prow = r - pslice * R;
-#pragma unroll 1
-            for (int e = wg; e < BM / 16; e += NWG) {
-                uint32_t v[16];
+            // D columns e*16 .. e*16+15 of this thread's channel (both accumulators added)
+            auto load_d = [&](int e, uint32_t (&v)[16]) {
                 tmem_ld16(tmem + lane_base + e * 16, v);
                 if (kNMI == 2 && nkb > 1) {  // add the odd-block accumulator
                     uint32_t v1[16];
@@ -468,18 +484,62 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 } else {
                     tmem_wait_ld();
                 }
-                if (args.splits == 1) {
+            };
+            if (args.splits > 1) {
+#pragma unroll 1
+                for (int e = wg; e < BM / 16; e += NWG) {
+                    uint32_t v[16];
+                    load_d(e, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        part[(pslice * BM + e * 16 + j) * R + prow] = __uint_as_float(v[j]);
+                }
+            } else if (!args.epi.residual) {
+                const int act = args.epi.act;
+#pragma unroll 1
+                for (int e = wg; e < BM / 16; e += NWG) {
+                    uint32_t v[16];
+                    load_d(e, v);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = m_tile * BM + e * 16 + j;
+                        const float y = __uint_as_float(v[j]) * cs + bias_n;
+                        if (m < args.M)
+                            Y[static_cast<size_t>(m) * args.N + n] =
+                                f32_to_dtype<DT>(act == kActNone ? y : apply_activation(y, act));
+                    }
+                }
+            } else {
+                // The residual may be Y itself, so its loads cannot move past earlier
+                // stores: the next group's 16 values are read before this group is stored.
+                const uint16_t* rp = args.epi.residual;
+                auto load_res = [&](int e, float (&r)[16]) {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const int m = m_tile * BM + e * 16 + j;
+                        r[j] = m < args.M
+                                   ? dtype_to_f32<DT>(rp[static_cast<size_t>(m) * args.N + n])
+                                   : 0.0f;
+                    }
+                };
+                float rnext[16];
+                if (wg < BM / 16) load_res(wg, rnext);
+#pragma unroll 1
+                for (int e = wg; e < BM / 16; e += NWG) {
+                    float res[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) res[j] = rnext[j];
+                    if (e + NWG < BM / 16) load_res(e + NWG, rnext);
+                    uint32_t v[16];
+                    load_d(e, v);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = m_tile * BM + e * 16 + j;
                         if (m < args.M)
-                            Y[static_cast<size_t>(m) * args.N + n] =
-                                f32_to_dtype<DT>(__uint_as_float(v[j]) * cs);
+                            Y[static_cast<size_t>(m) * args.N + n] = f32_to_dtype<DT>(
+                                apply_activation(__uint_as_float(v[j]) * cs + bias_n, args.epi.act) +
+                                res[j]);
                     }
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        part[(pslice * BM + e * 16 + j) * R + prow] = __uint_as_float(v[j]);
                 }
             }
         }
@@ -525,7 +585,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     }
                     const int n = n_tile * kTileN + r0 + j;
                     if (cscale) acc *= cscale[n];
-                    Y[static_cast<size_t>(m_tile * BM + ml) * args.N + n] = f32_to_dtype<DT>(acc);
+                    const float bias_n = args.epi.bias ? dtype_to_f32<DT>(args.epi.bias[n]) : 0.0f;
+                    const size_t o = static_cast<size_t>(m_tile * BM + ml) * args.N + n;
+                    Y[o] = f32_to_dtype<DT>(apply_epilogue<DT>(acc, bias_n, args.epi, o));
                 }
             }
         }
@@ -534,6 +596,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
 
     tc_fence_before();
     __syncthreads();
+    if (threadIdx.x == 0) W4G_TRACE(60, W4G_NOW());
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -564,7 +627,8 @@ EncodeTiledFn encode_fn() {
 
 template <int BM, int NWG, int DT>
 int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
-                       int K, int group, void* Y, const GemmPlan& plan, cudaStream_t stream) {
+                       int K, int group, void* Y, const GemmPlan& plan,
+                       const EpilogueArgs& epi, cudaStream_t stream) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return -3;
     const int a_rows = tc_a_rows(BM, M);
@@ -604,6 +668,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     if (plan.split_k > 1 && recv_bytes > ring) return -2;  // partials are staged in the ring
     args.recv_off = ring;
     args.timeout_ns = ctx.timeout_ns;
+    args.epi = epi;
 
     const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;
     if (smem > static_cast<size_t>(ctx.max_smem_optin)) return -2;
@@ -658,7 +723,9 @@ extern "C" int w4a16_trace_read(void* host, size_t bytes) {
 extern "C" int w4a16_trace_clear(void) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_w4a16_trace) != cudaSuccess) return -3;
-    return cudaMemset(p, 0, sizeof(g_w4a16_trace)) == cudaSuccess ? 0 : -3;
+    if (cudaMemset(p, 0, sizeof(g_w4a16_trace)) != cudaSuccess) return -3;
+    const unsigned zero = 0;
+    return cudaMemcpyToSymbol(g_w4a16_trace_next, &zero, sizeof(zero)) == cudaSuccess ? 0 : -3;
 }
 #endif
 
@@ -691,14 +758,14 @@ int tc_max_stages(int tile_m, int M, int group, int smem_budget) {
 
 int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                    int K, int group, int dtype, void* Y, const GemmPlan& plan,
-                   cudaStream_t stream) {
+                   const EpilogueArgs& epi, cudaStream_t stream) {
 #define W4G_TC_CASE(BMV, NWGV)                                                            \
     case BMV:                                                                            \
         return dtype == 0                                                                \
                    ? launch_tc_instance<BMV, NWGV, 0>(ctx, A, packed, M, N, K, group, Y, \
-                                                      plan, stream)                      \
+                                                      plan, epi, stream)                 \
                    : launch_tc_instance<BMV, NWGV, 1>(ctx, A, packed, M, N, K, group, Y, \
-                                                      plan, stream);
+                                                      plan, epi, stream);
     switch (plan.tile_m) {
         W4G_TC_CASE(16, W4A16_SMALL_TILE_WG)
         W4G_TC_CASE(32, W4A16_SMALL_TILE_WG)

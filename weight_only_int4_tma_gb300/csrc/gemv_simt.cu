@@ -26,6 +26,7 @@
 #include <cuda_fp16.h>
 
 #include "dequant.cuh"
+#include "epilogue.cuh"
 #include "format.cuh"
 #include "launch.h"
 #include "ptx.cuh"
@@ -117,7 +118,8 @@ __device__ __forceinline__ void chunk_fma(const uint4 v, uint32_t zp, uint32_t s
 template <int MM, int DT, int ROWS>
 __global__ void __launch_bounds__(kGemvThreads, 2) w4a16_gemv_kernel(
     const uint16_t* __restrict__ A, const uint8_t* __restrict__ packed,
-    uint16_t* __restrict__ Y, int* status, int M, int N, int K, int group, int prefetch_w) {
+    uint16_t* __restrict__ Y, int* status, int M, int N, int K, int group, int prefetch_w,
+    const EpilogueArgs epi) {
     constexpr int kSub = 32 / ROWS;            // K slots per warp
     constexpr int kSlots = kGemvWarps * kSub;
     // Ring stage s: nibbles [4 chunks][threads][16 B], then per thread and group of the
@@ -248,7 +250,9 @@ __global__ void __launch_bounds__(kGemvThreads, 2) w4a16_gemv_kernel(
                 for (int p = 0; p < kSlots; ++p) sum += red[ui & 1][p][m][jr];
                 const int n = n0 + jr;
                 if (cs) sum *= cs[n];
-                Y[static_cast<size_t>(m) * N + n] = f32_to_dtype_s<DT>(sum);
+                const float bias_n = epi.bias ? dtype_to_f32<DT>(epi.bias[n]) : 0.0f;
+                const size_t o = static_cast<size_t>(m) * N + n;
+                Y[o] = f32_to_dtype_s<DT>(apply_epilogue<DT>(sum, bias_n, epi, o));
             }
         }
     }
@@ -258,7 +262,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) w4a16_gemv_kernel(
 template <int MM, int DT, int ROWS>
 int launch_gemv_instance(const DeviceCtx& ctx, const void* A, const void* packed, int M,
                          int N, int K, int group, void* Y, const GemmPlan& plan,
-                         cudaStream_t stream) {
+                         const EpilogueArgs& epi, cudaStream_t stream) {
     auto kern = w4a16_gemv_kernel<MM, DT, ROWS>;
     const int G = groups_per_block(group);
     const size_t smem = static_cast<size_t>(kGemvStages) * kGemvThreads * (64 + 8 * G);
@@ -299,30 +303,31 @@ int launch_gemv_instance(const DeviceCtx& ctx, const void* A, const void* packed
     cfg.numAttrs = static_cast<unsigned>(na);
     const cudaError_t e = cudaLaunchKernelEx(
         &cfg, kern, static_cast<const uint16_t*>(A), static_cast<const uint8_t*>(packed),
-        static_cast<uint16_t*>(Y), ctx.status, M, N, K, group, plan.prefetch_weights ? 1 : 0);
+        static_cast<uint16_t*>(Y), ctx.status, M, N, K, group, plan.prefetch_weights ? 1 : 0,
+        epi);
     return e == cudaSuccess ? 0 : -3;
 }
 
 template <int MM>
 int launch_gemv_mm(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                    int K, int group, int dtype, void* Y, const GemmPlan& plan,
-                   cudaStream_t stream) {
+                   const EpilogueArgs& epi, cudaStream_t stream) {
     if (plan.tile_m == 16)
-        return dtype == 0 ? launch_gemv_instance<MM, 0, 16>(ctx, A, packed, M, N, K, group, Y, plan, stream)
-                          : launch_gemv_instance<MM, 1, 16>(ctx, A, packed, M, N, K, group, Y, plan, stream);
-    return dtype == 0 ? launch_gemv_instance<MM, 0, 32>(ctx, A, packed, M, N, K, group, Y, plan, stream)
-                      : launch_gemv_instance<MM, 1, 32>(ctx, A, packed, M, N, K, group, Y, plan, stream);
+        return dtype == 0 ? launch_gemv_instance<MM, 0, 16>(ctx, A, packed, M, N, K, group, Y, plan, epi, stream)
+                          : launch_gemv_instance<MM, 1, 16>(ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
+    return dtype == 0 ? launch_gemv_instance<MM, 0, 32>(ctx, A, packed, M, N, K, group, Y, plan, epi, stream)
+                      : launch_gemv_instance<MM, 1, 32>(ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
 }
 
 }  // namespace
 
 int launch_simt_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                      int K, int group, int dtype, void* Y, const GemmPlan& plan,
-                     cudaStream_t stream) {
-    if (M <= 1) return launch_gemv_mm<1>(ctx, A, packed, M, N, K, group, dtype, Y, plan, stream);
-    if (M <= 2) return launch_gemv_mm<2>(ctx, A, packed, M, N, K, group, dtype, Y, plan, stream);
-    if (M <= 4) return launch_gemv_mm<4>(ctx, A, packed, M, N, K, group, dtype, Y, plan, stream);
-    if (M <= 8) return launch_gemv_mm<8>(ctx, A, packed, M, N, K, group, dtype, Y, plan, stream);
+                     const EpilogueArgs& epi, cudaStream_t stream) {
+    if (M <= 1) return launch_gemv_mm<1>(ctx, A, packed, M, N, K, group, dtype, Y, plan, epi, stream);
+    if (M <= 2) return launch_gemv_mm<2>(ctx, A, packed, M, N, K, group, dtype, Y, plan, epi, stream);
+    if (M <= 4) return launch_gemv_mm<4>(ctx, A, packed, M, N, K, group, dtype, Y, plan, epi, stream);
+    if (M <= 8) return launch_gemv_mm<8>(ctx, A, packed, M, N, K, group, dtype, Y, plan, epi, stream);
     return -2;
 }
 

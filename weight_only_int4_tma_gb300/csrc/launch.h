@@ -4,6 +4,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "epilogue.cuh"
+
 namespace w4g {
 
 // Per-device state, created once per device on first use.
@@ -34,11 +36,11 @@ int launch_dequant_debug(const DeviceCtx& ctx, const void* packed, int N, int K,
 
 int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                    int K, int group, int dtype, void* Y, const GemmPlan& plan,
-                   cudaStream_t stream);
+                   const EpilogueArgs& epi, cudaStream_t stream);
 
 int launch_simt_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                      int K, int group, int dtype, void* Y, const GemmPlan& plan,
-                     cudaStream_t stream);
+                     const EpilogueArgs& epi, cudaStream_t stream);
 
 int launch_timeout_probe(const DeviceCtx& ctx, uint64_t limit_ns, cudaStream_t stream);
 
