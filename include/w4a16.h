@@ -101,11 +101,12 @@ const char* w4a16_status_string(int status);
 
 /*
  * Size in bytes of the packed blob that w4a16_repack writes for these arguments, or 0
- * if the shape is unsupported (see w4a16_repack).  The blob is
+ * if the shape is unsupported (see w4a16_repack).  With Np = N and Kp = K rounded up to
+ * multiples of 128, the blob is
  *     128-byte header
- *   + K*N/2 bytes of nibbles
- *   + (K/group)*N*2 bytes of scales
- *   + (K/group)*N/2 bytes of zeros           (only if has_zeros)
+ *   + Kp*Np/2 bytes of nibbles
+ *   + (Kp/group)*Np*2 bytes of scales
+ *   + (Kp/group)*Np/2 bytes of zeros         (only if has_zeros)
  *   + 4*N bytes of fp32 per-channel factors  (only if has_channel_scale)
  * laid out in the kernel's tile order (128 output channels x 128 K per block, blocks of
  * one channel tile contiguous along K; nibbles interleaved within each word so that
@@ -126,7 +127,11 @@ size_t w4a16_packed_bytes(int N, int K, int group, int has_zeros, int has_channe
  *                  gi is z[gi, 8w + j].  NULL = symmetric weights, every zero is 8.
  *   channel_scale  device, dtype [N]: optional factor c[n] applied to the fp32 result
  *                  of output channel n in the epilogue.  NULL = none.
- *   N, K, group    N % 128 == 0, K % 128 == 0, group in {32, 64, 128}; N, K > 0.
+ *   N, K, group    N, K > 0; N % 8 == 0 (zeros are packed along N); group in
+ *                  {32, 64, 128} and K % group == 0.  N and K need not be multiples of
+ *                  128: the blob is padded to whole 128 x 128 blocks (zero scales past N
+ *                  or K, so the padded weights are exactly 0) and records the logical
+ *                  N and K.
  *   dtype          w4a16_dtype of scales and channel_scale (and of A/Y at GEMM time).
  *   packed         device output, at least w4a16_packed_bytes(...) bytes, 16-byte
  *                  aligned, must not overlap the inputs.

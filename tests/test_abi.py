@@ -38,8 +38,17 @@ def test_packed_bytes_formula(L, N, K, g, z, c):
     assert w4.w4a16_packed_bytes(N, K, g, z, c) == want
 
 
+@pytest.mark.parametrize("N,K,g,z,c", [(520, 512, 128, 1, 0), (512, 64, 32, 1, 0),
+                                       (264, 4160, 64, 0, 1), (8, 96, 32, 1, 1)])
+def test_packed_bytes_padded(L, N, K, g, z, c):
+    """Shapes that are not multiples of 128 occupy whole 128 x 128 blocks."""
+    Np, Kp = -(-N // 128) * 128, -(-K // 128) * 128
+    want = 128 + Kp * Np // 2 + (Kp // g) * Np * 2 + (Kp // g) * Np // 2 * z + 4 * N * c
+    assert w4.w4a16_packed_bytes(N, K, g, z, c) == want
+
+
 @pytest.mark.parametrize("N,K,g", [(100, 512, 128), (512, 500, 128), (512, 512, 16),
-                                   (512, 512, 96), (0, 512, 128), (512, 64, 32)])
+                                   (512, 512, 96), (0, 512, 128), (512, 80, 32)])
 def test_packed_bytes_unsupported(L, N, K, g):
     assert w4.w4a16_packed_bytes(N, K, g, 1, 0) == 0
 
@@ -65,7 +74,7 @@ def test_gemm_host_validation(L):
     # M == 0 is a no-op that succeeds without touching the device
     assert L.w4a16_gemm(None, None, 0, 512, 512, 128, 0, None, None) == w4.W4A16_OK
     assert L.w4a16_gemm(fake, fake, -1, 512, 512, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG
-    assert L.w4a16_gemm(fake, fake, 4, 520, 512, 128, 0, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a16_gemm(fake, fake, 4, 516, 512, 128, 0, fake, None) == w4.W4A16_ERR_UNSUPPORTED
     assert L.w4a16_gemm(fake, fake, 4, 512, 512, 48, 0, fake, None) == w4.W4A16_ERR_UNSUPPORTED
     assert L.w4a16_gemm(None, fake, 4, 512, 512, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG
     assert L.w4a16_gemm(fake + 2, fake, 4, 512, 512, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG

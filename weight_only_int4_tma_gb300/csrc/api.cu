@@ -56,8 +56,10 @@ int check_shape(int N, int K, int group, int dtype) {
     if (N <= 0 || K <= 0) return W4A16_ERR_INVALID_ARG;
     if (dtype != W4A16_FP16 && dtype != W4A16_BF16) return W4A16_ERR_UNSUPPORTED;
     if (group != 32 && group != 64 && group != 128) return W4A16_ERR_UNSUPPORTED;
-    if (N % kTileN != 0 || K % kTileK != 0) return W4A16_ERR_UNSUPPORTED;
-    if (N / kTileN > 65535) return W4A16_ERR_UNSUPPORTED;  // grid.y limit
+    // N: zeros are packed 8 per word along N; K: whole groups (hence a multiple of 32).
+    // Anything else is padded to whole 128 x 128 blocks by the repack.
+    if (N % 8 != 0 || K % group != 0) return W4A16_ERR_UNSUPPORTED;
+    if (tiles_n(N) > 65535) return W4A16_ERR_UNSUPPORTED;  // grid.y limit
     return W4A16_OK;
 }
 
@@ -71,7 +73,7 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     // CUDA-core GEMV beats the tensor-core kernel there (the MMA's fixed issue cost and
     // the TMEM round trip of the unpacked tile dominate at one row, and the GEMV needs no
     // split-K reduction); longer K or more tiles favour the tensor-core kernel.
-    if (kernel == W4A16_KERNEL_AUTO && M == 1 && K <= 16384 && N / kTileN <= ctx.num_sms &&
+    if (kernel == W4A16_KERNEL_AUTO && M == 1 && K <= 16384 && tiles_n(N) <= ctx.num_sms &&
         !(cfg && (cfg->tile_m || cfg->split_k || cfg->stages)))
         kernel = W4A16_KERNEL_SIMT;
     int flags = 0;
@@ -99,8 +101,8 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     if (kernel != W4A16_KERNEL_AUTO && kernel != W4A16_KERNEL_TC) return W4A16_ERR_INVALID_ARG;
     plan->kernel = W4A16_KERNEL_TC;
 
-    const int n_tiles = N / kTileN;
-    const int kblocks = K / kTileK;
+    const int n_tiles = tiles_n(N);
+    const int kblocks = blocks_k(K);
     int bm = cfg && cfg->tile_m ? cfg->tile_m : 0;
     if (bm == 0) {
         if (M <= 16) bm = 16;
@@ -179,7 +181,7 @@ const char* w4a16_status_string(int status) {
 
 size_t w4a16_packed_bytes(int N, int K, int group, int has_zeros, int has_channel_scale) {
     if (check_shape(N, K, group, W4A16_FP16) != W4A16_OK) return 0;
-    const size_t blocks = static_cast<size_t>(N / kTileN) * static_cast<size_t>(K / kTileK);
+    const size_t blocks = static_cast<size_t>(tiles_n(N)) * static_cast<size_t>(blocks_k(K));
     return kHeaderBytes + blocks * block_bytes(group, has_zeros != 0) +
            (has_channel_scale ? 4ull * static_cast<size_t>(N) : 0ull);
 }

@@ -5,6 +5,9 @@
 // along K, so any K range of a tile is one contiguous byte range that a single bulk
 // TMA copy moves into shared memory, scales and zeros included.
 //
+// Shapes that are not multiples of 128 are padded to whole blocks at repack time (zero
+// scales and nibbles past N or K); the header keeps the logical N and K.
+//
 // Block layout (all offsets in bytes from the block start):
 //   [0, 8192)           nibbles: chunk c (32 K values) x row r (128) x word w (4),
 //                       16 bytes per (c, r).  A warp reading rows r..r+31 of one chunk
@@ -62,6 +65,11 @@ __host__ __device__ constexpr uint32_t zero_bytes(int group) {
 __host__ __device__ constexpr uint32_t block_bytes(int group, bool zeros) {
     return kNibbleBytes + scale_bytes(group) + (zeros ? zero_bytes(group) : 0u);
 }
+
+// Blocks along N and K: the blob covers ceil(N/128) x ceil(K/128) blocks; positions past
+// N or K hold zero scales (so the padded weights are exactly 0) and zero nibbles.
+__host__ __device__ constexpr int tiles_n(int N) { return (N + kTileN - 1) / kTileN; }
+__host__ __device__ constexpr int blocks_k(int K) { return (K + kTileK - 1) / kTileK; }
 
 // Nibble position of K offset j (0..7) inside a packed word.
 __host__ __device__ constexpr int nibble_pos(int j) { return 4 * (j & 1) + (j >> 1); }

@@ -85,6 +85,7 @@ struct TcArgs {
     int stages;           // ring depth
     int a_rows;           // rows per A chunk in shared memory (8, 16 or BM)
     int kps;              // 128-K blocks per ring stage (1 or 2)
+    int a_2d;             // A loaded as one 2-D box per 64-K chunk (K not a multiple of 64)
     int slice_rows;       // channels owned per cluster rank (ceil(128 / splits))
     int flags;
     uint32_t stage_bytes;
@@ -249,9 +250,18 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                              full0 + 8 * i, pol_w);
             }
             if (prefetch_w) grid_dep_wait();
+            auto load_a = [&](uint32_t st, int kchunk, uint32_t bar) {
+                if (args.a_2d) {  // chunk q of the stage at st + q * a_chunk; K tail zero-filled
+                    for (int q = 0; q < 2 * kps; ++q)
+                        tma_tensor_2d_g2s(st + static_cast<uint32_t>(q) * a_chunk, &tmap_a,
+                                          (kchunk + q) * 64, m0, bar, pol_a);
+                } else {
+                    tma_tensor_3d_g2s(st, &tmap_a, 0, m0, kchunk, bar, pol_a);
+                }
+            };
             for (int i = 0; i < pre; ++i) {
                 const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
-                tma_tensor_3d_g2s(st, &tmap_a, 0, m0, (kb0 + i * kps) * 2, full0 + 8 * i, pol_a);
+                load_a(st, (kb0 + i * kps) * 2, full0 + 8 * i);
                 if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
             }
             int issued = pre;
@@ -270,7 +280,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 const int nblk = left < kps ? left : kps;
                 mbar_arrive_expect_tx(fb, nblk * bb + a_bytes);
                 tma_bulk_g2s(st + a_bytes, wsrc, nblk * bb, fb, pol_w);
-                tma_tensor_3d_g2s(st, &tmap_a, 0, m0, kchunk, fb, pol_a);
+                load_a(st, kchunk, fb);
                 if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
                 ++issued;
                 left -= kps;
@@ -467,9 +477,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             const int n = n_tile * kTileN + r;
             uint16_t* Y = static_cast<uint16_t*>(args.Y);
             if (args.splits == 1) grid_dep_wait();  // Y may still be in use upstream
-            const float cs = (args.splits == 1 && cscale) ? cscale[n] : 1.0f;
-            const float bias_n =
-                (args.splits == 1 && args.epi.bias) ? dtype_to_f32<DT>(args.epi.bias[n]) : 0.0f;
+            const bool n_ok = n < args.N;  // rows past N are padding
+            const float cs = (args.splits == 1 && cscale && n_ok) ? cscale[n] : 1.0f;
+            const float bias_n = (args.splits == 1 && args.epi.bias && n_ok)
+                                     ? dtype_to_f32<DT>(args.epi.bias[n]) : 0.0f;
             const int pslice = r / R, prow = r - pslice * R;
             // D columns e*16 .. e*16+15 of this thread's channel (both accumulators added)
             auto load_d = [&](int e, uint32_t (&v)[16]) {
@@ -499,7 +510,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
 #pragma unroll 1
                 for (int e = wg; e < BM / 16; e += NWG) {
                     uint32_t v[16];
-                    load_d(e, v);
+                    load_d(e, v);  // warp-collective: every lane, padded rows included
+                    if (!n_ok) continue;  // a padded row: nothing to store
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = m_tile * BM + e * 16 + j;
@@ -517,7 +529,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = m_tile * BM + e * 16 + j;
-                        r[j] = m < args.M
+                        r[j] = (m < args.M && n_ok)
                                    ? dtype_to_f32<DT>(rp[static_cast<size_t>(m) * args.N + n])
                                    : 0.0f;
                     }
@@ -531,7 +543,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     for (int j = 0; j < 16; ++j) res[j] = rnext[j];
                     if (e + NWG < BM / 16) load_res(e + NWG, rnext);
                     uint32_t v[16];
-                    load_d(e, v);
+                    load_d(e, v);  // warp-collective: every lane, padded rows included
+                    if (!n_ok) continue;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const int m = m_tile * BM + e * 16 + j;
@@ -568,7 +581,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 if (warp == S::kDq0 && lane == 0) W4G_TRACE(54, W4G_NOW());
                 grid_dep_wait();
                 const int r0 = static_cast<int>(rank) * R;
-                const int nr = min(kTileN, r0 + R) - r0;
+                const int nr = min(min(kTileN, r0 + R), args.N - n_tile * kTileN) - r0;
                 const int mvalid = min(BM, args.M - m_tile * BM);
                 const float* recvp = reinterpret_cast<const float*>(base_ptr + args.recv_off);
                 uint16_t* Y = static_cast<uint16_t*>(args.Y);
@@ -634,16 +647,32 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     const int a_rows = tc_a_rows(BM, M);
     const int kps = tc_blocks_per_stage(BM);
     // A viewed as [K/64][M][64]: one box = 2*kps chunks of 64 K x a_rows rows, landing in
-    // shared memory chunk-major, each chunk a run of 128-byte-swizzled 8-row atoms.
+    // shared memory chunk-major, each chunk a run of 128-byte-swizzled 8-row atoms.  A
+    // chunk past K is outside the view and arrives as zeros.  If K is not a multiple of
+    // 64 that view does not exist: A is then the plain 2-D [M][K] tensor and every 64-K
+    // chunk is its own box (the part past K zero-filled), in the same shared layout.
     CUtensorMap map;
-    const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
-    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(a_rows), static_cast<cuuint32_t>(2 * kps)};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    CUresult cr = enc(&map, DT == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                      3, const_cast<void*>(A), dims, strides, box, estr,
-                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const bool a_2d = K % 64 != 0;
+    const auto dt = DT == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    CUresult cr;
+    if (!a_2d) {
+        const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(a_rows),
+                                   static_cast<cuuint32_t>(2 * kps)};
+        const cuuint32_t estr[3] = {1, 1, 1};
+        cr = enc(&map, dt, 3, const_cast<void*>(A), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(a_rows)};
+        const cuuint32_t estr[2] = {1, 1};
+        cr = enc(&map, dt, 2, const_cast<void*>(A), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     if (cr != CUDA_SUCCESS) return -3;
 
     TcArgs args;
@@ -654,11 +683,12 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     args.N = N;
     args.K = K;
     args.group = group;
-    args.kblocks = K / kTileK;
+    args.kblocks = blocks_k(K);
     args.splits = plan.split_k;
     args.stages = plan.stages;
     args.a_rows = a_rows;
     args.kps = kps;
+    args.a_2d = a_2d ? 1 : 0;
     args.slice_rows = (kTileN + plan.split_k - 1) / plan.split_k;
     args.flags = plan.prefetch_weights ? kFlagPrefetchW : 0;
     args.stage_bytes = tc_stage_bytes(BM, M, group);
@@ -688,7 +718,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     }
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(plan.split_k), static_cast<unsigned>(N / kTileN),
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.split_k), static_cast<unsigned>(tiles_n(N)),
                        static_cast<unsigned>((M + BM - 1) / BM));
     cfg.blockDim = dim3(32 * TcShape<BM>::kDq0 + 128 * NWG, 1, 1);
     cfg.dynamicSmemBytes = smem;

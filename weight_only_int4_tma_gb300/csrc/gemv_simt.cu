@@ -115,6 +115,40 @@ __device__ __forceinline__ void chunk_fma(const uint4 v, uint32_t zp, uint32_t s
     }
 }
 
+// One 128-K block of this thread's channel from its ring stage: w_s = its 64 nibble bytes
+// (chunk c at + c * 4 KB), sz_s = its scale / zero words (group gi at + 8 gi).
+// kChunks = 4: a full block (no per-chunk test); 0: only the first nck chunks.
+template <int MM, int DT, int kChunks>
+__device__ __forceinline__ void block_fma(uint32_t w_s, uint32_t sz_s, int gshift, bool has_z,
+                                          int r, const uint16_t* a_blk, int K, int M,
+                                          float (&acc)[MM][4], int nck = 4) {
+    uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
+    bool x16 = false;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (kChunks == 0 && c >= nck) break;
+        // the chunk starts a new group: c == 0 always, c == 2 for groups of 64 or 32,
+        // odd c for groups of 32
+        const bool fresh = c == 0 || (c == 2 && gshift <= 1) || ((c & 1) && gshift == 0);
+        if (fresh) {
+            const int gi = c >> gshift;
+            const uint32_t sw = lds_u32(sz_s + gi * 8);
+            const uint32_t sbits = (sw >> ((r & 1) * 16)) & 0xFFFFu;
+            uint32_t z = 8;
+            if (has_z) z = (lds_u32(sz_s + gi * 8 + 4) >> (((r >> 1) & 3) * 8 + (r & 1) * 4)) & 0xFu;
+            zp = zero_pair<DT>(z);
+            sp = scale_pair(sbits);
+            if constexpr (DT == 0) {
+                zp16 = zero_pair_x16(z);
+                sp16 = scale_pair_div16(sp);
+                x16 = f16_div16_exact(sp, sp16);
+            }
+        }
+        const uint4 v = lds_v4(w_s + c * (kGemvThreads * 16));
+        chunk_fma<MM, DT>(v, zp, sp, zp16, sp16, x16, a_blk + c * kChunkK, K, M, acc);
+    }
+}
+
 template <int MM, int DT, int ROWS>
 __global__ void __launch_bounds__(kGemvThreads, 2) w4a16_gemv_kernel(
     const uint16_t* __restrict__ A, const uint8_t* __restrict__ packed,
@@ -154,8 +188,8 @@ __global__ void __launch_bounds__(kGemvThreads, 2) w4a16_gemv_kernel(
     const uint32_t zoff = kNibbleBytes + scale_bytes(group);
     const int G = groups_per_block(group);
     const int gshift = group == 128 ? 2 : (group == 64 ? 1 : 0);
-    const int kblocks = K / kTileK;
-    const int units = N / ROWS;
+    const int kblocks = blocks_k(K);
+    const int units = tiles_n(N) * (kTileN / ROWS);
     const int grid = static_cast<int>(gridDim.x);
     const int u0 = static_cast<int>(blockIdx.x);
     const int nbs = slot < kblocks ? (kblocks - 1 - slot) / kSlots + 1 : 0;  // blocks per unit
@@ -206,32 +240,16 @@ __global__ void __launch_bounds__(kGemvThreads, 2) w4a16_gemv_kernel(
         for (int j = 0; j < nbs; ++j) {
             cp_async_wait<kGemvStages - 2>();  // this thread's copies of the item have landed
             const uint32_t so = static_cast<uint32_t>(cs_stage) * stage_bytes;
-            const uint16_t* a_blk = A + (slot + j * kSlots) * kTileK;
-            uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
-            bool x16 = false;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                // the chunk starts a new group: c == 0 always, c == 2 for groups of 64
-                // or 32, odd c for groups of 32
-                const bool fresh = c == 0 || (c == 2 && gshift <= 1) || ((c & 1) && gshift == 0);
-                if (fresh) {
-                    const int gi = c >> gshift;
-                    const uint32_t sw = lds_u32(my_sz + so + gi * 8);
-                    const uint32_t sbits = (sw >> ((r & 1) * 16)) & 0xFFFFu;
-                    uint32_t z = 8;
-                    if (has_z)
-                        z = (lds_u32(my_sz + so + gi * 8 + 4) >> (((r >> 1) & 3) * 8 + (r & 1) * 4)) & 0xFu;
-                    zp = zero_pair<DT>(z);
-                    sp = scale_pair(sbits);
-                    if constexpr (DT == 0) {
-                        zp16 = zero_pair_x16(z);
-                        sp16 = scale_pair_div16(sp);
-                        x16 = f16_div16_exact(sp, sp16);
-                    }
-                }
-                const uint4 v = lds_v4(my_w + so + c * (kGemvThreads * 16));
-                chunk_fma<MM, DT>(v, zp, sp, zp16, sp16, x16, a_blk + c * kChunkK, K, M, acc);
-            }
+            const int kb = slot + j * kSlots;
+            const uint16_t* a_blk = A + kb * kTileK;
+            // chunks of the block inside K (all 4 except in a padded last block, whose
+            // chunks past K have zero weights and must not read A)
+            const int nck = (kb + 1) * kTileK <= K ? 4 : (K - kb * kTileK) / kChunkK;
+            if (nck == 4)
+                block_fma<MM, DT, 4>(my_w + so, my_sz + so, gshift, has_z, r, a_blk, K, M, acc);
+            else
+                block_fma<MM, DT, 0>(my_w + so, my_sz + so, gshift, has_z, r, a_blk, K, M, acc,
+                                     nck);
             // refill the stage consumed one item ago (its shared-memory reads are done)
             if (issued < total) { issue_next(); ++issued; }
             cp_async_commit();
@@ -244,7 +262,7 @@ __global__ void __launch_bounds__(kGemvThreads, 2) w4a16_gemv_kernel(
         __syncthreads();  // one barrier per unit: red is double-buffered by unit parity
         for (int e = tid; e < MM * ROWS; e += kGemvThreads) {
             const int m = e / ROWS, jr = e - (e / ROWS) * ROWS;
-            if (m < M) {
+            if (m < M && n0 + jr < N) {  // channels past N are padding
                 float sum = 0.0f;
 #pragma unroll
                 for (int p = 0; p < kSlots; ++p) sum += red[ui & 1][p][m][jr];
@@ -285,7 +303,7 @@ int launch_gemv_instance(const DeviceCtx& ctx, const void* A, const void* packed
         occ[gidx] = 0;
         return -3;
     }
-    const int units = N / ROWS;
+    const int units = tiles_n(N) * (kTileN / ROWS);
     const int slots = occ[gidx] * ctx.num_sms;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(units < slots ? units : slots), 1, 1);

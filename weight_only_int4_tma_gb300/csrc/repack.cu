@@ -33,37 +33,47 @@ __global__ void __launch_bounds__(512) repack_kernel(
     const uint32_t* __restrict__ qzeros, const uint16_t* __restrict__ cscale, int N, int K,
     int group, int dtype, uint8_t* __restrict__ packed, uint32_t bb, uint64_t cs_off,
     uint64_t total) {
-    const int kblocks = K / kTileK;
+    const int kblocks = blocks_k(K);
     const int nt = blockIdx.x / kblocks;
     const int kb = blockIdx.x % kblocks;
     const int t = threadIdx.x;
     uint8_t* blk = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * bb;
     const int G = groups_per_block(group);
 
-    {   // nibbles: thread t -> chunk c = t / 128, row r = t % 128, four words
+    {   // nibbles: thread t -> chunk c = t / 128, row r = t % 128, four words (zero where
+        // the row is past N or the chunk past K; K is a multiple of 32, so a chunk is
+        // either wholly inside or wholly outside)
         const int c = t >> 7, r = t & 127;
         const int n = nt * kTileN + r;
-        const uint4 src = *reinterpret_cast<const uint4*>(
-            qweight + static_cast<size_t>(n) * (K / 8) + kb * (kTileK / 8) + c * 4);
-        uint4 dst;
-        dst.x = permute_nibbles(src.x);
-        dst.y = permute_nibbles(src.y);
-        dst.z = permute_nibbles(src.z);
-        dst.w = permute_nibbles(src.w);
+        uint4 dst = make_uint4(0u, 0u, 0u, 0u);
+        if (n < N && kb * kTileK + c * kChunkK < K) {
+            const uint4 src = *reinterpret_cast<const uint4*>(
+                qweight + static_cast<size_t>(n) * (K / 8) + kb * (kTileK / 8) + c * 4);
+            dst.x = permute_nibbles(src.x);
+            dst.y = permute_nibbles(src.y);
+            dst.z = permute_nibbles(src.z);
+            dst.w = permute_nibbles(src.w);
+        }
         *reinterpret_cast<uint4*>(blk + c * 2048 + r * 16) = dst;
     }
     const int gbase = kb * G;  // first global group index of this block
-    if (t < G * kTileN) {      // scales: [gi][r]
+    const int groups = K / group;
+    if (t < G * kTileN) {      // scales: [gi][r]; zero past N or K
         const int gi = t >> 7, r = t & 127;
-        const uint16_t s = scales[static_cast<size_t>(gbase + gi) * N + nt * kTileN + r];
+        const int n = nt * kTileN + r;
+        const uint16_t s = (n < N && gbase + gi < groups)
+                               ? scales[static_cast<size_t>(gbase + gi) * N + n] : uint16_t{0};
         reinterpret_cast<uint16_t*>(blk + kNibbleBytes)[gi * kTileN + r] = s;
     }
     if (qzeros != nullptr && t < G * (kTileN / 2)) {  // zeros: [gi][byte r/2]
         const int gi = t / (kTileN / 2), b = t % (kTileN / 2);
-        const int n0 = nt * kTileN + 2 * b;
-        const uint32_t* zrow = qzeros + static_cast<size_t>(gbase + gi) * (N / 8);
-        const uint32_t z0 = (zrow[n0 / 8] >> (4 * (n0 % 8))) & 0xFu;
-        const uint32_t z1 = (zrow[(n0 + 1) / 8] >> (4 * ((n0 + 1) % 8))) & 0xFu;
+        const int n0 = nt * kTileN + 2 * b;  // N is a multiple of 8: n0, n0 + 1 both in or out
+        uint32_t z0 = 8, z1 = 8;
+        if (n0 < N && gbase + gi < groups) {
+            const uint32_t* zrow = qzeros + static_cast<size_t>(gbase + gi) * (N / 8);
+            z0 = (zrow[n0 / 8] >> (4 * (n0 % 8))) & 0xFu;
+            z1 = (zrow[(n0 + 1) / 8] >> (4 * ((n0 + 1) % 8))) & 0xFu;
+        }
         blk[kNibbleBytes + scale_bytes(group) + gi * (kTileN / 2) + b] =
             static_cast<uint8_t>(z0 | (z1 << 4));
     }
@@ -107,9 +117,10 @@ __global__ void __launch_bounds__(512) dequant_debug_kernel(const uint8_t* __res
     }
     const bool has_z = (flags & kFlagZeros) != 0;
     const uint32_t bb = block_bytes(group, has_z);
-    const int kblocks = K / kTileK;
+    const int kblocks = blocks_k(K);
     const int nt = blockIdx.x / kblocks, kb = blockIdx.x % kblocks;
     const int c = threadIdx.x >> 7, r = threadIdx.x & 127;
+    if (nt * kTileN + r >= N || kb * kTileK + c * kChunkK >= K) return;  // padding
     const uint8_t* blk = packed + kHeaderBytes + static_cast<size_t>(blockIdx.x) * bb;
     const int gi = (c * kChunkK) / group;
     const uint32_t sbits = reinterpret_cast<const uint16_t*>(blk + kNibbleBytes)[gi * kTileN + r];
@@ -160,7 +171,7 @@ int launch_repack(const DeviceCtx& ctx, const uint32_t* qweight, const void* sca
     (void)ctx;
     const bool z = qzeros != nullptr;
     const uint32_t bb = block_bytes(group, z);
-    const size_t blocks = static_cast<size_t>(N / kTileN) * (K / kTileK);
+    const size_t blocks = static_cast<size_t>(tiles_n(N)) * blocks_k(K);
     const uint64_t cs_off = kHeaderBytes + blocks * bb;
     const uint64_t total = cs_off + (cscale ? 4ull * N : 0ull);
     repack_kernel<<<static_cast<unsigned>(blocks), 512, 0, stream>>>(
@@ -174,7 +185,7 @@ int launch_repack(const DeviceCtx& ctx, const uint32_t* qweight, const void* sca
 
 int launch_dequant_debug(const DeviceCtx& ctx, const void* packed, int N, int K, int group,
                          int dtype, void* W_out, cudaStream_t stream) {
-    const unsigned blocks = static_cast<unsigned>((N / kTileN) * (K / kTileK));
+    const unsigned blocks = static_cast<unsigned>(tiles_n(N) * blocks_k(K));
     const uint8_t* p = static_cast<const uint8_t*>(packed);
     uint16_t* w = static_cast<uint16_t*>(W_out);
     if (dtype == 0)
