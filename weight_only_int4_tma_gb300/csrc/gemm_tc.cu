@@ -14,12 +14,18 @@
 //   epilogue: tcgen05.ld -> (split-K: each CTA of the cluster owns a slice of the 128
 //        channels; the others push their fp32 partials for it into its shared memory
 //        with bulk DSMEM copies; the owner sums them in rank order) -> x per-channel
-//        factor -> round to dtype -> Y  ("量化开销对比" §6.2 "最后：累加器 × s_x → +bias →
-//        写出", §6.7 folding)
+//        factor -> optional + bias, activation, + residual -> round to dtype -> Y
+//        ("量化开销对比" §6.2 "最后：累加器 × s_x → +bias → 写出", §6.6, §6.7 folding)
 //
-// Warp roles: warp 0 = TMA producer, warp 1 = TMEM allocator + single-thread MMA issuer,
-// warps 2.. = dequant warps (4 per warpgroup; warp w may only touch TMEM lanes
-// 32*(w%4)..+31, so each warpgroup covers all 128 lanes) which also run the epilogue.
+// Warp roles: warp 0 = TMA producer; warps 1..NMI = MMA issuers, one thread each (two for
+// decode tiles of <= 32 rows, taking even / odd 128-K blocks into two accumulators;
+// warp 1 also allocates TMEM); then the dequant warps, 4 per warpgroup (warp w may only
+// touch TMEM lanes 32*(w%4)..+31, so each warpgroup covers all 128 lanes), which also run
+// the epilogue.  Decode tiles: warpgroup g unpacks whole blocks g, g + NWG, ...; larger
+// tiles: every warpgroup unpacks its chunks of every block.  Each mbarrier has a single
+// waiting party that passes every one of its phases (tfull per issuer and W buffer,
+// tempty per warpgroup and W buffer), because a parity wait only tells the current phase
+// from the one before it.
 //
 // Programmatic dependent launch: the prologue (barriers, TMEM, descriptor prefetch and,
 // unless disabled, the header check and the first ring stages of packed weights) runs
