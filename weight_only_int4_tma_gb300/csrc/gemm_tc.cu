@@ -36,6 +36,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstddef>
+#include <cstring>
 #include <mutex>
 
 #include "dequant.cuh"
@@ -183,38 +185,63 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         W4G_TRACE(59, smid_);
     }
 #endif
-    if (threadIdx.x == 0) {
-        W4G_TRACE(0, W4G_NOW());
-        *abort_flag = 0;
-        for (int s = 0; s < args.stages; ++s) {
+    // Thread 0 issues the header load first (its latency overlaps the barrier setup; with
+    // weight prefetch disabled it must wait for the previous kernel instead), and warp 0
+    // spreads the barrier initialisation over its lanes.
+    uint4 hv[4];
+    if (threadIdx.x == 0 && prefetch_w) {
+        const uint4* hp = reinterpret_cast<const uint4*>(args.packed);
+        for (int i = 0; i < 4; ++i) hv[i] = hp[i];
+    }
+    if (warp == 0) {
+        if (lane == 0) {
+            W4G_TRACE(0, W4G_NOW());
+            *abort_flag = 0;
+        }
+        for (int s = lane; s < args.stages; s += 32) {
             mbar_init(full0 + 8 * s, 1);
             // a stage is free once every issuer that read it has committed
             mbar_init(empty0 + 8 * s, (kNMI == 2 && args.kps == 2) ? 2 : 1);
         }
-        for (int t = 0; t < kNMI * kTBuf; ++t)  // the warps that write a block's W tile
+        for (int t = lane; t < kNMI * kTBuf; t += 32)  // the warps that write a block's W tile
             mbar_init(tfull0 + 8 * t, S::kInterleave ? 4 : 4 * NWG);
-        for (int t = 0; t < NWG * kTBuf; ++t)
+        for (int t = lane; t < NWG * kTBuf; t += 32)
             mbar_init(tempty0 + 8 * t, 1);  // one MMA commit
-        mbar_init(accum_bar, kNMI);
-        mbar_init(recv_bar, 1);
+        if (lane == 0) {
+            mbar_init(accum_bar, kNMI);
+            mbar_init(recv_bar, 1);
+        }
         fence_mbar_init();
-        if (args.splits > 1)  // partials of the other ranks for this rank's slice
-            mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(args.splits - 1) * slice_bytes);
-        if (!prefetch_w) grid_dep_wait();
-        const PackedHeader* h = reinterpret_cast<const PackedHeader*>(args.packed);
-        const int flags = check_header(h, args.N, args.K, args.group, DT);
-        info[0] = flags;
-        info[1] = flags < 0 ? 0 : static_cast<int>(h->block_bytes);
-        *cs_slot = (flags >= 0 && (flags & kFlagChannelScale))
-                       ? reinterpret_cast<const float*>(args.packed + h->cscale_offset)
-                       : nullptr;
-        if (flags < 0 && split == 0 && n_tile == 0 && m_tile == 0)
-            record_status(args.status, kStatusFormat);
-        prefetch_tensormap(&tmap_a);
+        if (lane == 0) {
+            if (args.splits > 1)  // partials of the other ranks for this rank's slice
+                mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(args.splits - 1) * slice_bytes);
+            W4G_TRACE(61, W4G_NOW());
+            if (!prefetch_w) {
+                grid_dep_wait();
+                const uint4* hp = reinterpret_cast<const uint4*>(args.packed);
+                for (int i = 0; i < 4; ++i) hv[i] = hp[i];
+            }
+            PackedHeader hl;  // the first 64 bytes: every field the check reads
+            static_assert(offsetof(PackedHeader, total_bytes) + 8 <= 64, "header prefix");
+            memcpy(&hl, hv, sizeof(hv));
+            const int flags = check_header(&hl, args.N, args.K, args.group, DT);
+            info[0] = flags;
+            info[1] = flags < 0 ? 0 : static_cast<int>(hl.block_bytes);
+            *cs_slot = (flags >= 0 && (flags & kFlagChannelScale))
+                           ? reinterpret_cast<const float*>(args.packed + hl.cscale_offset)
+                           : nullptr;
+            if (flags < 0 && split == 0 && n_tile == 0 && m_tile == 0)
+                record_status(args.status, kStatusFormat);
+            prefetch_tensormap(&tmap_a);
+            W4G_TRACE(62, W4G_NOW());
+        }
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), S::kTmemCols);
         tmem_relinquish();
+#ifdef W4A16_TRACE
+        if (lane == 0) *reinterpret_cast<unsigned long long*>(ctrl_ptr + 696) = W4G_NOW();
+#endif
     }
     tc_fence_before();
     __syncthreads();
@@ -225,7 +252,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const uint32_t tmem = *tmem_slot;
 #ifdef W4A16_TRACE
     trace_rec = *reinterpret_cast<const unsigned*>(ctrl_ptr + 488);
-    if (threadIdx.x == 0) W4G_TRACE(1, W4G_NOW());
+    if (threadIdx.x == 0) {
+        W4G_TRACE(1, W4G_NOW());
+        W4G_TRACE(63, *reinterpret_cast<const unsigned long long*>(ctrl_ptr + 696));
+    }
 #endif
     const int flags = info[0];
     const bool run = flags >= 0 && nkb > 0;
