@@ -149,9 +149,13 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         : ring_bytes;
     const uint32_t ctrl = base + ctrl_off;
     uint8_t* ctrl_ptr = base_ptr + ctrl_off;
-    // control block: full[16] empty[16] tfull[issuer][W buffer] (8)
-    // tempty[warpgroup][W buffer] (16) accum recv, then scalars
+    // control block: full[16] (weights of a stage) empty[16] tfull[issuer][W buffer] (8)
+    // tempty[warpgroup][W buffer] (16) accum recv, scalars, then afull[16] (A of a stage)
     const uint32_t full0 = ctrl, empty0 = ctrl + 128, tfull0 = ctrl + 256, tempty0 = ctrl + 320;
+    // Decode tiles give the A part of a stage its own barrier, so the weights can be
+    // unpacked into TMEM before the previous kernel has finished (programmatic dependent
+    // launch); larger tiles track both parts of a stage on full[].
+    const uint32_t afull0 = S::kInterleave ? ctrl + 768 : full0;
     const uint32_t accum_bar = ctrl + 448;
     const uint32_t recv_bar = ctrl + 456;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl_ptr + 464);
@@ -200,6 +204,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         }
         for (int s = lane; s < args.stages; s += 32) {
             mbar_init(full0 + 8 * s, 1);
+            if (S::kInterleave) mbar_init(afull0 + 8 * s, 1);
             // a stage is free once every issuer that read it has committed
             mbar_init(empty0 + 8 * s, (kNMI == 2 && args.kps == 2) ? 2 : 1);
         }
@@ -281,7 +286,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             for (int i = 0; i < pre; ++i) {  // weights do not depend on the previous grid
                 const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
                 const int nblk = min(kps, nkb - i * kps);
-                mbar_arrive_expect_tx(full0 + 8 * i, nblk * bb + a_bytes);
+                mbar_arrive_expect_tx(full0 + 8 * i, nblk * bb + (S::kInterleave ? 0u : a_bytes));
                 tma_bulk_g2s(st + a_bytes, src + static_cast<size_t>(i) * kps * bb, nblk * bb,
                              full0 + 8 * i, pol_w);
             }
@@ -297,7 +302,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             };
             for (int i = 0; i < pre; ++i) {
                 const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
-                load_a(st, (kb0 + i * kps) * 2, full0 + 8 * i);
+                if (S::kInterleave) mbar_arrive_expect_tx(afull0 + 8 * i, a_bytes);
+                load_a(st, (kb0 + i * kps) * 2, afull0 + 8 * i);
                 if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
             }
             int issued = pre;
@@ -312,11 +318,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     !mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, args.status, tlim))
                     break;
                 const uint32_t st = base + static_cast<uint32_t>(s) * args.stage_bytes;
-                const uint32_t fb = full0 + 8 * s;
+                const uint32_t fb = full0 + 8 * s, ab = afull0 + 8 * s;
                 const int nblk = left < kps ? left : kps;
-                mbar_arrive_expect_tx(fb, nblk * bb + a_bytes);
+                mbar_arrive_expect_tx(fb, nblk * bb + (S::kInterleave ? 0u : a_bytes));
                 tma_bulk_g2s(st + a_bytes, wsrc, nblk * bb, fb, pol_w);
-                load_a(st, kchunk, fb);
+                if (S::kInterleave) mbar_arrive_expect_tx(ab, a_bytes);
+                load_a(st, kchunk, ab);
                 if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
                 ++issued;
                 left -= kps;
@@ -332,6 +339,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     const uint32_t ph = static_cast<uint32_t>(i / args.stages) & 1u;
                     int dummy = 0;
                     (void)mbar_wait_bounded(full0 + 8 * s, ph, &dummy, nullptr, tlim);
+                    if (S::kInterleave)
+                        (void)mbar_wait_bounded(afull0 + 8 * s, ph, &dummy, nullptr, tlim);
                 }
             }
         }
@@ -353,8 +362,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             uint32_t ph = 0;
             uint32_t fpar = 0;  // bit t: parity of this issuer's next wait on tfull[k][t]
             for (int i = k; i < nkb; i += kNMI) {   // i: 128-K block
+                // the weights of block i are known to have landed through tfull (its
+                // dequant waited for them); this wait is for the stage's A
                 ok = (kNMI == 1 && b != 0) ||
-                     mbar_wait_spin(full0 + 8 * s, ph, abort_flag, args.status, tlim);
+                     mbar_wait_spin(afull0 + 8 * s, ph, abort_flag, args.status, tlim);
                 ok = ok && mbar_wait_spin(tfull0 + 8 * (k * kTBuf + t), (fpar >> t) & 1u,
                                           abort_flag, args.status, tlim);
                 fpar ^= 1u << t;
