@@ -130,6 +130,70 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// One 128 x 128 block, one weight row r per thread, written as 64 TMEM columns at taddr
+// (four 32-K chunks of 16 columns).  kGS = 32-K chunks per quantisation group (4, 2, 1
+// for groups of 128, 64, 32); kX16 selects the fp16 variant that masks the odd pairs in
+// place (valid when s/16 is exact for every group of the block).
+template <int DT, int kGS, bool kX16>
+__device__ __forceinline__ void unpack_block_rows(const uint8_t* wb, int r,
+                                                  const uint32_t (&sb)[4 / kGS],
+                                                  const uint32_t (&zb)[4 / kGS], uint32_t taddr) {
+    uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        if (c % kGS == 0) {  // first chunk of a group: its (group, row) constants
+            const uint32_t z = (zb[c / kGS] >> ((r & 1) * 4)) & 0xFu;  // 8 when no zeros
+            zp = zero_pair<DT>(z);
+            sp = scale_pair(sb[c / kGS]);
+            if constexpr (kX16) {
+                zp16 = zero_pair_x16(z);
+                sp16 = scale_pair_div16(sp);
+            }
+        }
+        const uint4 v = *reinterpret_cast<const uint4*>(wb + c * 2048 + r * 16);
+        uint32_t out[16];
+        if constexpr (kX16) {
+            dequant_word_f16_x16(v.x, zp, sp, zp16, sp16, out + 0);
+            dequant_word_f16_x16(v.y, zp, sp, zp16, sp16, out + 4);
+            dequant_word_f16_x16(v.z, zp, sp, zp16, sp16, out + 8);
+            dequant_word_f16_x16(v.w, zp, sp, zp16, sp16, out + 12);
+        } else {
+            dequant_word<DT>(v.x, zp, sp, out + 0);
+            dequant_word<DT>(v.y, zp, sp, out + 4);
+            dequant_word<DT>(v.z, zp, sp, out + 8);
+            dequant_word<DT>(v.w, zp, sp, out + 12);
+        }
+        tmem_st16(taddr + c * 16, out);
+    }
+}
+
+// Loads the block's group scales and zeros for row r, takes the fp16 x16 decision once for
+// the whole block (warp vote), and unpacks it.
+template <int DT, int kGS>
+__device__ __forceinline__ void unpack_block(const uint8_t* wb, int r, uint32_t zoff,
+                                             bool has_z, uint32_t taddr) {
+    constexpr int kG = 4 / kGS;
+    uint32_t sb[kG], zb[kG];
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+        sb[g] = reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[g * kTileN + r];
+        zb[g] = has_z ? wb[zoff + g * (kTileN / 2) + (r >> 1)] : 0x88u;
+    }
+    if constexpr (DT == 0) {
+        bool exact = true;
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const uint32_t sp = scale_pair(sb[g]);
+            exact = exact && f16_div16_exact(sp, scale_pair_div16(sp));
+        }
+        if (__all_sync(0xffffffffu, exact)) {
+            unpack_block_rows<DT, kGS, true>(wb, r, sb, zb, taddr);
+            return;
+        }
+    }
+    unpack_block_rows<DT, kGS, false>(wb, r, sb, zb, taddr);
+}
+
 template <int BM, int NWG, int DT>
 __global__ void __launch_bounds__(32 * (1 + TcShape<BM>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
@@ -463,42 +527,50 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(18 + i, W4G_NOW());
             const uint8_t* wb = base_ptr + a_bytes + static_cast<size_t>(s) * args.stage_bytes +
                                 static_cast<size_t>(b) * bb;
-            int cur_g = -1;
-            uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
-            bool x16 = false;
+            if constexpr (S::kInterleave) {  // whole block by this warpgroup
+                const uint32_t taddr = tmem + lane_base + S::kACol0 + t * 64;
+                if (gshift == 2) unpack_block<DT, 4>(wb, r, zoff, has_z, taddr);
+                else if (gshift == 1) unpack_block<DT, 2>(wb, r, zoff, has_z, taddr);
+                else unpack_block<DT, 1>(wb, r, zoff, has_z, taddr);
+            } else {  // this warpgroup's chunks of the block
+                int cur_g = -1;
+                uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
+                bool x16 = false;
 #pragma unroll
-            for (int j = 0; j < kCpw; ++j) {
-                const int c = S::kInterleave ? j : wg + j * NWG;  // 32-K chunk
-                if (!S::kInterleave && c >= 4) break;
-                const int gi = c >> gshift;
-                if (gi != cur_g) {  // per-(group, row) constants
-                    cur_g = gi;
-                    const uint32_t sbits =
-                        reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[gi * kTileN + r];
-                    uint32_t z = 8;
-                    if (has_z) z = (wb[zoff + gi * (kTileN / 2) + (r >> 1)] >> ((r & 1) * 4)) & 0xFu;
-                    zp = zero_pair<DT>(z);
-                    sp = scale_pair(sbits);
-                    if constexpr (DT == 0) {
-                        zp16 = zero_pair_x16(z);
-                        sp16 = scale_pair_div16(sp);
-                        x16 = __all_sync(0xffffffffu, f16_div16_exact(sp, sp16));
+                for (int j = 0; j < kCpw; ++j) {
+                    const int c = wg + j * NWG;  // 32-K chunk
+                    if (c >= 4) break;
+                    const int gi = c >> gshift;
+                    if (gi != cur_g) {  // per-(group, row) constants
+                        cur_g = gi;
+                        const uint32_t sbits =
+                            reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[gi * kTileN + r];
+                        uint32_t z = 8;
+                        if (has_z)
+                            z = (wb[zoff + gi * (kTileN / 2) + (r >> 1)] >> ((r & 1) * 4)) & 0xFu;
+                        zp = zero_pair<DT>(z);
+                        sp = scale_pair(sbits);
+                        if constexpr (DT == 0) {
+                            zp16 = zero_pair_x16(z);
+                            sp16 = scale_pair_div16(sp);
+                            x16 = __all_sync(0xffffffffu, f16_div16_exact(sp, sp16));
+                        }
                     }
+                    const uint4 v = *reinterpret_cast<const uint4*>(wb + c * 2048 + r * 16);
+                    uint32_t out[16];
+                    if (DT == 0 && x16) {
+                        dequant_word_f16_x16(v.x, zp, sp, zp16, sp16, out + 0);
+                        dequant_word_f16_x16(v.y, zp, sp, zp16, sp16, out + 4);
+                        dequant_word_f16_x16(v.z, zp, sp, zp16, sp16, out + 8);
+                        dequant_word_f16_x16(v.w, zp, sp, zp16, sp16, out + 12);
+                    } else {
+                        dequant_word<DT>(v.x, zp, sp, out + 0);
+                        dequant_word<DT>(v.y, zp, sp, out + 4);
+                        dequant_word<DT>(v.z, zp, sp, out + 8);
+                        dequant_word<DT>(v.w, zp, sp, out + 12);
+                    }
+                    tmem_st16(tmem + lane_base + S::kACol0 + t * 64 + c * 16, out);
                 }
-                const uint4 v = *reinterpret_cast<const uint4*>(wb + c * 2048 + r * 16);
-                uint32_t out[16];
-                if (DT == 0 && x16) {
-                    dequant_word_f16_x16(v.x, zp, sp, zp16, sp16, out + 0);
-                    dequant_word_f16_x16(v.y, zp, sp, zp16, sp16, out + 4);
-                    dequant_word_f16_x16(v.z, zp, sp, zp16, sp16, out + 8);
-                    dequant_word_f16_x16(v.w, zp, sp, zp16, sp16, out + 12);
-                } else {
-                    dequant_word<DT>(v.x, zp, sp, out + 0);
-                    dequant_word<DT>(v.y, zp, sp, out + 4);
-                    dequant_word<DT>(v.z, zp, sp, out + 8);
-                    dequant_word<DT>(v.w, zp, sp, out + 12);
-                }
-                tmem_st16(tmem + lane_base + S::kACol0 + t * 64 + c * 16, out);
             }
             tmem_wait_st();
             tc_fence_before();
