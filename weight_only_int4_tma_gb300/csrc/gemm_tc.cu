@@ -413,7 +413,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     } else if (warp <= kNMI) {
         // ---------------- MMA issuers (one thread per warp) ----------------
         const int k = warp - 1;  // issuer index: blocks k, k + kNMI, ...
-        if (lane == 0 && run) {
+        // The whole warp runs the loop (warp-uniform control and operand arithmetic);
+        // lane 0 issues the MMAs and the commits that track them.
+        if (run) {
             constexpr uint32_t idesc = idesc_f16(DT, 128, BM);
             // Descriptor of chunk c, 16-K step q of the A tile in a stage = descriptor of
             // the stage base + (c * a_chunk + 32 q) / 16; only the start address moves.
@@ -429,43 +431,46 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 // the weights of block i are known to have landed through tfull (its
                 // dequant waited for them); this wait is for the stage's A
                 ok = (kNMI == 1 && b != 0) ||
-                     mbar_wait_spin(afull0 + 8 * s, ph, abort_flag, args.status, tlim);
-                ok = ok && mbar_wait_spin(tfull0 + 8 * (k * kTBuf + t), (fpar >> t) & 1u,
-                                          abort_flag, args.status, tlim);
+                     mbar_wait_spin_warp(afull0 + 8 * s, ph, abort_flag, args.status, tlim);
+                ok = ok && mbar_wait_spin_warp(tfull0 + 8 * (k * kTBuf + t), (fpar >> t) & 1u,
+                                               abort_flag, args.status, tlim);
                 fpar ^= 1u << t;
                 if (!ok) break;
-                if (i < 8) W4G_TRACE(34 + i, W4G_NOW());
+                if (lane == 0 && i < 8) W4G_TRACE(34 + i, W4G_NOW());
                 tc_fence_after();
                 const uint64_t d0 = sw128_desc(base + static_cast<uint32_t>(s) * args.stage_bytes) +
                                     static_cast<uint64_t>(2 * b) * chunk16;
                 const uint64_t d1 = d0 + chunk16;
                 const uint32_t a0 = tmem + S::kACol0 + t * 64;
-                tc_mma_ts(dacc, a0, d0, idesc, i >= kNMI ? 1u : 0u);
-                tc_mma_ts(dacc, a0 + 8, d0 + 2, idesc, 1u);
-                tc_mma_ts(dacc, a0 + 16, d0 + 4, idesc, 1u);
-                tc_mma_ts(dacc, a0 + 24, d0 + 6, idesc, 1u);
-                tc_mma_ts(dacc, a0 + 32, d1, idesc, 1u);
-                tc_mma_ts(dacc, a0 + 40, d1 + 2, idesc, 1u);
-                tc_mma_ts(dacc, a0 + 48, d1 + 4, idesc, 1u);
-                tc_mma_ts(dacc, a0 + 56, d1 + 6, idesc, 1u);
                 // the W buffer is free for its next block, i + kTBuf (unpacked by warpgroup
                 // (i + kTBuf) % NWG when warpgroups take whole blocks, else by all)
-                tc_commit(tempty0 + 8 * ((S::kInterleave ? (i + kTBuf) % NWG : 0) * kTBuf + t));
-                if (i < 8) W4G_TRACE(42 + i, W4G_NOW());
+                const uint32_t te =
+                    tempty0 + 8 * ((S::kInterleave ? (i + kTBuf) % NWG : 0) * kTBuf + t);
+                const bool stage_done = kNMI == 2 || b + 1 == kps || i == nkb - 1;
+                if (lane == 0) {
+                    tc_mma_ts(dacc, a0, d0, idesc, i >= kNMI ? 1u : 0u);
+                    tc_mma_ts(dacc, a0 + 8, d0 + 2, idesc, 1u);
+                    tc_mma_ts(dacc, a0 + 16, d0 + 4, idesc, 1u);
+                    tc_mma_ts(dacc, a0 + 24, d0 + 6, idesc, 1u);
+                    tc_mma_ts(dacc, a0 + 32, d1, idesc, 1u);
+                    tc_mma_ts(dacc, a0 + 40, d1 + 2, idesc, 1u);
+                    tc_mma_ts(dacc, a0 + 48, d1 + 4, idesc, 1u);
+                    tc_mma_ts(dacc, a0 + 56, d1 + 6, idesc, 1u);
+                    tc_commit(te);
+                    if (stage_done) tc_commit(empty0 + 8 * s);
+                    if (i < 8) W4G_TRACE(42 + i, W4G_NOW());
+                }
+                __syncwarp();
                 t += kNMI;
                 if (t >= kTBuf) t -= kTBuf;
-                if (kNMI == 2) {
-                    tc_commit(empty0 + 8 * s);
-                    if (++s == args.stages) { s = 0; ph ^= 1u; }
-                } else if (++b == kps || i == nkb - 1) {
-                    tc_commit(empty0 + 8 * s);
-                    b = 0;
-                    if (++s == args.stages) { s = 0; ph ^= 1u; }
-                }
+                if (kNMI == 1) b = stage_done ? 0 : b + 1;
+                if (stage_done && ++s == args.stages) { s = 0; ph ^= 1u; }
             }
-            tc_commit(accum_bar);
-            W4G_TRACE(50, W4G_NOW());
-            if (!ok) {  // make sure no MMA is still reading TMEM/SMEM when the CTA exits
+            if (lane == 0) {
+                tc_commit(accum_bar);
+                W4G_TRACE(50, W4G_NOW());
+            }
+            if (!ok && lane == 0) {  // no MMA may still read TMEM/SMEM when the CTA exits
                 int dummy = 0;
                 (void)mbar_wait_bounded(accum_bar, 0, &dummy, nullptr, tlim);
             }

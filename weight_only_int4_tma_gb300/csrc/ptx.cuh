@@ -168,6 +168,14 @@ __device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity,
     return __all_sync(0xffffffffu, ok);
 }
 
+// Warp-uniform form of mbar_wait_spin.
+__device__ __forceinline__ bool mbar_wait_spin_warp(uint32_t bar, uint32_t parity,
+                                                    volatile int* abort_flag, int* status,
+                                                    uint64_t limit_ns) {
+    const bool ok = mbar_wait_spin(bar, parity, abort_flag, status, limit_ns);
+    return __all_sync(0xffffffffu, ok);
+}
+
 // ---- L2 cache policies -------------------------------------------------------------
 __device__ __forceinline__ uint64_t policy_evict_first() {
     uint64_t p;
