@@ -500,28 +500,19 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         // multiple of NWG / blocks-per-stage when groups take whole blocks).
         constexpr int kBStep = S::kInterleave ? NWG : 1;         // block stride of a group
         constexpr int kCpw = S::kInterleave ? 4 : (4 + NWG - 1) / NWG;  // chunks per block
+        // Decode tiles hold two blocks per ring stage, so warpgroup wg reads block wg % 2 of
+        // stages wg / 2, wg / 2 + NWG / 2, ... (the host keeps the ring depth a multiple
+        // of NWG / 2) and uses W buffers wg, wg + NWG, ... mod kTBuf.
+        static_assert(!S::kInterleave || NWG % 2 == 0, "decode tiles: an even group count");
         const int tw = S::kInterleave ? wg : 0;                  // tempty party
-        int cur_p = 0, s = 0;   // a ring stage, its slot and the parity of that use
-        uint32_t ph = 0;
-        bool waited = false;    // stage cur_p's full barrier already passed
-        int b = 0, t = 0;       // block i's place in its stage, its W buffer
+        int s = S::kInterleave ? wg / 2 : 0;  // ring slot of block i, and the parity
+        uint32_t ph = 0;                      // of that use of the slot
+        int b = S::kInterleave ? wg % 2 : 0;  // block i's place in its stage
+        int t = S::kInterleave ? wg % kTBuf : 0;  // its W buffer
         uint32_t epar = 0;      // bit t: parity of this warp's next wait on tempty[tw][t]
         for (int i = S::kInterleave ? wg : 0; i < nkb && ok; i += kBStep) {   // 128-K block
-            if constexpr (S::kInterleave) {
-                const int p = args.kps == 2 ? (i >> 1) : i;  // ring stage of block i
-                b = i - p * args.kps;
-                t = i % kTBuf;
-                if (p != cur_p || !waited) {
-                    while (cur_p < p) {
-                        ++cur_p;
-                        if (++s == args.stages) { s = 0; ph ^= 1u; }
-                    }
-                    ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
-                    waited = true;
-                }
-            } else if (b == 0) {  // every block, in order: (s, b, t) advance at the loop end
+            if (S::kInterleave || b == 0)  // (s, b, t) advance at the loop end
                 ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
-            }
             if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(10 + i, W4G_NOW());
             if (ok && i >= kTBuf) {
                 ok = mbar_wait_warp(tempty0 + 8 * (tw * kTBuf + t), (epar >> t) & 1u, abort_flag,
@@ -582,7 +573,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             __syncwarp();
             if (lane == 0) mbar_arrive(tfull0 + 8 * ((i % kNMI) * kTBuf + t));
             if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(26 + i, W4G_NOW());
-            if constexpr (!S::kInterleave) {
+            if constexpr (S::kInterleave) {
+                s += NWG / 2;
+                if (s >= args.stages) { s -= args.stages; ph ^= 1u; }
+                t += NWG % kTBuf;
+                if (t >= kTBuf) t -= kTBuf;
+            } else {
                 if (++t == kTBuf) t = 0;
                 if (++b == args.kps) {
                     b = 0;
