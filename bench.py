@@ -52,6 +52,9 @@ def parse():
                     choices=["none", "bias", "bias_relu", "bias_silu", "bias_residual",
                              "bias_silu_residual"],
                     help="fuse a bias / activation / residual epilogue into every GEMM")
+    ap.add_argument("--dequant", default="magic", choices=["magic", "lut"],
+                    help="weight unpack of the tensor-core decode tiles: exponent injection "
+                         "(default) or the 16-entry shared-memory table (same results)")
     ap.add_argument("--shape", action="append", default=[],
                     help="restrict the workload to this shape tag (repeatable; profiling)")
     return ap.parse_args()
@@ -327,7 +330,10 @@ def run_ours(a):
         Y = torch.empty((c.M, c.N), dtype=torch.int16, device=device)
         bufs.append((c, reps, A, Y))
     torch.cuda.synchronize()
-    ex = dict(kernel=a.kernel, split_k=a.split_k, tile_m=a.tile_m, stages=a.stages)
+    ex = dict(kernel=a.kernel, split_k=a.split_k, tile_m=a.tile_m, stages=a.stages,
+              flags=w4.W4A16_GEMM_DEQUANT_LUT if a.dequant == "lut" else 0)
+    # the plain public call when every launch option is the library's default
+    default_launch = not any(ex.values())
     # optional fused epilogue: a seeded bias per shape (resident, like the weights) and a
     # device-resident residual (the previous layer's output in a real forward pass)
     act = {"relu": w4.W4A16_ACT_RELU, "silu": w4.W4A16_ACT_SILU}
@@ -345,7 +351,7 @@ def run_ours(a):
     def gemm_call(j, A, packed, Y, stream_, public=False):
         c = bufs[j][0]
         if a.epilogue == "none":
-            if public:
+            if public and default_launch:
                 w4.w4a16_gemm(A, packed, c.M, c.N, c.K, c.group, c.dtype, Y, stream_)
             else:
                 w4.w4a16_gemm_ex(A, packed, c.M, c.N, c.K, c.group, c.dtype, Y, stream=stream_,
@@ -353,7 +359,8 @@ def run_ours(a):
         else:
             bias, res = epi[j]
             w4.w4a16_gemm_epilogue(A, packed, c.M, c.N, c.K, c.group, c.dtype, bias, res,
-                                   epi_act, Y, stream=stream_, **({} if public else ex))
+                                   epi_act, Y, stream=stream_,
+                                   **({} if public and default_launch else ex))
 
     # which of the two kernels each shape runs on (the library's own launch choice)
     kname = {w4.W4A16_KERNEL_TC: "w4a16_tc_kernel", w4.W4A16_KERNEL_SIMT: "w4a16_gemv_kernel"}
@@ -448,7 +455,9 @@ def run_ours(a):
     dom_bytes = sum(launch_bytes[j] for j in dom) / len(dom)
     dom_launch_s = sum(per_shape_ms[j] for j in dom) * 1e-3 / len(dom)
     achieved_gbs = dom_bytes / dom_launch_s / 1e9
-    traffic = profiled_traffic(a.workload, dominant)
+    # the recorded counters describe the default launch of the whole workload only
+    traffic = (profiled_traffic(a.workload, dominant)
+               if default_launch and a.epilogue == "none" and not a.shape else None)
     # Decode-sized workloads are bound by HBM (TB/s over algorithmic bytes); prefill and
     # batch-transition workloads (M >= 64 everywhere) by the tensor pipe (TFLOP/s).
     compute_bound = min(p["M"] for p in shapes) >= 64
@@ -569,7 +578,7 @@ def run_ours(a):
                    "timing": f"CUDA graph of {G} steps replayed; CUDA events on the launch "
                              f"stream around the whole timed region", "parallelism": f"replicas{ws}",
                    "kernel": a.kernel, "split_k": a.split_k, "tile_m": a.tile_m,
-                   "stages": a.stages},
+                   "stages": a.stages, **({"dequant": a.dequant} if a.dequant != "magic" else {})},
         "roofline": ({"bound": "tensor", "achieved": value, "peak": tflops_peak,
                       "unit": "TFLOP/s", "frac": value / tflops_peak, "traffic": traffic,
                       "peak_kind": f"{peak_kind} bf16 sustained (fp16 dense rate is the same)",

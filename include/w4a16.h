@@ -79,6 +79,14 @@ typedef enum w4a16_kernel {
  * before the GEMM in the same stream writes the packed blob itself; w4a16_repack needs
  * no flag (it ends with a launch that later kernels cannot overlap). */
 #define W4A16_GEMM_NO_WEIGHT_PREFETCH 2
+/* Unpack the weights through a 16-entry table in shared memory (nibble -> its value in
+ * the activation dtype; then the group's zero and scale, one rounding) instead of the
+ * exponent-injection unpack: "量化开销对比" §6.3 (16-entry LUT, then the group scale).
+ * Results are bit-identical to the default path; it is a measured alternative and is
+ * slower on this GPU.  Tensor-core kernel with 16- or 32-row tiles only: any other plan
+ * (the SIMT kernel, tile_m > 32, or M > 32 under the heuristic) returns
+ * W4A16_ERR_UNSUPPORTED. */
+#define W4A16_GEMM_DEQUANT_LUT 4
 
 typedef struct w4a16_gemm_config {
     int kernel;       /* w4a16_kernel; AUTO picks SIMT only if the three fields below

@@ -73,19 +73,22 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     // CUDA-core GEMV beats the tensor-core kernel there (the MMA's fixed issue cost and
     // the TMEM round trip of the unpacked tile dominate at one row, and the GEMV needs no
     // split-K reduction); longer K or more tiles favour the tensor-core kernel.
-    if (kernel == W4A16_KERNEL_AUTO && M == 1 && K <= 16384 && tiles_n(N) <= ctx.num_sms &&
-        !(cfg && (cfg->tile_m || cfg->split_k || cfg->stages)))
-        kernel = W4A16_KERNEL_SIMT;
     int flags = 0;
     if (cfg) {
         for (int i = 0; i < 3; ++i)
             if (cfg->reserved[i] != 0) return W4A16_ERR_INVALID_ARG;
-        if (cfg->flags & ~(W4A16_GEMM_NO_PDL | W4A16_GEMM_NO_WEIGHT_PREFETCH))
+        if (cfg->flags &
+            ~(W4A16_GEMM_NO_PDL | W4A16_GEMM_NO_WEIGHT_PREFETCH | W4A16_GEMM_DEQUANT_LUT))
             return W4A16_ERR_INVALID_ARG;
         flags = cfg->flags;
     }
+    plan->lut = (flags & W4A16_GEMM_DEQUANT_LUT) != 0;
+    if (kernel == W4A16_KERNEL_AUTO && M == 1 && K <= 16384 && tiles_n(N) <= ctx.num_sms &&
+        !plan->lut && !(cfg && (cfg->tile_m || cfg->split_k || cfg->stages)))
+        kernel = W4A16_KERNEL_SIMT;
     plan->pdl = (flags & W4A16_GEMM_NO_PDL) == 0;
     plan->prefetch_weights = plan->pdl && (flags & W4A16_GEMM_NO_WEIGHT_PREFETCH) == 0;
+    if (kernel == W4A16_KERNEL_SIMT && plan->lut) return W4A16_ERR_UNSUPPORTED;
     if (kernel == W4A16_KERNEL_SIMT) {
         if (M > 8) return W4A16_ERR_UNSUPPORTED;
         if (cfg && (cfg->split_k > 1 || cfg->stages != 0)) return W4A16_ERR_UNSUPPORTED;
@@ -112,6 +115,7 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
         else bm = 128;
     }
     if (bm != 16 && bm != 32 && bm != 64 && bm != 128 && bm != 256) return W4A16_ERR_UNSUPPORTED;
+    if (plan->lut && bm > 32) return W4A16_ERR_UNSUPPORTED;  // table unpack: decode tiles
     const int m_tiles = ceil_div(M, bm);
     if (m_tiles > 65535) return W4A16_ERR_UNSUPPORTED;
     const int base = n_tiles * m_tiles;
@@ -255,7 +259,8 @@ int w4a16_gemm_plan(int M, int N, int K, int group, int dtype, const w4a16_gemm_
     r.tile_m = plan.tile_m;
     r.stages = plan.stages;
     r.flags = (plan.pdl ? 0 : W4A16_GEMM_NO_PDL) |
-              (plan.prefetch_weights ? 0 : W4A16_GEMM_NO_WEIGHT_PREFETCH);
+              (plan.prefetch_weights ? 0 : W4A16_GEMM_NO_WEIGHT_PREFETCH) |
+              (plan.lut ? W4A16_GEMM_DEQUANT_LUT : 0);
     *out = r;
     return W4A16_OK;
 }

@@ -14,6 +14,9 @@
 //     w = t * s                     one rounding, to nearest even
 // with sub.rn / mul.rn on packed pairs: one LOP3 + one SUB + one MUL per pair of weights.
 #pragma once
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include <cstdint>
 
 namespace w4g {
@@ -116,6 +119,35 @@ __device__ __forceinline__ uint32_t scale_pair_div16(uint32_t sp) {
 // True when s/16 * 16 == s bit for bit, i.e. the division by 16 lost nothing.
 __device__ __forceinline__ bool f16_div16_exact(uint32_t sp, uint32_t sp16) {
     return mul_pair<0>(sp16, 0x4C004C00u) == sp;  // x 16
+}
+
+// ---- table variant ("量化开销对比" §6.3: nibble -> value through a 16-entry table in
+// shared memory, then the group's zero and scale) ----------------------------------------
+
+// Bits of the small integer q (0..15) in the activation dtype (exact).
+template <int DT>
+__device__ __forceinline__ uint16_t value_bits(int q) {
+    if constexpr (DT == 0) return __half_as_ushort(__float2half_rn(static_cast<float>(q)));
+    else return __bfloat16_as_ushort(__float2bfloat16_rn(static_cast<float>(q)));
+}
+
+// z in both halves, read from the table.
+__device__ __forceinline__ uint32_t lut_zero_pair(const uint16_t* lut, uint32_t z) {
+    return static_cast<uint32_t>(lut[z]) * 0x00010001u;
+}
+
+// Same output as dequant_word: each pair (q_2i, q_2i+1) is looked up in the table, then
+// (q - z) is formed exactly and multiplied by s with one rounding.
+template <int DT>
+__device__ __forceinline__ void dequant_word_lut(uint32_t x, const uint16_t* lut, uint32_t zp,
+                                                 uint32_t sp, uint32_t* out) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t lo = (x >> (4 * i)) & 0xFu;
+        const uint32_t hi = (x >> (4 * i + 16)) & 0xFu;
+        const uint32_t t = static_cast<uint32_t>(lut[lo]) | (static_cast<uint32_t>(lut[hi]) << 16);
+        out[i] = mul_pair<DT>(sub_pair<DT>(t, zp), sp);
+    }
 }
 
 }  // namespace w4g

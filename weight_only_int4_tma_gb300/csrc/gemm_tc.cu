@@ -130,29 +130,40 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Unpack modes of a decode-tile block.
+constexpr int kUnpackMagic = 0;     // exponent injection, pairs (k_2i, k_2i+1) shifted down
+constexpr int kUnpackMagicX16 = 1;  // fp16: odd pairs masked in place (s/16 exact)
+constexpr int kUnpackLut = 2;       // nibble -> value through a 16-entry shared table
+
 // One 128 x 128 block, one weight row r per thread, written as 64 TMEM columns at taddr
 // (four 32-K chunks of 16 columns).  kGS = 32-K chunks per quantisation group (4, 2, 1
-// for groups of 128, 64, 32); kX16 selects the fp16 variant that masks the odd pairs in
-// place (valid when s/16 is exact for every group of the block).
-template <int DT, int kGS, bool kX16>
+// for groups of 128, 64, 32).  lut: the shared 16-entry table (value bits of q = 0..15)
+// used by kUnpackLut.
+template <int DT, int kGS, int kMode>
 __device__ __forceinline__ void unpack_block_rows(const uint8_t* wb, int r,
                                                   const uint32_t (&sb)[4 / kGS],
-                                                  const uint32_t (&zb)[4 / kGS], uint32_t taddr) {
+                                                  const uint32_t (&zb)[4 / kGS], uint32_t taddr,
+                                                  const uint16_t* lut) {
     uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
         if (c % kGS == 0) {  // first chunk of a group: its (group, row) constants
             const uint32_t z = (zb[c / kGS] >> ((r & 1) * 4)) & 0xFu;  // 8 when no zeros
-            zp = zero_pair<DT>(z);
+            zp = kMode == kUnpackLut ? lut_zero_pair(lut, z) : zero_pair<DT>(z);
             sp = scale_pair(sb[c / kGS]);
-            if constexpr (kX16) {
+            if constexpr (kMode == kUnpackMagicX16) {
                 zp16 = zero_pair_x16(z);
                 sp16 = scale_pair_div16(sp);
             }
         }
         const uint4 v = *reinterpret_cast<const uint4*>(wb + c * 2048 + r * 16);
         uint32_t out[16];
-        if constexpr (kX16) {
+        if constexpr (kMode == kUnpackLut) {
+            dequant_word_lut<DT>(v.x, lut, zp, sp, out + 0);
+            dequant_word_lut<DT>(v.y, lut, zp, sp, out + 4);
+            dequant_word_lut<DT>(v.z, lut, zp, sp, out + 8);
+            dequant_word_lut<DT>(v.w, lut, zp, sp, out + 12);
+        } else if constexpr (kMode == kUnpackMagicX16) {
             dequant_word_f16_x16(v.x, zp, sp, zp16, sp16, out + 0);
             dequant_word_f16_x16(v.y, zp, sp, zp16, sp16, out + 4);
             dequant_word_f16_x16(v.z, zp, sp, zp16, sp16, out + 8);
@@ -168,16 +179,20 @@ __device__ __forceinline__ void unpack_block_rows(const uint8_t* wb, int r,
 }
 
 // Loads the block's group scales and zeros for row r, takes the fp16 x16 decision once for
-// the whole block (warp vote), and unpacks it.
-template <int DT, int kGS>
+// the whole block (warp vote), and unpacks it (kLut: through the shared table instead).
+template <int DT, int kGS, bool kLut>
 __device__ __forceinline__ void unpack_block(const uint8_t* wb, int r, uint32_t zoff,
-                                             bool has_z, uint32_t taddr) {
+                                             bool has_z, uint32_t taddr, const uint16_t* lut) {
     constexpr int kG = 4 / kGS;
     uint32_t sb[kG], zb[kG];
 #pragma unroll
     for (int g = 0; g < kG; ++g) {
         sb[g] = reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[g * kTileN + r];
         zb[g] = has_z ? wb[zoff + g * (kTileN / 2) + (r >> 1)] : 0x88u;
+    }
+    if constexpr (kLut) {
+        unpack_block_rows<DT, kGS, kUnpackLut>(wb, r, sb, zb, taddr, lut);
+        return;
     }
     if constexpr (DT == 0) {
         bool exact = true;
@@ -187,14 +202,16 @@ __device__ __forceinline__ void unpack_block(const uint8_t* wb, int r, uint32_t 
             exact = exact && f16_div16_exact(sp, scale_pair_div16(sp));
         }
         if (__all_sync(0xffffffffu, exact)) {
-            unpack_block_rows<DT, kGS, true>(wb, r, sb, zb, taddr);
+            unpack_block_rows<DT, kGS, kUnpackMagicX16>(wb, r, sb, zb, taddr, lut);
             return;
         }
     }
-    unpack_block_rows<DT, kGS, false>(wb, r, sb, zb, taddr);
+    unpack_block_rows<DT, kGS, kUnpackMagic>(wb, r, sb, zb, taddr, lut);
 }
 
-template <int BM, int NWG, int DT>
+// kLut (decode tiles only): unpack through a 16-entry shared table of the values 0..15
+// instead of exponent injection; same results, a measured alternative.
+template <int BM, int NWG, int DT, bool kLut = false>
 __global__ void __launch_bounds__(32 * (1 + TcShape<BM>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     using S = TcShape<BM>;
@@ -203,6 +220,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     constexpr int kNMI = S::kNMI;
     static_assert(S::kACol0 >= kNMI * BM, "accumulators overlap the W staging columns");
     static_assert(kNMI * kTBuf <= 8 && NWG * kTBuf <= 16, "control block barrier slots");
+    static_assert(!kLut || S::kInterleave, "the table unpack exists for decode tiles only");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -220,6 +238,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     // unpacked into TMEM before the previous kernel has finished (programmatic dependent
     // launch); larger tiles track both parts of a stage on full[].
     const uint32_t afull0 = S::kInterleave ? ctrl + 768 : full0;
+    uint16_t* lut = reinterpret_cast<uint16_t*>(ctrl_ptr + 960);  // 16 entries (kLut)
     const uint32_t accum_bar = ctrl + 448;
     const uint32_t recv_bar = ctrl + 456;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl_ptr + 464);
@@ -280,6 +299,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             mbar_init(accum_bar, kNMI);
             mbar_init(recv_bar, 1);
         }
+        if (kLut && lane < 16) lut[lane] = value_bits<DT>(lane);
         fence_mbar_init();
         if (lane == 0) {
             if (args.splits > 1)  // partials of the other ranks for this rank's slice
@@ -525,9 +545,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                                 static_cast<size_t>(b) * bb;
             if constexpr (S::kInterleave) {  // whole block by this warpgroup
                 const uint32_t taddr = tmem + lane_base + S::kACol0 + t * 64;
-                if (gshift == 2) unpack_block<DT, 4>(wb, r, zoff, has_z, taddr);
-                else if (gshift == 1) unpack_block<DT, 2>(wb, r, zoff, has_z, taddr);
-                else unpack_block<DT, 1>(wb, r, zoff, has_z, taddr);
+                if (gshift == 2) unpack_block<DT, 4, kLut>(wb, r, zoff, has_z, taddr, lut);
+                else if (gshift == 1) unpack_block<DT, 2, kLut>(wb, r, zoff, has_z, taddr, lut);
+                else unpack_block<DT, 1, kLut>(wb, r, zoff, has_z, taddr, lut);
             } else {  // this warpgroup's chunks of the block
                 int cur_g = -1;
                 uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
@@ -758,7 +778,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BM, int NWG, int DT>
+template <int BM, int NWG, int DT, bool LUT = false>
 int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                        int K, int group, void* Y, const GemmPlan& plan,
                        const EpilogueArgs& epi, cudaStream_t stream) {
@@ -822,11 +842,11 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
 
     const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;
     if (smem > static_cast<size_t>(ctx.max_smem_optin)) return -2;
-    auto kern = w4a16_tc_kernel<BM, NWG, DT>;
+    auto kern = w4a16_tc_kernel<BM, NWG, DT, LUT>;
     {   // raise the dynamic shared-memory limit once per device (not a stream operation,
         // but kept out of the steady state so that launches can be graph-captured cheaply)
         static std::mutex mu;
-        static size_t configured[64] = {};
+        static size_t configured[64] = {};  // per instantiation (template statics)
         std::lock_guard<std::mutex> lock(mu);
         const int d = ctx.device < 64 ? ctx.device : 63;
         if (configured[d] < smem) {
@@ -916,6 +936,22 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
                                                       plan, epi, stream)                 \
                    : launch_tc_instance<BMV, NWGV, 1>(ctx, A, packed, M, N, K, group, Y, \
                                                       plan, epi, stream);
+    if (plan.lut) {  // the table unpack: decode tiles only
+        switch (plan.tile_m) {
+            case 16:
+                return dtype == 0 ? launch_tc_instance<16, W4A16_SMALL_TILE_WG, 0, true>(
+                                        ctx, A, packed, M, N, K, group, Y, plan, epi, stream)
+                                  : launch_tc_instance<16, W4A16_SMALL_TILE_WG, 1, true>(
+                                        ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
+            case 32:
+                return dtype == 0 ? launch_tc_instance<32, W4A16_SMALL_TILE_WG, 0, true>(
+                                        ctx, A, packed, M, N, K, group, Y, plan, epi, stream)
+                                  : launch_tc_instance<32, W4A16_SMALL_TILE_WG, 1, true>(
+                                        ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
+            default:
+                return -2;
+        }
+    }
     switch (plan.tile_m) {
         W4G_TC_CASE(16, W4A16_SMALL_TILE_WG)
         W4G_TC_CASE(32, W4A16_SMALL_TILE_WG)

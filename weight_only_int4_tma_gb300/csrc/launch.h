@@ -24,6 +24,7 @@ struct GemmPlan {
     int stages;   // shared-memory ring depth
     bool pdl;               // launch with programmatic dependent launch
     bool prefetch_weights;  // read the packed blob before the dependency wait
+    bool lut;               // tensor-core decode tiles: unpack through the 16-entry table
 };
 
 // Launchers return a w4a16_status code.
