@@ -246,7 +246,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     int* info = reinterpret_cast<int*>(ctrl_ptr + 472);  // [0] flags or -1, [1] block bytes
     const float** cs_slot = reinterpret_cast<const float**>(ctrl_ptr + 480);
 
-    const int warp = static_cast<int>(threadIdx.x >> 5);
+    // warp-uniform by construction (broadcast from lane 0), so values derived from it can
+    // live in uniform registers (MMA and TMEM operands)
+    const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
     const int lane = static_cast<int>(threadIdx.x & 31);
     const int split = static_cast<int>(blockIdx.x);
     const int n_tile = static_cast<int>(blockIdx.y);
@@ -338,7 +340,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     if (args.splits > 1) cluster_arrive_release();  // peers may now target our barriers
     if (threadIdx.x == 0) grid_dep_launch();
 
-    const uint32_t tmem = *tmem_slot;
+    const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
 #ifdef W4A16_TRACE
     trace_rec = *reinterpret_cast<const unsigned*>(ctrl_ptr + 488);
     if (threadIdx.x == 0) {
