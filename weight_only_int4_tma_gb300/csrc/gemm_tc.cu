@@ -348,10 +348,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         W4G_TRACE(63, *reinterpret_cast<const unsigned long long*>(ctrl_ptr + 696));
     }
 #endif
-    const int flags = info[0];
+    const int flags = __shfl_sync(0xffffffffu, info[0], 0);
     const bool run = flags >= 0 && nkb > 0;
     const bool has_z = flags >= 0 && (flags & kFlagZeros) != 0;
-    const uint32_t bb = static_cast<uint32_t>(info[1]);
+    const uint32_t bb = static_cast<uint32_t>(__shfl_sync(0xffffffffu, info[1], 0));
     const float* cscale = *cs_slot;
     const uint64_t tlim = args.timeout_ns;
     const int kps = args.kps;
