@@ -361,7 +361,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
 
     if (warp == 0) {
         // ---------------- TMA producer ----------------
-        if (lane == 0 && run) {
+        // The whole warp runs the loop (warp-uniform control and address arithmetic);
+        // lane 0 arms the barriers and issues the copies.
+        if (run) {
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_a = policy_evict_last();
             const uint8_t* src = args.packed + kHeaderBytes +
@@ -369,7 +371,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             const int m0 = m_tile * BM;
             // stage i: blocks [i*kps, i*kps + nblk) as ONE bulk copy + ONE 3-D A box
             const int pre = prefetch_w ? (nst < args.stages ? nst : args.stages) : 0;
-            for (int i = 0; i < pre; ++i) {  // weights do not depend on the previous grid
+            for (int i = 0; i < pre && lane == 0; ++i) {  // weights do not depend on the previous grid
                 const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
                 const int nblk = min(kps, nkb - i * kps);
                 mbar_arrive_expect_tx(full0 + 8 * i, nblk * bb + (S::kInterleave ? 0u : a_bytes));
@@ -386,7 +388,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     tma_tensor_3d_g2s(st, &tmap_a, 0, m0, kchunk, bar, pol_a);
                 }
             };
-            for (int i = 0; i < pre; ++i) {
+            for (int i = 0; i < pre && lane == 0; ++i) {
                 const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
                 if (S::kInterleave) mbar_arrive_expect_tx(afull0 + 8 * i, a_bytes);
                 load_a(st, (kb0 + i * kps) * 2, afull0 + 8 * i);
@@ -401,23 +403,25 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             int left = nkb - pre * kps;          // blocks not yet issued
             for (int i = pre; i < nst; ++i) {
                 if (i >= args.stages &&
-                    !mbar_wait_bounded(empty0 + 8 * s, ph ^ 1u, abort_flag, args.status, tlim))
+                    !mbar_wait_warp(empty0 + 8 * s, ph ^ 1u, abort_flag, args.status, tlim))
                     break;
                 const uint32_t st = base + static_cast<uint32_t>(s) * args.stage_bytes;
                 const uint32_t fb = full0 + 8 * s, ab = afull0 + 8 * s;
                 const int nblk = left < kps ? left : kps;
-                mbar_arrive_expect_tx(fb, nblk * bb + (S::kInterleave ? 0u : a_bytes));
-                tma_bulk_g2s(st + a_bytes, wsrc, nblk * bb, fb, pol_w);
-                if (S::kInterleave) mbar_arrive_expect_tx(ab, a_bytes);
-                load_a(st, kchunk, ab);
-                if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(fb, nblk * bb + (S::kInterleave ? 0u : a_bytes));
+                    tma_bulk_g2s(st + a_bytes, wsrc, nblk * bb, fb, pol_w);
+                    if (S::kInterleave) mbar_arrive_expect_tx(ab, a_bytes);
+                    load_a(st, kchunk, ab);
+                    if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
+                }
                 ++issued;
                 left -= kps;
                 wsrc += static_cast<size_t>(kps) * bb;
                 kchunk += 2 * kps;
                 if (++s == args.stages) { s = 0; ph ^= 1u; }
             }
-            if (issued < nst || *abort_flag) {
+            if (lane == 0 && (issued < nst || *abort_flag)) {
                 // Drain: every issued copy must land before the CTA may exit.
                 const int first = issued > args.stages ? issued - args.stages : 0;
                 for (int i = first; i < issued; ++i) {
