@@ -63,7 +63,7 @@ typedef enum w4a16_dtype {
 
 /* Kernel selection for w4a16_gemm_ex (w4a16_gemm always uses W4A16_KERNEL_AUTO). */
 typedef enum w4a16_kernel {
-    W4A16_KERNEL_AUTO = 0,  /* M == 1, K <= 16384, N/128 <= SMs: SIMT; otherwise TC   */
+    W4A16_KERNEL_AUTO = 0,  /* M == 1, N*K <= 26*2^20, N/128 <= SMs: SIMT; else TC   */
     W4A16_KERNEL_TC = 1,    /* TMA ring -> dequant warps -> tcgen05.mma (swap-AB)      */
     W4A16_KERNEL_SIMT = 2   /* CUDA-core FMA GEMV (cp.async ring), M <= 8              */
 } w4a16_kernel;

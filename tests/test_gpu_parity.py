@@ -197,14 +197,16 @@ def test_gemm_simt_work_split(shape):
 
 
 def test_auto_routes_single_row():
-    """M == 1 goes to the GEMV up to K = 16384 (and one 128-channel tile per SM at most),
-    otherwise to the tensor-core kernel; both routes agree with the oracle."""
+    """M == 1 goes to the GEMV for matrices of up to 26 Mi weights (and one 128-channel
+    tile per SM at most), otherwise to the tensor-core kernel; both routes agree with the
+    oracle."""
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     plan = lambda M, N, K: w4.w4a16_gemm_plan(M, N, K, 128, FP16)["kernel"]
-    assert plan(1, 256, 16384) == w4.W4A16_KERNEL_SIMT
-    assert plan(1, 256, 16512) == w4.W4A16_KERNEL_TC
-    assert plan(1, 128 * sms, 4096) == w4.W4A16_KERNEL_SIMT
-    assert plan(1, 128 * (sms + 1), 4096) == w4.W4A16_KERNEL_TC
+    assert plan(1, 2048, 13312) == w4.W4A16_KERNEL_SIMT   # exactly 26 Mi weights
+    assert plan(1, 2048, 13440) == w4.W4A16_KERNEL_TC
+    assert plan(1, 4096, 4096) == w4.W4A16_KERNEL_SIMT
+    assert plan(1, 11008, 4096) == w4.W4A16_KERNEL_TC
+    assert plan(1, 128 * (sms + 1), 128) == w4.W4A16_KERNEL_TC  # more tiles than SMs
     assert plan(2, 256, 4096) == w4.W4A16_KERNEL_TC
     # between one and two decode tiles per SM: two K slices balance the SMs
     p = w4.w4a16_gemm_plan(8, 128 * (sms + 8), 8192, 128, BF16)

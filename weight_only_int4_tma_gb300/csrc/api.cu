@@ -69,10 +69,11 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
               const w4a16_gemm_config* cfg, GemmPlan* plan) {
     int kernel = cfg ? cfg->kernel : W4A16_KERNEL_AUTO;
-    // Single-row decode with K up to 16384 and at most one 128-channel tile per SM: the
-    // CUDA-core GEMV beats the tensor-core kernel there (the MMA's fixed issue cost and
-    // the TMEM round trip of the unpacked tile dominate at one row, and the GEMV needs no
-    // split-K reduction); longer K or more tiles favour the tensor-core kernel.
+    // Single-row decode of a small matrix (N*K up to 26 Mi weights, at most one 128-channel
+    // tile per SM): the CUDA-core GEMV beats the tensor-core kernel there (no split-K
+    // exchange, a shorter start); larger matrices favour the tensor-core kernel (measured
+    // over N 2048..19200, K 2048..14336: e.g. 5.5 vs 6.0 us at 4096 x 4096, 10.8 vs 9.1 us
+    // at 11008 x 4096).
     int flags = 0;
     if (cfg) {
         for (int i = 0; i < 3; ++i)
@@ -83,7 +84,8 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
         flags = cfg->flags;
     }
     plan->lut = (flags & W4A16_GEMM_DEQUANT_LUT) != 0;
-    if (kernel == W4A16_KERNEL_AUTO && M == 1 && K <= 16384 && tiles_n(N) <= ctx.num_sms &&
+    if (kernel == W4A16_KERNEL_AUTO && M == 1 &&
+        static_cast<long long>(N) * K <= (26LL << 20) && tiles_n(N) <= ctx.num_sms &&
         !plan->lut && !(cfg && (cfg->tile_m || cfg->split_k || cfg->stages)))
         kernel = W4A16_KERNEL_SIMT;
     plan->pdl = (flags & W4A16_GEMM_NO_PDL) == 0;
@@ -132,7 +134,15 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
         // (measured: 37.7 vs 44.2 us at N = 28672, K = 8192; with 32-row tiles the
         // receive area costs a ring stage and the split loses).
         else if (bm == 16 && base > ctx.num_sms) split = 2;
-        else split = slots / base;
+        else {
+            // Clusters are placed whole within a GPC, so not every slot takes a cluster
+            // CTA: above ~6/7 of the slots (260 CTAs on 152 SMs) the launch ran in two
+            // waves (measured, 16-row tiles, K 4096 / 8192: 48 tiles x 6 = 288 CTAs 11.7
+            // us, 48 x 5 = 240 CTAs 7.6 us, 48 x 4 7.3 us).
+            split = slots / base;
+            const int fit = slots * 6 / 7 / base;
+            if (split > 2 && fit < split) split = fit < 2 ? 2 : fit;
+        }
         if (split > 8) split = 8;
         if (split > kblocks) split = kblocks;
         if (split < 1) split = 1;
