@@ -709,17 +709,18 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             named_bar_sync(1, kEpiThreads);
             cluster_wait_acquire();  // every peer has initialised its receive barrier
             const uint32_t rank = cluster_ctarank();
-            if (warp == S::kDq0 && lane == 0) {
-                W4G_TRACE(53, W4G_NOW());
-                const uint32_t recv = base + args.recv_off;
-                for (int p = 0; p < args.splits; ++p) {
-                    if (p == static_cast<int>(rank)) continue;
+            if (warp == S::kDq0) {  // lane p sends the slice of rank p
+                if (lane == 0) W4G_TRACE(53, W4G_NOW());
+                const int p = lane;
+                if (p < args.splits && p != static_cast<int>(rank)) {
                     const uint32_t src = base + static_cast<uint32_t>(p) * slice_bytes;
-                    const uint32_t dst = map_to_rank(recv + rank * slice_bytes, p);
+                    const uint32_t dst =
+                        map_to_rank(base + args.recv_off + rank * slice_bytes, p);
                     bulk_s2cluster(dst, src, slice_bytes, map_to_rank(recv_bar, p));
+                    bulk_commit();
+                    bulk_wait_read_all();
                 }
-                bulk_commit();
-                bulk_wait_read_all();
+                __syncwarp();
             }
             // Sum this rank's slice over all ranks, in rank order, and store it.
             const bool got = mbar_wait_warp(recv_bar, 0, abort_flag, args.status, tlim);
