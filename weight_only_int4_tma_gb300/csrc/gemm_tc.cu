@@ -135,19 +135,19 @@ constexpr int kUnpackMagic = 0;     // exponent injection, pairs (k_2i, k_2i+1) 
 constexpr int kUnpackMagicX16 = 1;  // fp16: odd pairs masked in place (s/16 exact)
 constexpr int kUnpackLut = 2;       // nibble -> value through a 16-entry shared table
 
-// One 128 x 128 block, one weight row r per thread, written as 64 TMEM columns at taddr
-// (four 32-K chunks of 16 columns).  kGS = 32-K chunks per quantisation group (4, 2, 1
-// for groups of 128, 64, 32).  lut: the shared 16-entry table (value bits of q = 0..15)
-// used by kUnpackLut.
-template <int DT, int kGS, int kMode>
+// Chunks kC0, kC0 + kStep, ... (< 4) of one 128 x 128 block, one weight row r per thread;
+// 32-K chunk c lands in TMEM columns taddr + 16 c.  kGS = 32-K chunks per quantisation
+// group (4, 2, 1 for groups of 128, 64, 32).  lut: the shared 16-entry table (value bits
+// of q = 0..15) used by kUnpackLut.
+template <int DT, int kGS, int kMode, int kC0 = 0, int kStep = 1>
 __device__ __forceinline__ void unpack_block_rows(const uint8_t* wb, int r,
                                                   const uint32_t (&sb)[4 / kGS],
                                                   const uint32_t (&zb)[4 / kGS], uint32_t taddr,
                                                   const uint16_t* lut) {
     uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-        if (c % kGS == 0) {  // first chunk of a group: its (group, row) constants
+    for (int c = kC0; c < 4; c += kStep) {
+        if (c == kC0 || c / kGS != (c - kStep) / kGS) {  // a new group: its row constants
             const uint32_t z = (zb[c / kGS] >> ((r & 1) * 4)) & 0xFu;  // 8 when no zeros
             zp = kMode == kUnpackLut ? lut_zero_pair(lut, z) : zero_pair<DT>(z);
             sp = scale_pair(sb[c / kGS]);
@@ -211,6 +211,52 @@ __device__ __forceinline__ void unpack_block(const uint8_t* wb, int r, uint32_t 
 
 // kLut (decode tiles only): unpack through a 16-entry shared table of the values 0..15
 // instead of exponent injection; same results, a measured alternative.
+// Chunks kC0, kC0 + kStep, ... of a block, for tiles whose warpgroups share every block.
+template <int DT, int kGS, int kC0, int kStep>
+__device__ __forceinline__ void unpack_part(const uint8_t* wb, int r, uint32_t zoff,
+                                            bool has_z, uint32_t taddr) {
+    constexpr int kG = 4 / kGS;
+    uint32_t sb[kG], zb[kG];
+#pragma unroll
+    for (int g = 0; g < kG; ++g) {
+        sb[g] = reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[g * kTileN + r];
+        zb[g] = has_z ? wb[zoff + g * (kTileN / 2) + (r >> 1)] : 0x88u;
+    }
+    if constexpr (DT == 0) {
+        bool exact = true;
+#pragma unroll
+        for (int g = 0; g < kG; ++g) {
+            const uint32_t sp = scale_pair(sb[g]);
+            exact = exact && f16_div16_exact(sp, scale_pair_div16(sp));
+        }
+        if (__all_sync(0xffffffffu, exact)) {
+            unpack_block_rows<DT, kGS, kUnpackMagicX16, kC0, kStep>(wb, r, sb, zb, taddr,
+                                                                   nullptr);
+            return;
+        }
+    }
+    unpack_block_rows<DT, kGS, kUnpackMagic, kC0, kStep>(wb, r, sb, zb, taddr, nullptr);
+}
+
+// Warpgroup wg's chunks (wg, wg + NWG, ...) of a block, group layout resolved at compile time.
+template <int DT, int NWG>
+__device__ __forceinline__ void unpack_part_of(int wg, int gshift, const uint8_t* wb, int r,
+                                               uint32_t zoff, bool has_z, uint32_t taddr) {
+#define W4G_PART(C0)                                                                       \
+    if (wg == C0) {                                                                        \
+        if (gshift == 2) unpack_part<DT, 4, C0, NWG>(wb, r, zoff, has_z, taddr);           \
+        else if (gshift == 1) unpack_part<DT, 2, C0, NWG>(wb, r, zoff, has_z, taddr);      \
+        else unpack_part<DT, 1, C0, NWG>(wb, r, zoff, has_z, taddr);                       \
+        return;                                                                            \
+    }
+    static_assert(NWG >= 1 && NWG <= 4, "one to four warpgroups");
+    W4G_PART(0)
+    if constexpr (NWG > 1) { W4G_PART(1) }
+    if constexpr (NWG > 2) { W4G_PART(2) }
+    if constexpr (NWG > 3) { W4G_PART(3) }
+#undef W4G_PART
+}
+
 template <int BM, int NWG, int DT, bool kLut = false>
 __global__ void __launch_bounds__(32 * (1 + TcShape<BM>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
@@ -525,7 +571,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         // every phase of the ring slots it reads (the host keeps the ring depth a
         // multiple of NWG / blocks-per-stage when groups take whole blocks).
         constexpr int kBStep = S::kInterleave ? NWG : 1;         // block stride of a group
-        constexpr int kCpw = S::kInterleave ? 4 : (4 + NWG - 1) / NWG;  // chunks per block
         // Decode tiles hold two blocks per ring stage, so warpgroup wg reads block wg % 2 of
         // stages wg / 2, wg / 2 + NWG / 2, ... (the host keeps the ring depth a multiple
         // of NWG / 2) and uses W buffers wg, wg + NWG, ... mod kTBuf.
@@ -555,44 +600,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 else if (gshift == 1) unpack_block<DT, 2, kLut>(wb, r, zoff, has_z, taddr, lut);
                 else unpack_block<DT, 1, kLut>(wb, r, zoff, has_z, taddr, lut);
             } else {  // this warpgroup's chunks of the block
-                int cur_g = -1;
-                uint32_t zp = 0, sp = 0, zp16 = 0, sp16 = 0;
-                bool x16 = false;
-#pragma unroll
-                for (int j = 0; j < kCpw; ++j) {
-                    const int c = wg + j * NWG;  // 32-K chunk
-                    if (c >= 4) break;
-                    const int gi = c >> gshift;
-                    if (gi != cur_g) {  // per-(group, row) constants
-                        cur_g = gi;
-                        const uint32_t sbits =
-                            reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[gi * kTileN + r];
-                        uint32_t z = 8;
-                        if (has_z)
-                            z = (wb[zoff + gi * (kTileN / 2) + (r >> 1)] >> ((r & 1) * 4)) & 0xFu;
-                        zp = zero_pair<DT>(z);
-                        sp = scale_pair(sbits);
-                        if constexpr (DT == 0) {
-                            zp16 = zero_pair_x16(z);
-                            sp16 = scale_pair_div16(sp);
-                            x16 = __all_sync(0xffffffffu, f16_div16_exact(sp, sp16));
-                        }
-                    }
-                    const uint4 v = *reinterpret_cast<const uint4*>(wb + c * 2048 + r * 16);
-                    uint32_t out[16];
-                    if (DT == 0 && x16) {
-                        dequant_word_f16_x16(v.x, zp, sp, zp16, sp16, out + 0);
-                        dequant_word_f16_x16(v.y, zp, sp, zp16, sp16, out + 4);
-                        dequant_word_f16_x16(v.z, zp, sp, zp16, sp16, out + 8);
-                        dequant_word_f16_x16(v.w, zp, sp, zp16, sp16, out + 12);
-                    } else {
-                        dequant_word<DT>(v.x, zp, sp, out + 0);
-                        dequant_word<DT>(v.y, zp, sp, out + 4);
-                        dequant_word<DT>(v.z, zp, sp, out + 8);
-                        dequant_word<DT>(v.w, zp, sp, out + 12);
-                    }
-                    tmem_st16(tmem + lane_base + S::kACol0 + t * 64 + c * 16, out);
-                }
+                unpack_part_of<DT, NWG>(wg, gshift, wb, r, zoff, has_z,
+                                        tmem + lane_base + S::kACol0 + t * 64);
             }
             tmem_wait_st();
             tc_fence_before();
