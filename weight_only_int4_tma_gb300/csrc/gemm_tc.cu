@@ -17,15 +17,20 @@
 //        factor -> optional + bias, activation, + residual -> round to dtype -> Y
 //        ("量化开销对比" §6.2 "最后：累加器 × s_x → +bias → 写出", §6.6, §6.7 folding)
 //
-// Warp roles: warp 0 = TMA producer; warps 1..NMI = MMA issuers, one thread each (two for
-// decode tiles of <= 32 rows, taking even / odd 128-K blocks into two accumulators;
-// warp 1 also allocates TMEM); then the dequant warps, 4 per warpgroup (warp w may only
-// touch TMEM lanes 32*(w%4)..+31, so each warpgroup covers all 128 lanes), which also run
-// the epilogue.  Decode tiles: warpgroup g unpacks whole blocks g, g + NWG, ...; larger
-// tiles: every warpgroup unpacks its chunks of every block.  Each mbarrier has a single
-// waiting party that passes every one of its phases (tfull per issuer and W buffer,
-// tempty per warpgroup and W buffer), because a parity wait only tells the current phase
-// from the one before it.
+// Warp roles: warp 0 = TMA producer; warps 1..NMI = MMA issuers (two for decode tiles of
+// <= 32 rows, taking even / odd 128-K blocks into two accumulators; warp 1 also allocates
+// TMEM); then the dequant warps, 4 per warpgroup (warp w may only touch TMEM lanes
+// 32*(w%4)..+31, so each warpgroup covers all 128 lanes), which also run the epilogue.
+// The producer and issuer warps run their loops with all 32 lanes and let lane 0 issue,
+// and the warp index and TMEM base are broadcast from lane 0, so that control flow and
+// operand arithmetic are warp-uniform (uniform registers, fewer instructions per block).
+// Decode tiles: warpgroup g unpacks whole blocks g, g + NWG, ...; larger tiles: every
+// warpgroup unpacks its chunks of every block; both through unpack routines templated on
+// the group layout.  Each mbarrier has a single waiting party that passes every one of its
+// phases (tfull per issuer and W buffer, tempty per warpgroup and W buffer), because a
+// parity wait only tells the current phase from the one before it; for decode tiles the
+// A part of a ring stage has its own barrier so that weights can be unpacked before the
+// previous kernel has finished.
 //
 // Programmatic dependent launch: the prologue (barriers, TMEM, descriptor prefetch and,
 // unless disabled, the header check and the first ring stages of packed weights) runs
