@@ -221,6 +221,24 @@ def test_auto_routes_single_row():
     assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
 
 
+def test_heuristic_split_keeps_clusters_in_one_wave():
+    """The split-K heuristic fills the SMs' two slots per SM, but a clustered launch stays
+    within ~6/7 of them (clusters are placed whole within a GPC; above that the launch
+    ran in two waves)."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    slots = 2 * sms
+    for tiles in (16, 24, 32, 40, 48, 56, 64, 86, 112):
+        p = w4.w4a16_gemm_plan(16, 128 * tiles, 4096, 128, FP16)
+        assert p["kernel"] == w4.W4A16_KERNEL_TC and p["tile_m"] == 16
+        ctas = tiles * p["split_k"]
+        assert p["split_k"] <= 8 and ctas <= slots
+        if p["split_k"] > 2:
+            assert ctas <= slots * 6 // 7, (tiles, p["split_k"])
+        # and it is not needlessly small: one more K slice would break the bound
+        if p["split_k"] < 8 and p["split_k"] > 2:
+            assert tiles * (p["split_k"] + 1) > slots * 6 // 7
+
+
 @pytest.mark.parametrize("kernel", [w4.W4A16_KERNEL_TC, w4.W4A16_KERNEL_SIMT])
 def test_channel_scale(kernel):
     c = si.make_case(4, 256, 512, 128, BF16, seed=3, channel_scale=(0.25, 4.0))
