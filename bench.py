@@ -52,9 +52,11 @@ def parse():
                     choices=["none", "bias", "bias_relu", "bias_silu", "bias_residual",
                              "bias_silu_residual"],
                     help="fuse a bias / activation / residual epilogue into every GEMM")
-    ap.add_argument("--dequant", default="magic", choices=["magic", "lut"],
+    ap.add_argument("--dequant", default="magic", choices=["magic", "lut", "int"],
                     help="weight unpack of the tensor-core decode tiles: exponent injection "
-                         "(default) or the 16-entry shared-memory table (same results)")
+                         "(default), the 16-entry shared-memory table (same results), or "
+                         "the integer operand with fp32 group rescale (16-row tiles, "
+                         "groups of 128; unrounded weights)")
     ap.add_argument("--shape", action="append", default=[],
                     help="restrict the workload to this shape tag (repeatable; profiling)")
     return ap.parse_args()
@@ -331,7 +333,8 @@ def run_ours(a):
         bufs.append((c, reps, A, Y))
     torch.cuda.synchronize()
     ex = dict(kernel=a.kernel, split_k=a.split_k, tile_m=a.tile_m, stages=a.stages,
-              flags=w4.W4A16_GEMM_DEQUANT_LUT if a.dequant == "lut" else 0)
+              flags={"magic": 0, "lut": w4.W4A16_GEMM_DEQUANT_LUT,
+                     "int": w4.W4A16_GEMM_DEQUANT_INT}[a.dequant])
     # the plain public call when every launch option is the library's default
     default_launch = not any(ex.values())
     # optional fused epilogue: a seeded bias per shape (resident, like the weights) and a

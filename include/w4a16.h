@@ -87,6 +87,15 @@ typedef enum w4a16_kernel {
  * (the SIMT kernel, tile_m > 32, or M > 32 under the heuristic) returns
  * W4A16_ERR_UNSUPPORTED. */
 #define W4A16_GEMM_DEQUANT_LUT 4
+/* Integer-operand variant: the MMA takes the exact integers (q - z) and each 128-K block's
+ * fp32 partial sum is multiplied by its group scale before it is accumulated ("fine-grained
+ * scaling" per group; the pages' alternative to scaling the weight operand, "量化开销对比"
+ * §6.2 explains why the scale cannot simply move to the end).  The weights are then NOT
+ * rounded to the activation dtype, so the results differ from the default path (they are
+ * the exact product to fp32 accumulation).  Tensor-core kernel with 16-row tiles (M <= 16)
+ * and groups of 128 only; anything else returns W4A16_ERR_UNSUPPORTED.  Exclusive with
+ * W4A16_GEMM_DEQUANT_LUT (both set: W4A16_ERR_INVALID_ARG). */
+#define W4A16_GEMM_DEQUANT_INT 8
 
 typedef struct w4a16_gemm_config {
     int kernel;       /* w4a16_kernel; AUTO picks SIMT only if the three fields below

@@ -80,6 +80,8 @@ def _load():
         lib.w4o_gemm_sampled.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32,
                                          P, P, i64, P, P, P]
         lib.w4o_gemm_sampled.restype = i32
+        lib.w4o_gemm_exact_w.argtypes = [P, P, P, P, P, i32, i32, i32, i32, i32, P, P, P]
+        lib.w4o_gemm_exact_w.restype = i32
         lib.w4o_check.argtypes = [P, P, P, i64, i32, f64, P, P]
         lib.w4o_check.restype = i64
         lib.w4o_epilogue.argtypes = [P, P, P, P, i32, i32, i32, i32, P, P, P]
@@ -186,6 +188,21 @@ def gemm_sampled(A, qweight, scales, qzeros, M: int, N: int, K: int, group: int,
     rc = _load().w4o_gemm_sampled(_ptr(a), _ptr(qw), _ptr(sc), _ptr(qz), _ptr(c), M, N, K,
                                   group, dtype, _ptr(im), _ptr(inn), cnt, _ptr(yd), _ptr(bb),
                                   _ptr(yr))
+    assert rc == 0, rc
+    return yd, bb, yr
+
+
+def gemm_exact_w(A, qweight, scales, qzeros, M: int, N: int, K: int, group: int, dtype: int,
+                 cscale=None):
+    """(Yd, Babs, Yref) [M, N] of the product with unrounded weights (q - z) * s: what the
+    integer-operand variant computes up to fp32 accumulation."""
+    a, qw, sc, qz = _u16(A), _u32(qweight), _u16(scales), _u32(qzeros)
+    c = None if cscale is None else _u16(cscale)
+    yd = np.empty((M, N), dtype=np.float64)
+    bb = np.empty((M, N), dtype=np.float64)
+    yr = np.empty((M, N), dtype=np.uint16)
+    rc = _load().w4o_gemm_exact_w(_ptr(a), _ptr(qw), _ptr(sc), _ptr(qz), _ptr(c), M, N, K,
+                                  group, dtype, _ptr(yd), _ptr(bb), _ptr(yr))
     assert rc == 0, rc
     return yd, bb, yr
 

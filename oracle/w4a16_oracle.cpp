@@ -280,6 +280,51 @@ int w4o_gemm_sampled(const uint16_t* A, const uint32_t* qweight, const uint16_t*
     return 0;
 }
 
+// The product with weights that are NOT rounded to the activation dtype: the integer-
+// operand variant (the MMA takes the exact q - z, the group scale multiplies each group's
+// partial sum: "fine-grained" per-group scaling; [P3] §6.2 explains why the group scale
+// cannot move past the whole k-sum, only past each group's part of it).  Mathematically the k-sum of
+//   A[m,k] * (q[n,k] - z[k/g,n]) * s[k/g,n]
+// with every term exact in fp64 (no encode of the weight):
+//   Yd[m,n] = c[n] * sum_k A[m,k] (q - z) s,   Babs[m,n] = |c[n]| * sum_k |A[m,k] (q - z) s|.
+int w4o_gemm_exact_w(const uint16_t* A, const uint32_t* qweight, const uint16_t* scales,
+                     const uint32_t* qzeros, const uint16_t* cscale, int M, int N, int K,
+                     int group, int dtype, double* Yd, double* Babs, uint16_t* Yref) {
+    if (!shape_ok(N, K, group) || M <= 0) return -1;
+    const Fmt& F = fmt_of(dtype);
+    std::vector<double> Ad(static_cast<size_t>(M) * K);
+    for (size_t i = 0; i < Ad.size(); ++i) Ad[i] = decode(A[i], F);
+#pragma omp parallel
+    {
+        std::vector<double> w(K);
+#pragma omp for schedule(dynamic, 4)
+        for (int n = 0; n < N; ++n) {
+            for (int k = 0; k < K; ++k) {
+                const int gi = k / group;
+                const int q = nibble_q(qweight, K, n, k);
+                const int z = nibble_z(qzeros, N, gi, n);
+                w[k] = static_cast<double>(q - z) * decode(scales[static_cast<size_t>(gi) * N + n], F);
+            }
+            const double c = cscale ? decode(cscale[n], F) : 1.0;
+            for (int m = 0; m < M; ++m) {
+                const double* a = &Ad[static_cast<size_t>(m) * K];
+                double acc = 0.0, mag = 0.0;
+                for (int k = 0; k < K; ++k) {
+                    const double t = a[k] * w[k];
+                    acc += t;
+                    mag += std::fabs(t);
+                }
+                const size_t o = static_cast<size_t>(m) * N + n;
+                const double y = c * acc;
+                if (Yd) Yd[o] = y;
+                if (Babs) Babs[o] = std::fabs(c) * mag;
+                if (Yref) Yref[o] = encode(y, F);
+            }
+        }
+    }
+    return 0;
+}
+
 // Element-wise acceptance test:  |Y - Yd| <= rel_tol * Babs + ulp_dtype(RNE_dtype(Yd)).
 // Returns the number of failing elements; *first_bad receives the first failing index
 // (or -1) and *worst the largest |Y - Yd| / (rel_tol * Babs + ulp) seen.

@@ -141,3 +141,66 @@ def test_transposed_operand_is_caught(orc):
     wrong = (q - z[k_idx // g, n_idx]) * flat[(n_idx * G + k_idx // g) % flat.size]
     assert not np.array_equal(orc.decode(wd, FP16),
                               wrong.astype(np.float16).astype(np.float64))
+
+
+# ---- the product with unrounded weights (integer-operand variant) -------------------
+
+def _nibble(words, idx):
+    """Nibble idx of a flat little-endian array of uint32 words (8 per word)."""
+    return (int(words[idx // 8]) >> (4 * (idx % 8))) & 0xF
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+@pytest.mark.parametrize("asym", [True, False])
+def test_exact_w_tiny_brute_force(orc, dtype, asym):
+    """Plain loops over the canonical inputs (nibbles read here, not through the
+    oracle's unpack), exact rational arithmetic: sum_k A (q - z) s."""
+    M, N, K, g = 2, 8, 64, 32
+    c = si.make_case(M, N, K, g, dtype, seed=5 + dtype, asym=asym, channel_scale=(0.5, 2.0))
+    yd, bb, yr = orc.gemm_exact_w(c.A, c.qweight, c.scales, c.qzeros, M, N, K, g, dtype,
+                                  cscale=c.cscale)
+    A = orc.decode(c.A, dtype)
+    S = orc.decode(c.scales, dtype)
+    C = orc.decode(c.cscale, dtype)
+    qw = c.qweight.ravel()
+    qz = None if c.qzeros is None else c.qzeros.ravel()
+    for m in range(M):
+        for n in range(N):
+            ex, mag = Fraction(0), Fraction(0)
+            for k in range(K):
+                q = _nibble(qw, n * K + k)
+                gi = k // g
+                z = 8 if qz is None else _nibble(qz, gi * N + n)
+                t = Fraction(float(A[m, k])) * (q - z) * Fraction(float(S[gi, n]))
+                ex += t
+                mag += abs(t)
+            ex *= Fraction(float(C[n]))
+            mag *= abs(Fraction(float(C[n])))
+            assert abs(Fraction(yd[m, n]) - ex) <= Fraction(2.0 ** -40) * (mag + 1)
+            assert abs(Fraction(bb[m, n]) - mag) <= Fraction(2.0 ** -40) * (mag + 1)
+            assert yr[m, n] == orc.encode(np.array([float(ex)]), dtype)[0]
+
+
+@pytest.mark.parametrize("dtype", [FP16, BF16])
+def test_exact_w_equals_rounded_for_power_of_two_scales(orc, dtype):
+    """With scales 2^e every (q - z) s is exact in the dtype, so rounding the weight is the
+    identity and both products agree bit for bit."""
+    M, N, K, g = 3, 32, 256, 64
+    c = si.make_case(M, N, K, g, dtype, seed=9)
+    rng = np.random.default_rng(1)
+    e = rng.integers(-8, -2, size=c.scales.shape)
+    c.scales = orc.encode(np.ldexp(1.0, e) * rng.choice([-1.0, 1.0], size=e.shape), dtype)
+    wd = orc.dequant(c.qweight, c.scales, c.qzeros, N, K, g, dtype)
+    y1, b1, r1 = orc.gemm(c.A, wd, M, N, K, dtype)
+    y2, b2, r2 = orc.gemm_exact_w(c.A, c.qweight, c.scales, c.qzeros, M, N, K, g, dtype)
+    assert np.array_equal(y1, y2) and np.array_equal(b1, b2) and np.array_equal(r1, r2)
+
+
+def test_exact_w_is_linear_in_the_scales(orc):
+    """Doubling every scale doubles the exact product (a power-of-two factor is exact)."""
+    M, N, K, g = 2, 16, 128, 32
+    c = si.make_case(M, N, K, g, FP16, seed=4)
+    y1, b1, _ = orc.gemm_exact_w(c.A, c.qweight, c.scales, c.qzeros, M, N, K, g, FP16)
+    s2 = orc.encode(2.0 * orc.decode(c.scales, FP16), FP16)
+    y2, b2, _ = orc.gemm_exact_w(c.A, c.qweight, s2, c.qzeros, M, N, K, g, FP16)
+    assert np.array_equal(2.0 * y1, y2) and np.array_equal(2.0 * b1, b2)

@@ -38,6 +38,7 @@ W4A16_ACT_SILU = 2
 W4A16_GEMM_NO_PDL = 1
 W4A16_GEMM_NO_WEIGHT_PREFETCH = 2
 W4A16_GEMM_DEQUANT_LUT = 4
+W4A16_GEMM_DEQUANT_INT = 8
 
 _lock = threading.Lock()
 _lib = None

@@ -79,18 +79,22 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
         for (int i = 0; i < 3; ++i)
             if (cfg->reserved[i] != 0) return W4A16_ERR_INVALID_ARG;
         if (cfg->flags &
-            ~(W4A16_GEMM_NO_PDL | W4A16_GEMM_NO_WEIGHT_PREFETCH | W4A16_GEMM_DEQUANT_LUT))
+            ~(W4A16_GEMM_NO_PDL | W4A16_GEMM_NO_WEIGHT_PREFETCH | W4A16_GEMM_DEQUANT_LUT |
+              W4A16_GEMM_DEQUANT_INT))
             return W4A16_ERR_INVALID_ARG;
         flags = cfg->flags;
     }
-    plan->lut = (flags & W4A16_GEMM_DEQUANT_LUT) != 0;
+    if ((flags & W4A16_GEMM_DEQUANT_LUT) && (flags & W4A16_GEMM_DEQUANT_INT))
+        return W4A16_ERR_INVALID_ARG;
+    plan->dequant = (flags & W4A16_GEMM_DEQUANT_LUT) ? 1 : (flags & W4A16_GEMM_DEQUANT_INT) ? 2 : 0;
     if (kernel == W4A16_KERNEL_AUTO && M == 1 &&
         static_cast<long long>(N) * K <= (26LL << 20) && tiles_n(N) <= ctx.num_sms &&
-        !plan->lut && !(cfg && (cfg->tile_m || cfg->split_k || cfg->stages)))
+        !plan->dequant && !(cfg && (cfg->tile_m || cfg->split_k || cfg->stages)))
         kernel = W4A16_KERNEL_SIMT;
     plan->pdl = (flags & W4A16_GEMM_NO_PDL) == 0;
     plan->prefetch_weights = plan->pdl && (flags & W4A16_GEMM_NO_WEIGHT_PREFETCH) == 0;
-    if (kernel == W4A16_KERNEL_SIMT && plan->lut) return W4A16_ERR_UNSUPPORTED;
+    if (kernel == W4A16_KERNEL_SIMT && plan->dequant) return W4A16_ERR_UNSUPPORTED;
+    if (plan->dequant == 2 && group != 128) return W4A16_ERR_UNSUPPORTED;
     if (kernel == W4A16_KERNEL_SIMT) {
         if (M > 8) return W4A16_ERR_UNSUPPORTED;
         if (cfg && (cfg->split_k > 1 || cfg->stages != 0)) return W4A16_ERR_UNSUPPORTED;
@@ -117,7 +121,8 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
         else bm = 128;
     }
     if (bm != 16 && bm != 32 && bm != 64 && bm != 128 && bm != 256) return W4A16_ERR_UNSUPPORTED;
-    if (plan->lut && bm > 32) return W4A16_ERR_UNSUPPORTED;  // table unpack: decode tiles
+    if (plan->dequant == 1 && bm > 32) return W4A16_ERR_UNSUPPORTED;  // table: decode tiles
+    if (plan->dequant == 2 && bm != 16) return W4A16_ERR_UNSUPPORTED;  // integer: 16 rows
     const int m_tiles = ceil_div(M, bm);
     if (m_tiles > 65535) return W4A16_ERR_UNSUPPORTED;
     const int base = n_tiles * m_tiles;
@@ -270,7 +275,8 @@ int w4a16_gemm_plan(int M, int N, int K, int group, int dtype, const w4a16_gemm_
     r.stages = plan.stages;
     r.flags = (plan.pdl ? 0 : W4A16_GEMM_NO_PDL) |
               (plan.prefetch_weights ? 0 : W4A16_GEMM_NO_WEIGHT_PREFETCH) |
-              (plan.lut ? W4A16_GEMM_DEQUANT_LUT : 0);
+              (plan.dequant == 1 ? W4A16_GEMM_DEQUANT_LUT : 0) |
+              (plan.dequant == 2 ? W4A16_GEMM_DEQUANT_INT : 0);
     *out = r;
     return W4A16_OK;
 }

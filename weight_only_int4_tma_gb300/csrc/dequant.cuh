@@ -121,6 +121,48 @@ __device__ __forceinline__ bool f16_div16_exact(uint32_t sp, uint32_t sp16) {
     return mul_pair<0>(sp16, 0x4C004C00u) == sp;  // x 16
 }
 
+// ---- integer-operand variant (the MMA takes the exact integers q - z; the group scale
+// multiplies each block's fp32 partial sum afterwards) ---------------------------------
+
+template <int DT>
+__device__ __forceinline__ uint32_t fma_pair(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t d;
+    if constexpr (DT == 0) {
+        asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    } else {
+        asm("fma.rn.bf16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    }
+    return d;
+}
+
+// out[i] = (q_2i - z, q_2i+1 - z), exact small integers in the activation dtype.
+// bf16: the four pairs are shifted down and biased like dequant_word, without the scale.
+// fp16: the pairs at nibble positions (1,5) and (3,7) are masked in place (1024 + 16 q)
+// and fma'd with 1/16 and -(64 + z): (64 + q) - (64 + z), exact inside the fma.
+template <int DT>
+__device__ __forceinline__ void int_word(uint32_t x, uint32_t zp, uint32_t nz64,
+                                         uint32_t* out) {
+    constexpr uint32_t kM = Magic<DT>::kPair;
+    if constexpr (DT == 0) {
+        const uint32_t y = x >> 8;
+        out[0] = sub_pair<0>(lop3_and_or(x, 0x000F000Fu, kM), zp);
+        out[1] = fma_pair<0>(lop3_and_or(x, 0x00F000F0u, kM), 0x2C002C00u, nz64);
+        out[2] = sub_pair<0>(lop3_and_or(y, 0x000F000Fu, kM), zp);
+        out[3] = fma_pair<0>(lop3_and_or(y, 0x00F000F0u, kM), 0x2C002C00u, nz64);
+    } else {
+        out[0] = sub_pair<1>(lop3_and_or(x, 0x000F000Fu, kM), zp);
+        out[1] = sub_pair<1>(lop3_and_or(x >> 4, 0x000F000Fu, kM), zp);
+        out[2] = sub_pair<1>(lop3_and_or(x >> 8, 0x000F000Fu, kM), zp);
+        out[3] = sub_pair<1>(lop3_and_or(x >> 12, 0x000F000Fu, kM), zp);
+    }
+}
+
+// -(64 + z) in both fp16 halves (exact).
+__device__ __forceinline__ uint32_t neg64_pair(uint32_t z) {
+    return static_cast<uint32_t>(__half_as_ushort(__float2half_rn(-(64.0f + static_cast<float>(z))))) *
+           0x00010001u;
+}
+
 // ---- table variant ("量化开销对比" §6.3: nibble -> value through a 16-entry table in
 // shared memory, then the group's zero and scale) ----------------------------------------
 

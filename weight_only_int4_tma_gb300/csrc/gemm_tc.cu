@@ -183,6 +183,33 @@ __device__ __forceinline__ void unpack_block_rows(const uint8_t* wb, int r,
     }
 }
 
+// Integer-operand unpack of one block (groups of 128: one scale and zero per block and
+// row): the exact integers q - z go to TMEM; returns the row's scale, which the caller
+// applies to the block's fp32 partial sum after the MMA.
+template <int DT>
+__device__ __forceinline__ float unpack_block_int(const uint8_t* wb, int r, uint32_t zoff,
+                                                  bool has_z, uint32_t taddr) {
+    const uint32_t z = has_z ? (wb[zoff + (r >> 1)] >> ((r & 1) * 4)) & 0xFu : 8u;
+    const uint32_t zp = zero_pair<DT>(z);
+    const uint32_t nz64 = DT == 0 ? neg64_pair(z) : 0u;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+        const uint4 v = *reinterpret_cast<const uint4*>(wb + c * 2048 + r * 16);
+        uint32_t out[16];
+        int_word<DT>(v.x, zp, nz64, out + 0);
+        int_word<DT>(v.y, zp, nz64, out + 4);
+        int_word<DT>(v.z, zp, nz64, out + 8);
+        int_word<DT>(v.w, zp, nz64, out + 12);
+        tmem_st16(taddr + c * 16, out);
+    }
+    return dtype_to_f32<DT>(reinterpret_cast<const uint16_t*>(wb + kNibbleBytes)[r]);
+}
+
+// Dequant modes of the tensor-core kernel (the alternatives for decode tiles only).
+constexpr int kDqMagic = 0;  // exponent injection, one RNE of (q - z) s per weight
+constexpr int kDqLut = 1;    // the 16-entry table, then the group's zero and scale
+constexpr int kDqInt = 2;    // exact q - z to the MMA, the group scale on the fp32 partial
+
 // Loads the block's group scales and zeros for row r, takes the fp16 x16 decision once for
 // the whole block (warp vote), and unpacks it (kLut: through the shared table instead).
 template <int DT, int kGS, bool kLut>
@@ -214,8 +241,6 @@ __device__ __forceinline__ void unpack_block(const uint8_t* wb, int r, uint32_t 
     unpack_block_rows<DT, kGS, kUnpackMagic>(wb, r, sb, zb, taddr, lut);
 }
 
-// kLut (decode tiles only): unpack through a 16-entry shared table of the values 0..15
-// instead of exponent injection; same results, a measured alternative.
 // Chunks kC0, kC0 + kStep, ... of a block, for tiles whose warpgroups share every block.
 template <int DT, int kGS, int kC0, int kStep>
 __device__ __forceinline__ void unpack_part(const uint8_t* wb, int r, uint32_t zoff,
@@ -262,7 +287,11 @@ __device__ __forceinline__ void unpack_part_of(int wg, int gshift, const uint8_t
 #undef W4G_PART
 }
 
-template <int BM, int NWG, int DT, bool kLut = false>
+// kDq (the alternatives for decode tiles only): kDqLut unpacks through a 16-entry shared
+// table of the values 0..15 instead of exponent injection (same results); kDqInt feeds
+// the MMA the exact integers q - z and scales each block's fp32 partial (16-row tiles,
+// groups of 128; the weights are not rounded to the activation dtype).
+template <int BM, int NWG, int DT, int kDq = kDqMagic>
 __global__ void __launch_bounds__(32 * (1 + TcShape<BM>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     using S = TcShape<BM>;
@@ -271,7 +300,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     constexpr int kNMI = S::kNMI;
     static_assert(S::kACol0 >= kNMI * BM, "accumulators overlap the W staging columns");
     static_assert(kNMI * kTBuf <= 8 && NWG * kTBuf <= 16, "control block barrier slots");
-    static_assert(!kLut || S::kInterleave, "the table unpack exists for decode tiles only");
+    constexpr bool kLut = kDq == kDqLut;
+    constexpr bool kInt = kDq == kDqInt;
+    static_assert(kDq == kDqMagic || S::kInterleave, "the alternatives exist for decode tiles");
+    static_assert(!kInt || (BM == 16 && kNMI == 2 && NWG == 2), "integer operand: 16-row tiles");
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -290,6 +322,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     // launch); larger tiles track both parts of a stage on full[].
     const uint32_t afull0 = S::kInterleave ? ctrl + 768 : full0;
     uint16_t* lut = reinterpret_cast<uint16_t*>(ctrl_ptr + 960);  // 16 entries (kLut)
+    // kInt: dfull[issuer][slot], the block's fp32 partial in D slot (issuer, slot) is done
+    const uint32_t dfull0 = ctrl + 496;
     const uint32_t accum_bar = ctrl + 448;
     const uint32_t recv_bar = ctrl + 456;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl_ptr + 464);
@@ -352,6 +386,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             mbar_init(accum_bar, kNMI);
             mbar_init(recv_bar, 1);
         }
+        if (kInt && lane < 4) mbar_init(dfull0 + 8 * lane, 1);
         if (kLut && lane < 16) lut[lane] = value_bits<DT>(lane);
         fence_mbar_init();
         if (lane == 0) {
@@ -524,16 +559,20 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 const uint32_t te =
                     tempty0 + 8 * ((S::kInterleave ? (i + kTBuf) % NWG : 0) * kTBuf + t);
                 const bool stage_done = kNMI == 2 || b + 1 == kps || i == nkb - 1;
+                // kInt: block i's own fp32 partial, in D slot (k, (i / kNMI) & 1)
+                const uint32_t dslot = (k * 2 + ((i / kNMI) & 1)) * BM;
+                const uint32_t dd = kInt ? tmem + dslot : dacc;
                 if (lane == 0) {
-                    tc_mma_ts(dacc, a0, d0, idesc, i >= kNMI ? 1u : 0u);
-                    tc_mma_ts(dacc, a0 + 8, d0 + 2, idesc, 1u);
-                    tc_mma_ts(dacc, a0 + 16, d0 + 4, idesc, 1u);
-                    tc_mma_ts(dacc, a0 + 24, d0 + 6, idesc, 1u);
-                    tc_mma_ts(dacc, a0 + 32, d1, idesc, 1u);
-                    tc_mma_ts(dacc, a0 + 40, d1 + 2, idesc, 1u);
-                    tc_mma_ts(dacc, a0 + 48, d1 + 4, idesc, 1u);
-                    tc_mma_ts(dacc, a0 + 56, d1 + 6, idesc, 1u);
+                    tc_mma_ts(dd, a0, d0, idesc, (!kInt && i >= kNMI) ? 1u : 0u);
+                    tc_mma_ts(dd, a0 + 8, d0 + 2, idesc, 1u);
+                    tc_mma_ts(dd, a0 + 16, d0 + 4, idesc, 1u);
+                    tc_mma_ts(dd, a0 + 24, d0 + 6, idesc, 1u);
+                    tc_mma_ts(dd, a0 + 32, d1, idesc, 1u);
+                    tc_mma_ts(dd, a0 + 40, d1 + 2, idesc, 1u);
+                    tc_mma_ts(dd, a0 + 48, d1 + 4, idesc, 1u);
+                    tc_mma_ts(dd, a0 + 56, d1 + 6, idesc, 1u);
                     tc_commit(te);
+                    if (kInt) tc_commit(dfull0 + dslot / 2);  // 8 bytes per (k, slot)
                     if (stage_done) tc_commit(empty0 + 8 * s);
                     if (i < 8) W4G_TRACE(42 + i, W4G_NOW());
                 }
@@ -586,6 +625,28 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         int b = S::kInterleave ? wg % 2 : 0;  // block i's place in its stage
         int t = S::kInterleave ? wg % kTBuf : 0;  // its W buffer
         uint32_t epar = 0;      // bit t: parity of this warp's next wait on tempty[tw][t]
+        // kInt: this thread's running sum over its group's blocks (row r, BM columns), the
+        // scale of the block unpacked last, and that block's place in the group's order
+        float iacc[kInt ? BM : 1];
+#pragma unroll
+        for (int m = 0; m < (kInt ? BM : 1); ++m) iacc[m] = 0.0f;
+        float s_last = 0.0f;
+        int jn = 0;             // blocks this group has unpacked
+        // adds block j's partial (D slot (wg, j & 1), ready when dfull's phase j / 2 is)
+        auto rescale = [&](int j, float sc) {
+            if constexpr (kInt) {
+                const uint32_t sl = static_cast<uint32_t>(j & 1);
+                ok = ok && mbar_wait_warp(dfull0 + 8 * (wg * 2 + sl), (j >> 1) & 1, abort_flag,
+                                          args.status, tlim);
+                if (!ok) return;
+                tc_fence_after();
+                uint32_t v[16];
+                tmem_ld16(tmem + lane_base + (wg * 2 + sl) * BM, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int m = 0; m < BM; ++m) iacc[m] = fmaf(__uint_as_float(v[m]), sc, iacc[m]);
+            }
+        };
         for (int i = S::kInterleave ? wg : 0; i < nkb && ok; i += kBStep) {   // 128-K block
             if (S::kInterleave || b == 0)  // (s, b, t) advance at the loop end
                 ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
@@ -599,9 +660,11 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(18 + i, W4G_NOW());
             const uint8_t* wb = base_ptr + a_bytes + static_cast<size_t>(s) * args.stage_bytes +
                                 static_cast<size_t>(b) * bb;
+            float s_cur = 0.0f;  // kInt: the block's scale for row r
             if constexpr (S::kInterleave) {  // whole block by this warpgroup
                 const uint32_t taddr = tmem + lane_base + S::kACol0 + t * 64;
-                if (gshift == 2) unpack_block<DT, 4, kLut>(wb, r, zoff, has_z, taddr, lut);
+                if constexpr (kInt) s_cur = unpack_block_int<DT>(wb, r, zoff, has_z, taddr);
+                else if (gshift == 2) unpack_block<DT, 4, kLut>(wb, r, zoff, has_z, taddr, lut);
                 else if (gshift == 1) unpack_block<DT, 2, kLut>(wb, r, zoff, has_z, taddr, lut);
                 else unpack_block<DT, 1, kLut>(wb, r, zoff, has_z, taddr, lut);
             } else {  // this warpgroup's chunks of the block
@@ -613,6 +676,11 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             __syncwarp();
             if (lane == 0) mbar_arrive(tfull0 + 8 * ((i % kNMI) * kTBuf + t));
             if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(26 + i, W4G_NOW());
+            if constexpr (kInt) {  // the previous block's partial, while this one is in the MMA
+                if (jn > 0) rescale(jn - 1, s_last);
+                s_last = s_cur;
+                ++jn;
+            }
             if constexpr (S::kInterleave) {
                 s += NWG / 2;
                 if (s >= args.stages) { s -= args.stages; ph ^= 1u; }
@@ -627,10 +695,28 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             }
         }
 
+        if (kInt && ok && jn > 0) rescale(jn - 1, s_last);
+
         // ---------------- epilogue ----------------
         const int R = args.slice_rows;
         float* part = reinterpret_cast<float*>(base_ptr);  // [slice][BM][R] when split
         ok = ok && mbar_wait_warp(accum_bar, 0, abort_flag, args.status, tlim);
+        // kInt: each group's sum goes to TMEM where the epilogue expects the two issuers'
+        // accumulators (columns d_base and d_base + BM, in the now idle W buffer area)
+        uint32_t d_base = 0;
+        if constexpr (kInt) {
+            d_base = S::kACol0;
+            if (ok) {
+                tc_fence_after();
+                uint32_t v[16];
+#pragma unroll
+                for (int m = 0; m < 16; ++m) v[m] = __float_as_uint(iacc[m]);
+                tmem_st16(tmem + lane_base + d_base + wg * BM, v);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            named_bar_sync(2, kEpiThreads);  // both groups' sums are in place
+        }
         if (ok) {
             if (warp == S::kDq0 && lane == 0) W4G_TRACE(51, W4G_NOW());
             tc_fence_after();
@@ -644,10 +730,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             const int pslice = r / R, prow = r - pslice * R;
             // D columns e*16 .. e*16+15 of this thread's channel (both accumulators added)
             auto load_d = [&](int e, uint32_t (&v)[16]) {
-                tmem_ld16(tmem + lane_base + e * 16, v);
+                tmem_ld16(tmem + lane_base + d_base + e * 16, v);
                 if (kNMI == 2 && nkb > 1) {  // add the odd-block accumulator
                     uint32_t v1[16];
-                    tmem_ld16(tmem + lane_base + BM + e * 16, v1);
+                    tmem_ld16(tmem + lane_base + d_base + BM + e * 16, v1);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 16; ++j)
@@ -799,7 +885,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BM, int NWG, int DT, bool LUT = false>
+template <int BM, int NWG, int DT, int DQ = kDqMagic>
 int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                        int K, int group, void* Y, const GemmPlan& plan,
                        const EpilogueArgs& epi, cudaStream_t stream) {
@@ -863,7 +949,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
 
     const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;
     if (smem > static_cast<size_t>(ctx.max_smem_optin)) return -2;
-    auto kern = w4a16_tc_kernel<BM, NWG, DT, LUT>;
+    auto kern = w4a16_tc_kernel<BM, NWG, DT, DQ>;
     {   // raise the dynamic shared-memory limit once per device (not a stream operation,
         // but kept out of the steady state so that launches can be graph-captured cheaply)
         static std::mutex mu;
@@ -957,21 +1043,28 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
                                                       plan, epi, stream)                 \
                    : launch_tc_instance<BMV, NWGV, 1>(ctx, A, packed, M, N, K, group, Y, \
                                                       plan, epi, stream);
-    if (plan.lut) {  // the table unpack: decode tiles only
+    if (plan.dequant == 1) {  // the table unpack: decode tiles only
         switch (plan.tile_m) {
             case 16:
-                return dtype == 0 ? launch_tc_instance<16, W4A16_SMALL_TILE_WG, 0, true>(
+                return dtype == 0 ? launch_tc_instance<16, W4A16_SMALL_TILE_WG, 0, kDqLut>(
                                         ctx, A, packed, M, N, K, group, Y, plan, epi, stream)
-                                  : launch_tc_instance<16, W4A16_SMALL_TILE_WG, 1, true>(
+                                  : launch_tc_instance<16, W4A16_SMALL_TILE_WG, 1, kDqLut>(
                                         ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
             case 32:
-                return dtype == 0 ? launch_tc_instance<32, W4A16_SMALL_TILE_WG, 0, true>(
+                return dtype == 0 ? launch_tc_instance<32, W4A16_SMALL_TILE_WG, 0, kDqLut>(
                                         ctx, A, packed, M, N, K, group, Y, plan, epi, stream)
-                                  : launch_tc_instance<32, W4A16_SMALL_TILE_WG, 1, true>(
+                                  : launch_tc_instance<32, W4A16_SMALL_TILE_WG, 1, kDqLut>(
                                         ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
             default:
                 return -2;
         }
+    }
+    if (plan.dequant == 2) {  // integer operand: 16-row tiles, groups of 128
+        if (plan.tile_m != 16 || group != 128) return -2;
+        return dtype == 0 ? launch_tc_instance<16, 2, 0, kDqInt>(ctx, A, packed, M, N, K, group,
+                                                                Y, plan, epi, stream)
+                          : launch_tc_instance<16, 2, 1, kDqInt>(ctx, A, packed, M, N, K, group,
+                                                                Y, plan, epi, stream);
     }
     switch (plan.tile_m) {
         W4G_TC_CASE(16, W4A16_SMALL_TILE_WG)

@@ -24,7 +24,8 @@ struct GemmPlan {
     int stages;   // shared-memory ring depth
     bool pdl;               // launch with programmatic dependent launch
     bool prefetch_weights;  // read the packed blob before the dependency wait
-    bool lut;               // tensor-core decode tiles: unpack through the 16-entry table
+    int dequant;            // tensor-core decode tiles: 0 exponent injection, 1 the
+                            // 16-entry table, 2 integer operand + fp32 group rescale
 };
 
 // Launchers return a w4a16_status code.
