@@ -67,6 +67,9 @@ KERNELS = {
     "tc_split1": dict(kernel=w4.W4A16_KERNEL_TC, tile_m=16, split_k=1),
     "tc_split4": dict(kernel=w4.W4A16_KERNEL_TC, tile_m=16, split_k=4),
     "tc_tile128": dict(kernel=w4.W4A16_KERNEL_TC, tile_m=128),
+    # one K slice: the larger tiles' staged, vectorised store path
+    "tc_tile128_s1": dict(kernel=w4.W4A16_KERNEL_TC, tile_m=128, split_k=1),
+    "tc_tile64_s1": dict(kernel=w4.W4A16_KERNEL_TC, tile_m=64, split_k=1),
     "gemv": dict(kernel=w4.W4A16_KERNEL_SIMT),
 }
 
@@ -75,7 +78,7 @@ KERNELS = {
 @pytest.mark.parametrize("act", [NONE, RELU, SILU])
 @pytest.mark.parametrize("dtype", [FP16, BF16])
 def test_bias_act_residual(kname, act, dtype):
-    M = 130 if kname == "tc_tile128" else (3 if kname == "gemv" else 11)
+    M = {"tc_tile128": 130, "tc_tile128_s1": 130, "tc_tile64_s1": 70, "gemv": 3}.get(kname, 11)
     c = si.make_case(M, 384, 1024, 64, dtype, seed=7 + act, channel_scale=(0.5, 2.0))
     packed = repack_case(c)
     bias, res = epilogue_inputs(c, seed=act, with_bias=True, with_res=True)
@@ -93,7 +96,7 @@ def test_optional_parts(kname, with_bias, with_res):
     assert_epilogue_parity(c, Y, bias, res, SILU)
 
 
-@pytest.mark.parametrize("kname", ["tc_split1", "tc_split4", "gemv"])
+@pytest.mark.parametrize("kname", ["tc_split1", "tc_split4", "tc_tile128_s1", "gemv"])
 def test_in_place_residual(kname):
     c = si.make_case(4, 256, 768, 128, BF16, seed=11)
     packed = repack_case(c)
@@ -131,3 +134,23 @@ def test_bad_activation_rejected():
     with pytest.raises(w4.W4A16Error) as e:
         run_epilogue(c, packed, None, None, 7)
     assert e.value.status == w4.W4A16_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("offset", [0, 1])
+def test_staged_store_ragged_and_unaligned(offset):
+    """Larger tiles with one K slice store through shared memory, 8 channels per 16-byte
+    access; a ragged N and M, and a residual that is only 2-byte aligned (the scalar path
+    then; Y itself must be 16-byte aligned), give the same results."""
+    c = si.make_case(70, 520, 512, 128, FP16, seed=21 + offset)
+    packed = repack_case(c)
+    bias, res = epilogue_inputs(c, seed=4, with_bias=True, with_res=True)
+    n = c.M * c.N
+    rbuf = torch.zeros(n + 8, dtype=torch.int16, device="cuda")
+    rbuf[offset:offset + n] = torch.from_numpy(res.view(np.int16).ravel()).cuda()
+    Y = torch.empty((c.M, c.N), dtype=torch.int16, device="cuda")
+    R = rbuf[offset:offset + n].view(c.M, c.N)
+    w4.w4a16_gemm_epilogue(to_dev(c.A), packed, c.M, c.N, c.K, c.group, c.dtype,
+                           to_dev(bias), R, SILU, Y, kernel=w4.W4A16_KERNEL_TC, tile_m=64,
+                           split_k=1)
+    assert w4.w4a16_get_device_status() == 0
+    assert_epilogue_parity(c, Y.cpu().numpy().view(np.uint16), bias, res, SILU)

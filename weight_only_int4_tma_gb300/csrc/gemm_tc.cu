@@ -751,6 +751,57 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     for (int j = 0; j < 16; ++j)
                         part[(pslice * BM + e * 16 + j) * R + prow] = __uint_as_float(v[j]);
                 }
+            } else if (BM >= 64 &&
+                       ((reinterpret_cast<uintptr_t>(args.Y) |
+                         reinterpret_cast<uintptr_t>(args.epi.residual)) & 15u) == 0) {
+                // Larger tiles: each warp stages its 32 channels x 16 rows of A through
+                // shared memory (the idle ring) and stores 8 channels per 16-byte access,
+                // reading the residual the same way; the fp32 operations and their order
+                // are those of the paths below, so the results are the same bits.
+                const int act = args.epi.act;
+                const uint16_t* rp = args.epi.residual;
+                float* T = reinterpret_cast<float*>(base_ptr) + (warp - S::kDq0) * 512;  // [16][32]
+                const int n0w = n_tile * kTileN + q * 32;  // first channel of this warp
+#pragma unroll 1
+                for (int e = wg; e < BM / 16; e += NWG) {
+                    uint32_t v[16];
+                    load_d(e, v);  // warp-collective: every lane, padded rows included
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float y = __uint_as_float(v[j]) * cs + bias_n;
+                        T[j * 32 + lane] = act == kActNone ? y : apply_activation(y, act);
+                    }
+                    __syncwarp();
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const int jm = p * 8 + (lane >> 2);  // row of A within the group
+                        const int nb = (lane & 3) * 8;       // first of 8 channels
+                        const int m = m_tile * BM + e * 16 + jm;
+                        const int nn = n0w + nb;             // N % 8 == 0: 8 valid or none
+                        if (m < args.M && nn < args.N) {
+                            const float4 lo = *reinterpret_cast<const float4*>(T + jm * 32 + nb);
+                            const float4 hi =
+                                *reinterpret_cast<const float4*>(T + jm * 32 + nb + 4);
+                            float f[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+                            const size_t o = static_cast<size_t>(m) * args.N + nn;
+                            if (rp) {
+                                const uint4 rv = *reinterpret_cast<const uint4*>(rp + o);
+                                const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+                                for (int h = 0; h < 8; ++h)
+                                    f[h] += dtype_to_f32<DT>(
+                                        static_cast<uint16_t>(rw[h >> 1] >> ((h & 1) * 16)));
+                            }
+                            uint32_t ow[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h)
+                                ow[h] = static_cast<uint32_t>(f32_to_dtype<DT>(f[2 * h])) |
+                                        (static_cast<uint32_t>(f32_to_dtype<DT>(f[2 * h + 1])) << 16);
+                            *reinterpret_cast<uint4*>(Y + o) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+                        }
+                    }
+                    __syncwarp();  // the tile is read before the next group overwrites it
+                }
             } else if (!args.epi.residual) {
                 const int act = args.epi.act;
 #pragma unroll 1
