@@ -3,11 +3,15 @@
 One step = one pass of the decode sweep: the fused GEMM for M in {1,2,4,8,16},
 K = 4096, N in {4096, 11008}, group 128, fp16 activations, asymmetric int4 weights
 (10 launches).  The repack is offline and not timed.  The headline metric is achieved
-HBM TB/s over algorithmic bytes (packed weights + scales + zeros + A + Y).
+HBM TB/s over algorithmic bytes (packed weights + scales + zeros + A + Y).  A default run
+also times, with the same step count, the 70B-shaped decode FFN (HBM TB/s), the batch
+transition sweep and the prefill GEMM (tensor TFLOP/s), each with its own roofline, under
+the line's "per_workload" key.
 
-Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead.
+Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead, with the
+same metric string, unit and workload.
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload NAME]
+                       [--workload NAME] [--no-extra-workloads]
 """
 from __future__ import annotations
 
@@ -59,6 +63,9 @@ def parse():
                          "groups of 128; unrounded weights)")
     ap.add_argument("--shape", action="append", default=[],
                     help="restrict the workload to this shape tag (repeatable; profiling)")
+    ap.add_argument("--no-extra-workloads", dest="extra_workloads", action="store_false",
+                    help="time only --workload (by default the 70B-shaped decode, the batch "
+                         "transition and the prefill workloads are timed beside it)")
     return ap.parse_args()
 
 
@@ -197,17 +204,34 @@ def profiled_traffic(workload, kernel):
     return d.get("dram_bytes_per_launch")
 
 
+# ---- what a workload is measured in (shared by both arms) ----------------------------
+
+def compute_bound(shapes) -> bool:
+    """Prefill and batch-transition workloads (M >= 64 everywhere) are bound by the tensor
+    pipe and measured in TFLOP/s; decode-sized ones by HBM, in TB/s."""
+    return min(p["M"] for p in shapes) >= 64
+
+
+def metric_name(workload: str, shapes) -> str:
+    """The line's metric string: identical for the GPU arm and the reference arm of one
+    workload, so that their values divide."""
+    kind = "tensor TFLOP/s" if compute_bound(shapes) else "HBM TB/s"
+    return f"W4A16 GEMM achieved {kind} ({workload})"
+
+
+def metric_unit(shapes) -> str:
+    return "TFLOP/s" if compute_bound(shapes) else "TB/s"
+
+
 # ---- the reference arm: the CPU oracle ----------------------------------------------
 
 def oracle_slice(orc, c, n0, nc):
     """Oracle dequant + GEMM for output channels [n0, n0 + nc) of a case."""
-    G = c.K // c.group
     qw = c.qweight[n0:n0 + nc]
     sc = np.ascontiguousarray(c.scales[:, n0:n0 + nc])
     qz = None if c.qzeros is None else np.ascontiguousarray(c.qzeros[:, n0 // 8:(n0 + nc) // 8])
     wd = orc.dequant(qw, sc, qz, nc, c.K, c.group, c.dtype)
     orc.gemm(c.A, wd, c.M, nc, c.K, c.dtype)
-    _ = G
 
 
 def shape_bytes(p, epilogue="none"):
@@ -219,12 +243,18 @@ def shape_bytes(p, epilogue="none"):
     return b
 
 
+def shape_work(p, tflops: bool, epilogue="none"):
+    """Work of one GEMM in the workload's unit: flops, or algorithmic bytes."""
+    return si.flops(p["M"], p["N"], p["K"]) if tflops else shape_bytes(p, epilogue)
+
+
 def cpu_oracle_rate(cases, shapes, budget_s):
     """Times the oracle over slices of the workload's shapes for about budget_s seconds.
-    Returns (bytes/s, sample description, threads)."""
+    Returns (work units/s in the workload's unit, sample description, threads, seconds)."""
     import oracle as orc
     orc.build()
-    total_bytes = 0.0
+    tfl = compute_bound(shapes)
+    total = 0.0
     t_used = 0.0
     done = []
     nc = 256
@@ -232,16 +262,17 @@ def cpu_oracle_rate(cases, shapes, budget_s):
     while t_used < budget_s and i < 100000:
         c, p = cases[i % len(cases)], shapes[i % len(cases)]
         n0 = (i // len(cases)) * nc % c.N
+        n = min(nc, c.N - n0)
         t0 = time.perf_counter()
-        oracle_slice(orc, c, n0, nc)
+        oracle_slice(orc, c, n0, n)
         dt = time.perf_counter() - t0
         t_used += dt
-        total_bytes += shape_bytes(p) * nc / c.N
-        done.append(f"{si.shape_tag(p)}[n {n0}:{n0 + nc}]")
+        total += shape_work(p, tfl) * n / c.N
+        done.append(f"{si.shape_tag(p)}[n {n0}:{n0 + n}]")
         i += 1
-    desc = (f"{len(done)} slices of {nc} output channels (dequant + fp64 GEMM), e.g. "
+    desc = (f"{len(done)} slices of up to {nc} output channels (dequant + fp64 GEMM), e.g. "
             + ", ".join(done[:3]))
-    return total_bytes / t_used, desc, orc.num_threads(), t_used
+    return total / t_used, desc, orc.num_threads(), t_used
 
 
 def run_reference(a):
@@ -252,21 +283,21 @@ def run_reference(a):
             return
     shapes = workload_shapes(a)
     cases = [si.make_case(**p) for p in shapes]
-    step_bytes = sum(shape_bytes(p) for p in shapes)
+    tfl = compute_bound(shapes)
     import oracle as orc
     orc.build()
-    # Each step: one slice of output channels of one shape, sized so that the whole run
-    # stays within about two minutes.
+    # Each step: one slice of output channels of one shape (the shapes in turn), sized so
+    # that the whole run stays within about two minutes.
     budget = 120.0 / max(1, a.steps + a.warmup)
-    probe_c, probe_p = cases[0], shapes[0]
+    probe_c = max(cases, key=lambda c: c.M * c.K)
     t0 = time.perf_counter()
     oracle_slice(orc, probe_c, 0, 8)
     per_ch = (time.perf_counter() - t0) / 8
-    nc = int(max(8, min(probe_c.N, (budget / max(per_ch, 1e-9)) // 8 * 8)))
+    nc = int(max(8, min(max(c.N for c in cases), (budget / max(per_ch, 1e-9)) // 8 * 8)))
     for i in range(a.warmup):
         c = cases[i % len(cases)]
         oracle_slice(orc, c, 0, min(nc, c.N))
-    tot_b = 0.0
+    tot = 0.0
     t0 = time.perf_counter()
     for i in range(a.steps):
         c, p = cases[i % len(cases)], shapes[i % len(cases)]
@@ -274,44 +305,51 @@ def run_reference(a):
         n0 = (i * n) % c.N
         n = min(n, c.N - n0)
         oracle_slice(orc, c, n0, n)
-        tot_b += shape_bytes(p) * n / c.N
+        tot += shape_work(p, tfl) * n / c.N
     el = time.perf_counter() - t0
-    v = tot_b / el / 1e12
-    sample = f"per step: {nc} output channels of one decode shape (dequant + fp64 GEMM)"
+    v = tot / el / 1e12
+    unit = metric_unit(shapes)
+    sample = (f"per step: up to {nc} output channels of one shape of the workload, the shapes "
+              f"in turn (dequant + fp64 GEMM)")
     line = {
-        "impl": "reference", "metric": "W4A16 GEMM achieved HBM TB/s (decode sweep)",
-        "value": v, "unit": "TB/s", "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
+        "impl": "reference", "metric": metric_name(a.workload, shapes),
+        "value": v, "unit": unit, "n_gpus": a.gpus, "steps": a.steps, "warmup": a.warmup,
         "ms_per_step": el / max(1, a.steps) * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": a.workload, "step_bytes_full": step_bytes},
-        "cpu_baseline": {"value": v, "unit": "TB/s", "cores": orc.num_threads(),
+        "config": {"workload": a.workload, "shapes": len(shapes),
+                   "step_bytes": sum(shape_bytes(p) for p in shapes),
+                   "step_flops": sum(si.flops(p["M"], p["N"], p["K"]) for p in shapes)},
+        "cpu_baseline": {"value": v, "unit": unit, "cores": orc.num_threads(),
                          "kind": "oracle", "sample": sample},
-        "e2e": {"value": v, "unit": "TB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "e2e": {"value": v, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
 # ---- our arm ------------------------------------------------------------------------
 
-def run_ours(a):
+def tensor_peak(peaks, region_s: float):
+    """The dense bf16 (= fp16) tensor peak that matches a timed region: the burst figure
+    for a region under a second, the sustained (power-capped) one for longer regions."""
+    burst = float(peaks.get("bf16_tflops", 1900.0))
+    sustained = float(peaks.get("bf16_tflops_sustained", burst))
+    return (burst, "burst") if region_s < 1.0 else (sustained, "sustained")
+
+
+class Measured:
+    """Everything one workload's measurement produces (the JSON line's parts)."""
+
+
+def measure_workload(a, w4, device, stream, sampler, workload, shapes, ex, steps,
+                     warmup, epilogue="none"):
     import torch
 
-    ws, rank, local = dist_info()
-    if not torch.cuda.is_available():
-        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    if ws > 1:
-        dist_init("nccl")
-
-    from weight_only_int4_tma_gb300 import build as w4build
-    w4build.build()
-    import weight_only_int4_tma_gb300 as w4
-
-    shapes = workload_shapes(a)
+    ws, rank, _ = dist_info()
     cases = [si.make_case(**p) for p in shapes]
-    step_bytes = sum(shape_bytes(p, a.epilogue) for p in shapes)
+    tfl = compute_bound(shapes)
+    step_bytes = sum(shape_bytes(p, epilogue) for p in shapes)
     step_flops = sum(si.flops(p["M"], p["N"], p["K"]) for p in shapes)
+    step_work = step_flops if tfl else step_bytes
 
     def dev(x):
         if x is None:
@@ -320,8 +358,9 @@ def run_ours(a):
         return torch.from_numpy(np.ascontiguousarray(v)).to(device)
 
     # Weights rotate over enough copies that each launch reads them from HBM, not L2.
-    packed_per_step = sum(w4.w4a16_packed_bytes(c.N, c.K, c.group, c.qzeros is not None)
-                          for c in cases)
+    shape_packed = [w4.w4a16_packed_bytes(c.N, c.K, c.group, c.qzeros is not None)
+                    for c in cases]
+    packed_per_step = sum(shape_packed)
     copies = max(2, -(-3 * L2_BYTES // max(1, packed_per_step)))
     bufs = []
     for c in cases:
@@ -332,28 +371,25 @@ def run_ours(a):
         Y = torch.empty((c.M, c.N), dtype=torch.int16, device=device)
         bufs.append((c, reps, A, Y))
     torch.cuda.synchronize()
-    ex = dict(kernel=a.kernel, split_k=a.split_k, tile_m=a.tile_m, stages=a.stages,
-              flags={"magic": 0, "lut": w4.W4A16_GEMM_DEQUANT_LUT,
-                     "int": w4.W4A16_GEMM_DEQUANT_INT}[a.dequant])
     # the plain public call when every launch option is the library's default
     default_launch = not any(ex.values())
+    act = {"relu": w4.W4A16_ACT_RELU, "silu": w4.W4A16_ACT_SILU}
+    epi_act = next((v for k, v in act.items() if k in epilogue), w4.W4A16_ACT_NONE)
     # optional fused epilogue: a seeded bias per shape (resident, like the weights) and a
     # device-resident residual (the previous layer's output in a real forward pass)
-    act = {"relu": w4.W4A16_ACT_RELU, "silu": w4.W4A16_ACT_SILU}
-    epi_act = next((v for k, v in act.items() if k in a.epilogue), w4.W4A16_ACT_NONE)
     epi = []
     for c, _, _, _ in bufs:
         tdt = torch.float16 if c.dtype == 0 else torch.bfloat16
         g = torch.Generator().manual_seed(c.M * 100003 + c.N)
         bias = (torch.randn(c.N, generator=g).to(tdt).view(torch.int16).to(device)
-                if a.epilogue != "none" else None)
+                if epilogue != "none" else None)
         res = (torch.randn((c.M, c.N), generator=g).to(tdt).view(torch.int16).to(device)
-               if a.epilogue.endswith("residual") else None)
+               if epilogue.endswith("residual") else None)
         epi.append((bias, res))
 
     def gemm_call(j, A, packed, Y, stream_, public=False):
         c = bufs[j][0]
-        if a.epilogue == "none":
+        if epilogue == "none":
             if public and default_launch:
                 w4.w4a16_gemm(A, packed, c.M, c.N, c.K, c.group, c.dtype, Y, stream_)
             else:
@@ -370,40 +406,34 @@ def run_ours(a):
     shape_kernel = [kname[w4.w4a16_gemm_plan(c.M, c.N, c.K, c.group, c.dtype, **ex)["kernel"]]
                     for c in cases]
 
-    stream = torch.cuda.Stream(device=device)
-
     def launch_step(step_idx):
         for j, (c, reps, A, Y) in enumerate(bufs):
             gemm_call(j, A, reps[step_idx % copies], Y, stream)
 
     with torch.cuda.stream(stream):
-        for i in range(max(3, a.warmup)):
+        for i in range(max(3, warmup)):
             launch_step(i)
     stream.synchronize()
     st = w4.w4a16_get_device_status(stream)
     if st != 0:
-        raise SystemExit(f"device status after warm-up: {w4.status_string(st)}")
+        raise SystemExit(f"{workload}: device status after warm-up: {w4.status_string(st)}")
 
     # Capture G steps into one CUDA graph (no events inside: consecutive GEMMs overlap
     # their prologues through programmatic dependent launch).
-    G = max(1, min(a.graph_steps, a.steps))
+    G = max(1, min(a.graph_steps, steps))
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):
         with torch.cuda.graph(graph, stream=stream):
             for g in range(G):
                 launch_step(g)
     stream.synchronize()
-    full_replays = a.steps // G
-    eager_tail = a.steps - full_replays * G
-
+    full_replays = steps // G
+    eager_tail = steps - full_replays * G
     with torch.cuda.stream(stream):
         for _ in range(2):
             graph.replay()
     stream.synchronize()
 
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(device)
     torch.cuda.synchronize(device)
@@ -419,23 +449,26 @@ def run_ours(a):
     torch.cuda.synchronize(device)
     barrier(device)
     t_wall1 = time.time()
-    time.sleep(0.3)
-    sampler.stop()
     elapsed_ms = e0.elapsed_time(e1)
     st = w4.w4a16_get_device_status(stream)
     if st != 0:
-        raise SystemExit(f"device status after timed region: {w4.status_string(st)}")
+        raise SystemExit(f"{workload}: device status after timed region: {w4.status_string(st)}")
     elapsed_ms = max_over_ranks(elapsed_ms, device)
+    del graph
 
-    # Per-shape breakdown (outside the timed region): back-to-back launches of one shape.
+    # Per-shape pass (outside the timed region): back-to-back launches of one shape in a
+    # graph, rotating over at least 3 x L2 of that shape's own weight copies.
     per_shape_ms = []
+    per_shape_region_s = []
     for j, (c, reps, A, Y) in enumerate(bufs):
+        cs = max(3, -(-3 * L2_BYTES // max(1, shape_packed[j])))
+        own = list(reps[:cs]) + [reps[0].clone() for _ in range(cs - len(reps))]
+        nl = max(20, cs)
         gj = torch.cuda.CUDAGraph()
-        nl = 20
         with torch.cuda.stream(stream):
             with torch.cuda.graph(gj, stream=stream):
                 for i in range(nl):
-                    gemm_call(j, A, reps[i % copies], Y, stream)
+                    gemm_call(j, A, own[i % cs], Y, stream)
             gj.replay()
             f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             f0.record(stream)
@@ -443,34 +476,51 @@ def run_ours(a):
                 gj.replay()
             f1.record(stream)
         stream.synchronize()
-        per_shape_ms.append(f0.elapsed_time(f1) / (3 * nl))
-        del gj
+        ms = f0.elapsed_time(f1)
+        per_shape_ms.append(ms / (3 * nl))
+        per_shape_region_s.append(ms * 1e-3)
+        del gj, own
+    torch.cuda.synchronize(device)
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"{workload}: device status after per-shape pass: {w4.status_string(st)}")
+
     peaks, peak_kind = measured_peaks()
     hbm_peak = float(peaks["hbm_gbs"])
-    launch_bytes = [shape_bytes(p, a.epilogue) for p in shapes]
+    launch_bytes = [shape_bytes(p, epilogue) for p in shapes]
+    launch_flops = [si.flops(p["M"], p["N"], p["K"]) for p in shapes]
     # The roofline is that of the dominant kernel (the one most launches of a step run
-    # on): its algorithmic bytes per launch over its average launch duration, both over
-    # its own shapes, the durations from the per-shape pass (CUDA events on the launch
-    # stream, back-to-back launches of one shape).
+    # on): its algorithmic bytes (or flops) per launch over its average launch duration,
+    # both over its own shapes, the durations from the per-shape pass (CUDA events on the
+    # launch stream, back-to-back launches of one shape).
     counts = {k: shape_kernel.count(k) for k in sorted(set(shape_kernel))}
     dominant = max(sorted(counts), key=lambda k: (counts[k], k == "w4a16_tc_kernel"))
     dom = [j for j, k in enumerate(shape_kernel) if k == dominant]
-    dom_bytes = sum(launch_bytes[j] for j in dom) / len(dom)
     dom_launch_s = sum(per_shape_ms[j] for j in dom) * 1e-3 / len(dom)
-    achieved_gbs = dom_bytes / dom_launch_s / 1e9
     # the recorded counters describe the default launch of the whole workload only
-    traffic = (profiled_traffic(a.workload, dominant)
-               if default_launch and a.epilogue == "none" and not a.shape else None)
-    # Decode-sized workloads are bound by HBM (TB/s over algorithmic bytes); prefill and
-    # batch-transition workloads (M >= 64 everywhere) by the tensor pipe (TFLOP/s).
-    compute_bound = min(p["M"] for p in shapes) >= 64
-    tflops_peak = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    if compute_bound:
-        value = step_flops * a.steps * ws / (elapsed_ms * 1e-3) / 1e12
-        unit = "TFLOP/s"
+    traffic = (profiled_traffic(workload, dominant)
+               if default_launch and epilogue == "none" and not a.shape else None)
+    if tfl:
+        dom_flops = sum(launch_flops[j] for j in dom) / len(dom)
+        achieved = dom_flops / dom_launch_s / 1e12
+        tpeak, tkind = tensor_peak(peaks, max(per_shape_region_s[j] for j in dom))
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": tpeak,
+                    "unit": "TFLOP/s", "frac": achieved / tpeak, "traffic": traffic,
+                    "peak_kind": f"{peak_kind} bf16 dense, {tkind} (the fp16 dense rate is "
+                                 f"the same)",
+                    "kernel": dominant, "launches_per_step": counts[dominant],
+                    "algorithmic_flops_per_launch": dom_flops}
+        value = step_flops * steps * ws / (elapsed_ms * 1e-3) / 1e12
     else:
-        value = step_bytes * a.steps * ws / (elapsed_ms * 1e-3) / 1e12
-        unit = "TB/s"
+        dom_bytes = sum(launch_bytes[j] for j in dom) / len(dom)
+        achieved = dom_bytes / dom_launch_s / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak,
+                    "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                    "peak_kind": peak_kind, "kernel": dominant,
+                    "launches_per_step": counts[dominant],
+                    "algorithmic_bytes_per_launch": dom_bytes}
+        value = step_bytes * steps * ws / (elapsed_ms * 1e-3) / 1e12
+    tpeak_shape, _ = tensor_peak(peaks, 0.0)
 
     # End to end through the public API, as a serving loop runs it: every step copies that
     # step's activations (all shapes, one copy) from pinned host memory, calls w4a16_gemm
@@ -524,7 +574,7 @@ def run_ours(a):
             hostY[b].copy_(devY[b], non_blocking=True)
             out_done[b].record(out_stream)
 
-    e2e_steps = max(1, min(a.e2e_steps, a.steps))
+    e2e_steps = max(1, min(a.e2e_steps, steps))
     e2e_steps = max(1, min(e2e_steps, int(8e9 // (h2d + d2h))))
     for i in range(3):
         e2e_step(i)
@@ -540,71 +590,126 @@ def run_ours(a):
     torch.cuda.synchronize(device)
     st = w4.w4a16_get_device_status(stream)
     if st != 0:
-        raise SystemExit(f"device status after end-to-end region: {w4.status_string(st)}")
+        raise SystemExit(f"{workload}: device status after end-to-end region: "
+                         f"{w4.status_string(st)}")
     e2e_ms = max_over_ranks(f0.elapsed_time(f1), device)
-    e2e_val = (step_flops if compute_bound else step_bytes) * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12
+    e2e_val = step_work * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12
 
-    cpu = None
-    if rank == 0 and ws == 1 and not a.no_cpu_baseline:
-        rate, desc, cores, used = cpu_oracle_rate(cases, shapes, budget_s=12.0)
-        cpu_val = rate / 1e12
-        if compute_bound:  # the oracle's rate in the same unit as the line (flops per byte)
-            cpu_val = rate * (step_flops / step_bytes) / 1e12
-        cpu = {"value": cpu_val, "unit": unit, "cores": cores, "kind": "oracle",
-               "sample": f"{desc}; {used:.1f} s of CPU time"}
-
-    if rank != 0:
-        return
     per_shape = []
-    for p, ms, b in zip(shapes, per_shape_ms, launch_bytes):
-        fl = si.flops(p["M"], p["N"], p["K"])
-        per_shape.append({"shape": si.shape_tag(p), "kernel": shape_kernel[len(per_shape)],
+    for j, (p, ms, b, fl) in enumerate(zip(shapes, per_shape_ms, launch_bytes, launch_flops)):
+        per_shape.append({"shape": si.shape_tag(p), "kernel": shape_kernel[j],
                           "us": round(ms * 1e3, 3),
                           "gbs": round(b / (ms * 1e-3) / 1e9, 1),
                           "hbm_frac": round(b / (ms * 1e-3) / 1e9 / hbm_peak, 4),
                           "tflops": round(fl / (ms * 1e-3) / 1e12, 1),
-                          "tensor_frac": round(fl / (ms * 1e-3) / 1e12 / tflops_peak, 4)})
-    clocks = sampler.summary(t_wall0, t_wall1)
+                          "tensor_frac": round(fl / (ms * 1e-3) / 1e12 / tpeak_shape, 4)})
+    m = Measured()
+    m.cases, m.shapes, m.tfl = cases, shapes, tfl
+    m.value, m.unit = value, metric_unit(shapes)
+    m.elapsed_ms, m.steps = elapsed_ms, steps
+    m.step_bytes, m.step_flops = step_bytes, step_flops
+    m.copies, m.packed_per_step, m.G = copies, packed_per_step, G
+    m.roofline, m.per_shape = roofline, per_shape
+    m.e2e = {"value": e2e_val, "unit": m.unit, "h2d_bytes_per_step": h2d,
+             "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+             "note": "per step: one pinned-host copy of all shapes' A in, one w4a16_gemm "
+                     "call per shape, one copy of all Y out; two buffer sets, copy-in and "
+                     "copy-out streams overlapping the neighbouring steps' GEMMs; packed "
+                     "weights resident (uploaded once, as in serving)"}
+    m.dominant, m.counts = dominant, counts
+    m.gpu_launches = steps * len(shapes)
+    m.clocks = sampler.summary(t_wall0, t_wall1)
+    del bufs, devA, devY, hostA, hostY
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    return m
+
+
+# Workloads timed beside the headline in a default run (M <= 16 decode at 70B scale, the
+# batch transition and prefill: the rest of the metric), each with its own roofline.
+EXTRA_WORKLOADS = ["ffn70b_decode_bf16", "transition_k8192_n8192",
+                   "prefill_m4096_k4096_n11008"]
+
+
+def run_ours(a):
+    import torch
+
+    ws, rank, local = dist_info()
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device (the library has no CPU path)")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if ws > 1:
+        dist_init("nccl")
+
+    from weight_only_int4_tma_gb300 import build as w4build
+    w4build.build()
+    import weight_only_int4_tma_gb300 as w4
+
+    ex = dict(kernel=a.kernel, split_k=a.split_k, tile_m=a.tile_m, stages=a.stages,
+              flags={"magic": 0, "lut": w4.W4A16_GEMM_DEQUANT_LUT,
+                     "int": w4.W4A16_GEMM_DEQUANT_INT}[a.dequant])
+    stream = torch.cuda.Stream(device=device)
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+
+    shapes = workload_shapes(a)
+    m = measure_workload(a, w4, device, stream, sampler, a.workload, shapes, ex, a.steps,
+                         a.warmup, a.epilogue)
+    extra = []
+    if a.extra_workloads and not a.shape and a.epilogue == "none" and not any(ex.values()):
+        for name in EXTRA_WORKLOADS:
+            if name == a.workload:
+                continue
+            shp = si.WORKLOADS[name]
+            x = measure_workload(a, w4, device, stream, sampler, name, shp, ex, a.steps,
+                                 a.warmup)
+            extra.append({
+                "workload": name, "metric": metric_name(name, shp), "value": x.value,
+                "unit": x.unit, "ms_per_step": x.elapsed_ms / x.steps, "steps": x.steps,
+                "shapes": len(shp), "step_bytes": x.step_bytes, "step_flops": x.step_flops,
+                "l2": f"inputs larger than L2: {x.copies} rotating copies of the packed "
+                      f"weights ({x.copies * x.packed_per_step / 2**20:.0f} MiB per rotation)",
+                "roofline": x.roofline, "per_shape": x.per_shape, "e2e": x.e2e,
+                "kernels_per_step": x.counts, "gpu_launches": x.gpu_launches,
+                "clocks": x.clocks})
+    time.sleep(0.3)
+    sampler.stop()
+
+    cpu = None
+    if rank == 0 and ws == 1 and not a.no_cpu_baseline:
+        rate, desc, cores, used = cpu_oracle_rate(m.cases, m.shapes, budget_s=12.0)
+        cpu = {"value": rate / 1e12, "unit": m.unit, "cores": cores, "kind": "oracle",
+               "sample": f"{desc}; {used:.1f} s of CPU time"}
+
+    if rank != 0:
+        return
     line = {
-        "metric": ("W4A16 GEMM achieved tensor TFLOP/s" if compute_bound else
-                   "W4A16 GEMM achieved HBM TB/s") + f" ({a.workload})",
-        "value": value, "unit": unit, "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
-        "ms_per_step": elapsed_ms / a.steps, "higher_is_better": True, "scaling": "weak",
+        "metric": metric_name(a.workload, shapes),
+        "value": m.value, "unit": m.unit, "n_gpus": ws, "steps": a.steps, "warmup": a.warmup,
+        "ms_per_step": m.elapsed_ms / a.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "config": {"workload": a.workload, "shapes": len(shapes),
                    **({"epilogue": a.epilogue} if a.epilogue != "none" else {}),
                    **({"shape_subset": a.shape} if a.shape else {}),
-                   "step_bytes": step_bytes,
-                   "step_flops": step_flops,
-                   "l2": f"inputs larger than L2: {copies} rotating copies of the packed "
-                         f"weights ({copies * packed_per_step / 2**20:.0f} MiB per rotation)",
-                   "timing": f"CUDA graph of {G} steps replayed; CUDA events on the launch "
+                   "step_bytes": m.step_bytes,
+                   "step_flops": m.step_flops,
+                   "l2": f"inputs larger than L2: {m.copies} rotating copies of the packed "
+                         f"weights ({m.copies * m.packed_per_step / 2**20:.0f} MiB per rotation)",
+                   "timing": f"CUDA graph of {m.G} steps replayed; CUDA events on the launch "
                              f"stream around the whole timed region", "parallelism": f"replicas{ws}",
                    "kernel": a.kernel, "split_k": a.split_k, "tile_m": a.tile_m,
                    "stages": a.stages, **({"dequant": a.dequant} if a.dequant != "magic" else {})},
-        "roofline": ({"bound": "tensor", "achieved": value, "peak": tflops_peak,
-                      "unit": "TFLOP/s", "frac": value / tflops_peak, "traffic": traffic,
-                      "peak_kind": f"{peak_kind} bf16 sustained (fp16 dense rate is the same)",
-                      "algorithmic_flops_per_launch": step_flops / len(shapes)}
-                     if compute_bound else
-                     {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_peak,
-                      "unit": "GB/s", "frac": achieved_gbs / hbm_peak,
-                      "traffic": traffic, "peak_kind": peak_kind, "kernel": dominant,
-                      "launches_per_step": counts[dominant],
-                      "algorithmic_bytes_per_launch": dom_bytes}),
-        "per_shape": per_shape,
+        "roofline": m.roofline,
+        "per_shape": m.per_shape,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_val, "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps,
-                "note": "per step: one pinned-host copy of all shapes' A in, one w4a16_gemm "
-                        "call per shape, one copy of all Y out; two buffer sets, copy-in and "
-                        "copy-out streams overlapping the neighbouring steps' GEMMs; packed "
-                        "weights resident (uploaded once, as in serving)"},
-        "kernel": dominant,
-        "kernels_per_step": counts,
-        "gpu_launches": a.steps * len(shapes),
-        "clocks": clocks,
+        "e2e": m.e2e,
+        "kernel": m.dominant,
+        "kernels_per_step": m.counts,
+        "gpu_launches": m.gpu_launches,
+        "clocks": m.clocks,
+        "per_workload": extra,
     }
     print(json.dumps(line), flush=True)
 

@@ -118,7 +118,10 @@ const char* w4a16_status_string(int status);
 
 /*
  * Size in bytes of the packed blob that w4a16_repack writes for these arguments, or 0
- * if the shape is unsupported (see w4a16_repack).  With Np = N and Kp = K rounded up to
+ * if the shape is unsupported (see w4a16_repack).  Source: "量化开销对比" §6.4 (weights,
+ * scales and zeros repacked offline into the kernel's tile order) and "W4A16 GEMM 算子浅析"
+ * §"Marlin 与 CUTLASS 中的寄存器解包黑魔法" (eight 4-bit weights per uint32, hence K*N/2
+ * bytes of nibbles).  Host-only: touches no device memory.  With Np = N and Kp = K rounded up to
  * multiples of 128, the blob is
  *     128-byte header
  *   + Kp*Np/2 bytes of nibbles
@@ -223,13 +226,21 @@ int w4a16_gemm_plan(int M, int N, int K, int group, int dtype, const w4a16_gemm_
 
 /*
  * Debug / parity only: expand the packed blob to dtype W_out[N][K] (row-major, device)
- * with exactly the unpack + dequant arithmetic the GEMM kernels use.  This is the
- * materialised-weight path the pages warn against; it is never used by w4a16_gemm.
+ * with exactly the unpack + dequant arithmetic the GEMM kernels use, i.e. step 2 of the
+ * pipeline in "W4A16 GEMM 算子浅析" §"计算流水线的核心哲学", W = (W_int4 - Zero) * Scale,
+ * rounded once to nearest-even into dtype.  This is the materialised-weight path that
+ * "量化开销对比" §6.1 warns against; it is never used by w4a16_gemm.
+ *   packed  device, blob written by w4a16_repack with the same N, K, group, dtype.
+ *   W_out   device output, dtype [N][K], 16-byte aligned (caller-owned).
+ * The header is checked as in w4a16_gemm (W4A16_ERR_FORMAT in the status word, W_out
+ * untouched).  Errors returned directly: INVALID_ARG, UNSUPPORTED, CUDA.
  */
 int w4a16_dequant_debug(const void* packed, int N, int K, int group, int dtype,
                         void* W_out, void* stream);
 
 /*
+ * Library infrastructure (no passage of the pages describes it): the error channel of
+ * the kernels' bounded waits and header checks.
  * Synchronises `stream`, then reads and clears the current device's status word.
  * Returns W4A16_OK, or the first error a kernel recorded since the last call
  * (W4A16_ERR_FORMAT, W4A16_ERR_DEVICE_TIMEOUT), or W4A16_ERR_CUDA if the stream itself

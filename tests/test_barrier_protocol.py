@@ -11,6 +11,11 @@ Layout modelled (as in csrc/gemm_tc.cu): ring slots full[s] / empty[s]; W buffer
 with tfull[issuer][t] (count: the warps that write the tile) and
 tempty[warpgroup][t] (one MMA commit).  Decode tiles: warpgroup w unpacks blocks
 w, w + NWG, ...; larger tiles: every warpgroup unpacks every block.
+
+Events carry their own times (the heap key), and every callback is given that time, so
+the random latencies really reorder the agents; the earlier shared layout (one tfull and
+one tempty per W buffer for both issuers and both warpgroups) is flagged by the model,
+the per-party layout is not.
 """
 import heapq
 import itertools
@@ -145,8 +150,8 @@ def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
     for ai in range(len(agents)):
         at(rng.uniform(0, 0.5), lambda n, ai=ai: step(ai, n))
     while events and not errors:
-        _, _, f = heapq.heappop(events)
-        f(_)
+        t_ev, _, f = heapq.heappop(events)
+        f(t_ev)
     if errors:
         return errors[0]
     if len(finished) != len(agents) or waiting:
@@ -189,3 +194,68 @@ def test_model_catches_a_ring_depth_that_breaks_the_rule():
         hits = sum(1 for trial in range(20)
                    if simulate(1, 4, 2, 1, S, 16, random.Random(trial), interleave=True))
         assert hits > 0, S
+
+
+def test_model_reproduces_the_shared_layout_failure():
+    """The first layout of whole-block warpgroups shared one tfull[t] / tempty[t] per W
+    buffer between both MMA issuers and both warpgroups; on the GPU it ran into the
+    bounded-wait timeout in about one decode run of two.  The interleaving: with three W
+    buffers and two issuers, buffer t holds blocks b, b + 3, ... written by alternating
+    warpgroups and consumed by alternating issuers.  When block b + 1 (other group) is
+    finished before block b, the issuer of b + 1 moves on to b + 3 and parity-waits on
+    tfull[t] for phase j + 1 while phase j (block b) is still open; that parity is the
+    one of the completed phase j - 1, so the wait returns at once and the MMA reads a
+    buffer that block b is still being written into.  The model must flag it (decode-tile
+    parameters: 2 issuers, 2 warpgroups, 3 W buffers, 2 blocks per stage), and must not
+    flag the per-party layout with the same parameters and seeds."""
+    shared = per_party = 0
+    for S in (2, 4, 6):
+        for trial in range(40):
+            e = simulate(2, 2, 3, 2, S, 16, random.Random(trial), True, per_party=False)
+            shared += e is not None and e.startswith("parity alias")
+            per_party += simulate(2, 2, 3, 2, S, 16, random.Random(trial), True) is not None
+    assert shared > 20, shared
+    assert per_party == 0, per_party
+
+
+def exchange_model(ranks, rng, exit_barrier, limit=10.0, late_rank=None):
+    """Split-K exchange of one cluster: every rank finishes its K slice at a random time,
+    pushes its partial of every other rank's slice (each push lands after a random
+    latency), waits for the pushes into its own receive area with a bounded wait, and
+    exits.  With exit_barrier the ranks meet at a cluster barrier before exiting (a rank
+    arrives once its pushes have been read out) and then wait, bounded again, for any
+    push still landing.  `late_rank` finishes after the others' waits have run out.
+    Returns the number of pushes that land in a rank after it has exited."""
+    done = [rng.uniform(0.0, 2.0) for _ in range(ranks)]
+    if late_rank is not None:
+        done[late_rank] = 3.0 * limit
+    land = {(src, dst): done[src] + rng.uniform(0.05, 0.5)
+            for src in range(ranks) for dst in range(ranks) if src != dst}
+    read_out = [done[r] + 0.05 for r in range(ranks)]  # source reads of its pushes done
+    recv_end = []
+    for r in range(ranks):
+        arrivals = [land[(s, r)] for s in range(ranks) if s != r]
+        start = done[r] + 0.05
+        recv_end.append(min(max(arrivals), start + limit))
+    if not exit_barrier:
+        exit_t = recv_end
+    else:
+        release = max(max(recv_end[r], read_out[r]) for r in range(ranks))
+        exit_t = []
+        for r in range(ranks):
+            arrivals = [land[(s, r)] for s in range(ranks) if s != r]
+            exit_t.append(max(release, min(max(arrivals), release + limit)))
+    return sum(1 for (s, d), t in land.items() if t > exit_t[d])
+
+
+def test_split_k_exit_waits_for_every_push():
+    """With the exit barrier no push ever lands in a rank that has left, also when one
+    rank is so late that the others' receive waits run out; without it, such a late
+    rank's pushes land in exited ranks (the undefined case the barrier removes)."""
+    for ranks in (2, 3, 8):
+        for trial in range(50):
+            rng = random.Random(trial)
+            assert exchange_model(ranks, rng, exit_barrier=True) == 0
+            late = trial % ranks
+            assert exchange_model(ranks, random.Random(trial), True, late_rank=late) == 0
+    assert sum(exchange_model(3, random.Random(t), False, late_rank=0) for t in range(20)) > 0

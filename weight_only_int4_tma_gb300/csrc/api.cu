@@ -170,6 +170,14 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
         if (stages > 8) stages = 8;
         stages -= stages % mult;
     }
+    // With split-K a rank first writes its own partials of every slice to the start of
+    // the ring (then pushes them to the owners), so the ring must hold recv bytes.
+    const int stage_b = static_cast<int>(tc_stage_bytes(bm, M, group));
+    if (split > 1 && stages * stage_b < recv) {
+        if (cfg && cfg->stages) return W4A16_ERR_UNSUPPORTED;
+        while (stages * stage_b < recv && stages + mult <= max_st) stages += mult;
+    }
+    if (split > 1 && stages * stage_b < recv) return W4A16_ERR_UNSUPPORTED;
     if (stages < 2 || stages > max_st || stages % mult != 0) return W4A16_ERR_UNSUPPORTED;
     plan->tile_m = bm;
     plan->split_k = split;

@@ -58,27 +58,6 @@ namespace {
 constexpr int kMaxStages = 16;
 constexpr int kCtrlBytes = 1024;
 
-#ifdef W4A16_TRACE
-// Development-only timeline (built with -DW4A16_TRACE, never in the product library):
-// every CTA claims one record (in start order, across launches) and stamps globaltimer
-// values into its slots; slots 57..59 identify the launch and the CTA.
-constexpr int kTraceRecs = 8192;
-constexpr int kTraceSlots = 64;
-__device__ unsigned long long g_w4a16_trace[kTraceRecs * kTraceSlots];
-__device__ unsigned int g_w4a16_trace_next;
-#define W4G_TRACE(slot, value)                                                         \
-    do {                                                                              \
-        const int slot_ = (slot);                                                     \
-        if (trace_rec < static_cast<unsigned>(kTraceRecs) && slot_ >= 0 &&            \
-            slot_ < kTraceSlots)                                                      \
-            g_w4a16_trace[trace_rec * kTraceSlots + slot_] = (value);                 \
-    } while (0)
-#define W4G_NOW() globaltimer_ns()
-#else
-#define W4G_TRACE(slot, value) do { } while (0)
-#define W4G_NOW() 0ull
-#endif
-
 #ifndef W4A16_BIG_TILE_WG
 #define W4A16_BIG_TILE_WG 2    // dequant warpgroups for 256-row tiles
 #endif
@@ -344,21 +323,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const bool prefetch_w = (args.flags & kFlagPrefetchW) != 0;
     const uint32_t slice_bytes = static_cast<uint32_t>(BM * args.slice_rows * 4);
 
-#ifdef W4A16_TRACE
-    unsigned trace_rec = 0xFFFFFFFFu;
-    if (threadIdx.x == 0) {
-        trace_rec = atomicAdd(&g_w4a16_trace_next, 1u);
-        *reinterpret_cast<unsigned*>(ctrl_ptr + 488) = trace_rec;
-        W4G_TRACE(57, static_cast<unsigned long long>(args.M) |
-                          (static_cast<unsigned long long>(args.N) << 16) |
-                          (static_cast<unsigned long long>(args.K) << 32));
-        W4G_TRACE(58, blockIdx.x | (static_cast<unsigned long long>(blockIdx.y) << 16) |
-                          (static_cast<unsigned long long>(blockIdx.z) << 32));
-        unsigned smid_;
-        asm volatile("mov.u32 %0, %%smid;" : "=r"(smid_));
-        W4G_TRACE(59, smid_);
-    }
-#endif
     // Thread 0 issues the header load first (its latency overlaps the barrier setup; with
     // weight prefetch disabled it must wait for the previous kernel instead), and warp 0
     // spreads the barrier initialisation over its lanes.
@@ -369,7 +333,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     }
     if (warp == 0) {
         if (lane == 0) {
-            W4G_TRACE(0, W4G_NOW());
             *abort_flag = 0;
         }
         for (int s = lane; s < args.stages; s += 32) {
@@ -392,7 +355,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         if (lane == 0) {
             if (args.splits > 1)  // partials of the other ranks for this rank's slice
                 mbar_arrive_expect_tx(recv_bar, static_cast<uint32_t>(args.splits - 1) * slice_bytes);
-            W4G_TRACE(61, W4G_NOW());
             if (!prefetch_w) {
                 grid_dep_wait();
                 const uint4* hp = reinterpret_cast<const uint4*>(args.packed);
@@ -410,15 +372,11 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             if (flags < 0 && split == 0 && n_tile == 0 && m_tile == 0)
                 record_status(args.status, kStatusFormat);
             prefetch_tensormap(&tmap_a);
-            W4G_TRACE(62, W4G_NOW());
         }
     }
     if (warp == 1) {
         tmem_alloc(smem_addr(tmem_slot), S::kTmemCols);
         tmem_relinquish();
-#ifdef W4A16_TRACE
-        if (lane == 0) *reinterpret_cast<unsigned long long*>(ctrl_ptr + 696) = W4G_NOW();
-#endif
     }
     tc_fence_before();
     __syncthreads();
@@ -427,13 +385,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     if (threadIdx.x == 0) grid_dep_launch();
 
     const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
-#ifdef W4A16_TRACE
-    trace_rec = *reinterpret_cast<const unsigned*>(ctrl_ptr + 488);
-    if (threadIdx.x == 0) {
-        W4G_TRACE(1, W4G_NOW());
-        W4G_TRACE(63, *reinterpret_cast<const unsigned long long*>(ctrl_ptr + 696));
-    }
-#endif
     const int flags = __shfl_sync(0xffffffffu, info[0], 0);
     const bool run = flags >= 0 && nkb > 0;
     const bool has_z = flags >= 0 && (flags & kFlagZeros) != 0;
@@ -478,7 +429,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
                 if (S::kInterleave) mbar_arrive_expect_tx(afull0 + 8 * i, a_bytes);
                 load_a(st, (kb0 + i * kps) * 2, afull0 + 8 * i);
-                if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
             }
             int issued = pre;
             int s = pre;              // ring slot of stage i, and the parity of its use
@@ -499,7 +449,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     tma_bulk_g2s(st + a_bytes, wsrc, nblk * bb, fb, pol_w);
                     if (S::kInterleave) mbar_arrive_expect_tx(ab, a_bytes);
                     load_a(st, kchunk, ab);
-                    if (i < 8) W4G_TRACE(2 + i, W4G_NOW());
                 }
                 ++issued;
                 left -= kps;
@@ -548,7 +497,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                                                abort_flag, args.status, tlim);
                 fpar ^= 1u << t;
                 if (!ok) break;
-                if (lane == 0 && i < 8) W4G_TRACE(34 + i, W4G_NOW());
                 tc_fence_after();
                 const uint64_t d0 = sw128_desc(base + static_cast<uint32_t>(s) * args.stage_bytes) +
                                     static_cast<uint64_t>(2 * b) * chunk16;
@@ -574,7 +522,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     tc_commit(te);
                     if (kInt) tc_commit(dfull0 + dslot / 2);  // 8 bytes per (k, slot)
                     if (stage_done) tc_commit(empty0 + 8 * s);
-                    if (i < 8) W4G_TRACE(42 + i, W4G_NOW());
                 }
                 __syncwarp();
                 t += kNMI;
@@ -584,7 +531,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             }
             if (lane == 0) {
                 tc_commit(accum_bar);
-                W4G_TRACE(50, W4G_NOW());
             }
             if (!ok && lane == 0) {  // no MMA may still read TMEM/SMEM when the CTA exits
                 int dummy = 0;
@@ -650,14 +596,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         for (int i = S::kInterleave ? wg : 0; i < nkb && ok; i += kBStep) {   // 128-K block
             if (S::kInterleave || b == 0)  // (s, b, t) advance at the loop end
                 ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
-            if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(10 + i, W4G_NOW());
             if (ok && i >= kTBuf) {
                 ok = mbar_wait_warp(tempty0 + 8 * (tw * kTBuf + t), (epar >> t) & 1u, abort_flag,
                                     args.status, tlim);
                 epar ^= 1u << t;
             }
             if (!ok) break;
-            if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(18 + i, W4G_NOW());
             const uint8_t* wb = base_ptr + a_bytes + static_cast<size_t>(s) * args.stage_bytes +
                                 static_cast<size_t>(b) * bb;
             float s_cur = 0.0f;  // kInt: the block's scale for row r
@@ -675,7 +619,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tfull0 + 8 * ((i % kNMI) * kTBuf + t));
-            if (warp == S::kDq0 && lane == 0 && i < 8) W4G_TRACE(26 + i, W4G_NOW());
             if constexpr (kInt) {  // the previous block's partial, while this one is in the MMA
                 if (jn > 0) rescale(jn - 1, s_last);
                 s_last = s_cur;
@@ -718,7 +661,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             named_bar_sync(2, kEpiThreads);  // both groups' sums are in place
         }
         if (ok) {
-            if (warp == S::kDq0 && lane == 0) W4G_TRACE(51, W4G_NOW());
             tc_fence_after();
             const int n = n_tile * kTileN + r;
             uint16_t* Y = static_cast<uint16_t*>(args.Y);
@@ -853,7 +795,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 }
             }
         }
-        if (warp == S::kDq0 && lane == 0) W4G_TRACE(52, W4G_NOW());
         if (args.splits > 1) {
             // Push our partial of every other rank's slice into that rank's receive area.
             fence_proxy_async_smem();
@@ -861,7 +802,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             cluster_wait_acquire();  // every peer has initialised its receive barrier
             const uint32_t rank = cluster_ctarank();
             if (warp == S::kDq0) {  // lane p sends the slice of rank p
-                if (lane == 0) W4G_TRACE(53, W4G_NOW());
                 const int p = lane;
                 if (p < args.splits && p != static_cast<int>(rank)) {
                     const uint32_t src = base + static_cast<uint32_t>(p) * slice_bytes;
@@ -873,10 +813,13 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 }
                 __syncwarp();
             }
-            // Sum this rank's slice over all ranks, in rank order, and store it.
-            const bool got = mbar_wait_warp(recv_bar, 0, abort_flag, args.status, tlim);
+            // Sum this rank's slice over all ranks, in rank order, and store it.  Every
+            // peer pushes its partial even after a failure of its own, so this wait is
+            // bounded by time only (not by this CTA's abort flag): the pushes are allowed
+            // to land before the CTA may leave.
+            volatile int no_abort = 0;
+            const bool got = mbar_wait_warp(recv_bar, 0, &no_abort, args.status, tlim);
             if (ok && got) {
-                if (warp == S::kDq0 && lane == 0) W4G_TRACE(54, W4G_NOW());
                 grid_dep_wait();
                 const int r0 = static_cast<int>(rank) * R;
                 const int nr = min(min(kTileN, r0 + R), args.N - n_tile * kTileN) - r0;
@@ -903,11 +846,22 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             }
         }
     }
-    if (threadIdx.x == 0) W4G_TRACE(55, W4G_NOW());
 
     tc_fence_before();
     __syncthreads();
-    if (threadIdx.x == 0) W4G_TRACE(60, W4G_NOW());
+    // A cluster rank must not exit while a peer may still push partials into its shared
+    // memory (after a timed-out wait on the receive barrier, for instance): every rank
+    // reaches this barrier once its own pushes have been read out, since every earlier
+    // wait is bounded.
+    if (args.splits > 1) {
+        cluster_sync_all();
+        // Every peer has now issued its push into this CTA; if the receive wait above
+        // ran out, give those pushes (bounded) time to land before the CTA exits.
+        if (threadIdx.x == 0) {
+            int dummy = 0;
+            (void)mbar_wait_bounded(recv_bar, 0, &dummy, nullptr, tlim);
+        }
+    }
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -949,29 +903,57 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     // chunk past K is outside the view and arrives as zeros.  If K is not a multiple of
     // 64 that view does not exist: A is then the plain 2-D [M][K] tensor and every 64-K
     // chunk is its own box (the part past K zero-filled), in the same shared layout.
-    CUtensorMap map;
     const bool a_2d = K % 64 != 0;
-    const auto dt = DT == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    CUresult cr;
-    if (!a_2d) {
-        const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
-        const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
-        const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(a_rows),
-                                   static_cast<cuuint32_t>(2 * kps)};
-        const cuuint32_t estr[3] = {1, 1, 1};
-        cr = enc(&map, dt, 3, const_cast<void*>(A), dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    } else {
-        const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-        const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-        const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(a_rows)};
-        const cuuint32_t estr[2] = {1, 1};
-        cr = enc(&map, dt, 2, const_cast<void*>(A), dims, strides, box, estr,
-                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    // Encoding a tensor map costs host time on every call; the encoded map depends only
+    // on the values below, so each host thread keeps the last few it made.
+    struct MapEntry {
+        CUtensorMap map;
+        const void* ptr;
+        int M, K, a_rows, kps, dt, valid;
+    };
+    thread_local MapEntry cache[8];
+    thread_local int cache_next = 0;
+    const CUtensorMap* mp = nullptr;
+    for (const MapEntry& e : cache)
+        if (e.valid && e.ptr == A && e.M == M && e.K == K && e.a_rows == a_rows && e.kps == kps &&
+            e.dt == DT) {
+            mp = &e.map;
+            break;
+        }
+    if (!mp) {
+        MapEntry& e = cache[cache_next];
+        cache_next = (cache_next + 1) % 8;
+        e.valid = 0;
+        const auto dt = DT == 0 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+        CUresult cr;
+        if (!a_2d) {
+            const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(M), static_cast<cuuint64_t>(K / 64)};
+            const cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, 128};
+            const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(a_rows),
+                                       static_cast<cuuint32_t>(2 * kps)};
+            const cuuint32_t estr[3] = {1, 1, 1};
+            cr = enc(&e.map, dt, 3, const_cast<void*>(A), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        } else {
+            const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+            const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+            const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(a_rows)};
+            const cuuint32_t estr[2] = {1, 1};
+            cr = enc(&e.map, dt, 2, const_cast<void*>(A), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        }
+        if (cr != CUDA_SUCCESS) return -3;
+        e.ptr = A;
+        e.M = M;
+        e.K = K;
+        e.a_rows = a_rows;
+        e.kps = kps;
+        e.dt = DT;
+        e.valid = 1;
+        mp = &e.map;
     }
-    if (cr != CUDA_SUCCESS) return -3;
 
     TcArgs args;
     args.packed = static_cast<const uint8_t*>(packed);
@@ -993,7 +975,9 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     const uint32_t ring = static_cast<uint32_t>(plan.stages) * args.stage_bytes;
     const uint32_t recv_bytes = plan.split_k > 1
         ? static_cast<uint32_t>(plan.split_k * BM * args.slice_rows * 4) : 0u;
-    if (plan.split_k > 1 && recv_bytes > ring) return -2;  // partials are staged in the ring
+    // This rank's own partials (all slices) are written to the start of the ring before
+    // they are pushed; the receive area for the peers' partials follows the ring.
+    if (plan.split_k > 1 && recv_bytes > ring) return -2;
     args.recv_off = ring;
     args.timeout_ns = ctx.timeout_ns;
     args.epi = epi;
@@ -1037,25 +1021,11 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     }
     cfg.attrs = attr;
     cfg.numAttrs = nattr;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, map, args);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kern, *mp, args);
     return e == cudaSuccess ? 0 : -3;
 }
 
 }  // namespace
-
-#ifdef W4A16_TRACE
-extern "C" int w4a16_trace_read(void* host, size_t bytes) {
-    if (bytes > sizeof(g_w4a16_trace)) bytes = sizeof(g_w4a16_trace);
-    return cudaMemcpyFromSymbol(host, g_w4a16_trace, bytes) == cudaSuccess ? 0 : -3;
-}
-extern "C" int w4a16_trace_clear(void) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_w4a16_trace) != cudaSuccess) return -3;
-    if (cudaMemset(p, 0, sizeof(g_w4a16_trace)) != cudaSuccess) return -3;
-    const unsigned zero = 0;
-    return cudaMemcpyToSymbol(g_w4a16_trace_next, &zero, sizeof(zero)) == cudaSuccess ? 0 : -3;
-}
-#endif
 
 int tc_a_rows(int tile_m, int M) {
     if (tile_m > 16) return tile_m;

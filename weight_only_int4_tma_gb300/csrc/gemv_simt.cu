@@ -8,20 +8,22 @@
 //
 // Work split.  A unit is ROWS (16 or 32) consecutive output channels over the whole K
 // range.  The grid is persistent (at most as many CTAs as fit on the GPU at once); CTA b
-// takes units b, b + grid, ...  Its 8 warps split K: warp w handles the 128-K blocks
-// w, w + 8, ... of every unit, so partial sums never leave the CTA.  Each warp runs its
-// own ring of shared-memory stages: lane 0 fills a stage with bulk TMA copies (the ROWS
-// rows of the four 32-K chunks of one block, 256 or 512 contiguous bytes each, plus the
-// scales and zeros of those rows), all 32 lanes wait on the stage's mbarrier, unpack and
-// multiply, and lane 0 refills the stage with the warp's next block -- across unit
-// boundaries, so the stream never drains between units.  A thread owns one channel (and,
-// for ROWS = 16, every other chunk).  A is read through the L1 cache with broadcast
-// 128-bit loads.  At the end of a unit the warps' fp32 partials are combined in shared
-// memory in warp order (deterministic) and stored as Y.
+// takes units b, b + grid, ...  Its 8 warps form 256 / ROWS K slots (a slot is ROWS
+// lanes); slot p handles the 128-K blocks p, p + slots, ... of every unit, so partial
+// sums never leave the CTA.  A thread owns one channel of its slot and streams, per
+// block, its 64 bytes of nibbles (four 16-byte pieces, one per 32-K chunk) and the 4-byte
+// words holding its scale and zero into a private ring of kGemvStages shared-memory
+// stages with per-thread cp.async copies; completion is tracked per thread with
+// cp.async commit groups (cp.async.wait_group), so no thread waits on another and there
+// is no mbarrier.  The ring is refilled with the thread's next block -- across unit
+// boundaries, so the stream never drains between units.  A is read through the L1 cache
+// with broadcast 128-bit loads.  At the end of a unit the slots' fp32 partials are
+// combined in shared memory in slot order (deterministic) and stored as Y.
 //
 // With programmatic dependent launch the header check and the first ring stages run
 // before the dependency wait (the packed weights do not depend on the previous kernel);
-// A is read and Y written only after it.  Every mbarrier wait is bounded.
+// A is read and Y written only after it.  The kernel has no spin-wait: cp.async
+// completion waits end when the thread's own copies land.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
