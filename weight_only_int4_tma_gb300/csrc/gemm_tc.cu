@@ -83,6 +83,7 @@ struct TcArgs {
     uint32_t stage_bytes;
     uint32_t recv_off;    // offset of the split-K receive area from the ring base
     uint64_t timeout_ns;
+    int l2_ahead;         // CTA c < l2_ahead prefetches the weights of CTAs c + l2_ahead, ...
     EpilogueArgs epi;     // bias / activation / residual applied to the fp32 result
 };
 
@@ -372,6 +373,23 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             if (flags < 0 && split == 0 && n_tile == 0 && m_tile == 0)
                 record_status(args.status, kStatusFormat);
             prefetch_tensormap(&tmap_a);
+            // The CTAs that start first (in the slots the previous kernel left free) pull
+            // the weight slices of the CTAs that can only start once that kernel's CTAs
+            // exit into L2, so that those find their first bytes in L2 and the weights
+            // stream while the previous kernel finishes (its tail leaves HBM idle).
+            const int nlin = args.splits * static_cast<int>(gridDim.y);  // one m tile's CTAs
+            const int c = split + args.splits * (n_tile + static_cast<int>(gridDim.y) * m_tile);
+            if (flags >= 0 && args.l2_ahead > 0 && c < args.l2_ahead) {
+                const uint32_t bbl = hl.block_bytes;
+                for (int c2 = c + args.l2_ahead; c2 < nlin; c2 += args.l2_ahead) {
+                    const int s2 = c2 % args.splits, t2 = c2 / args.splits;
+                    const int kb2 = s2 * kb_per + (s2 < kb_rem ? s2 : kb_rem);
+                    const int nk2 = kb_per + (s2 < kb_rem ? 1 : 0);
+                    bulk_prefetch_l2(args.packed + kHeaderBytes +
+                                         (static_cast<size_t>(t2) * args.kblocks + kb2) * bbl,
+                                     static_cast<uint32_t>(nk2) * bbl);
+                }
+            }
         }
     }
     if (warp == 1) {
@@ -381,7 +399,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (args.splits > 1) cluster_arrive_release();  // peers may now target our barriers
+    // peers may now target our barriers (their initialisation is fenced at cluster scope)
+    if (args.splits > 1) cluster_arrive_relaxed();
     if (threadIdx.x == 0) grid_dep_launch();
 
     const uint32_t tmem = __shfl_sync(0xffffffffu, *tmem_slot, 0);
@@ -470,7 +489,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             }
         }
         __syncwarp();
-        if (args.splits > 1) cluster_wait_acquire();
+        if (args.splits > 1) {  // phase 0 (peers' barriers ready), then arrive for the exit
+            cluster_wait_acquire();
+            cluster_arrive_relaxed();
+        }
     } else if (warp <= kNMI) {
         // ---------------- MMA issuers (one thread per warp) ----------------
         const int k = warp - 1;  // issuer index: blocks k, k + kNMI, ...
@@ -540,7 +562,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             tc_commit(accum_bar);  // no MMAs to track: arrive at once
         }
         __syncwarp();
-        if (args.splits > 1) cluster_wait_acquire();
+        if (args.splits > 1) {
+            cluster_wait_acquire();
+            cluster_arrive_relaxed();
+        }
     } else {
         // ---------------- dequant warps ----------------
         const int q = warp & 3;                 // TMEM lane quarter of this warp
@@ -814,11 +839,15 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 __syncwarp();
             }
             // Sum this rank's slice over all ranks, in rank order, and store it.  Every
-            // peer pushes its partial even after a failure of its own, so this wait is
-            // bounded by time only (not by this CTA's abort flag): the pushes are allowed
-            // to land before the CTA may leave.
+            // peer pushes its partial even after a failure of its own (a peer is late by
+            // at most one wait limit), so this wait is bounded by time only, twice the
+            // limit, not by this CTA's abort flag: the pushes are allowed to land before
+            // the CTA may leave.  Arriving at the exit phase of the cluster barrier right
+            // after it tells the peers that their pushes into this CTA have landed, i.e.
+            // that their sources have been read.
             volatile int no_abort = 0;
-            const bool got = mbar_wait_warp(recv_bar, 0, &no_abort, args.status, tlim);
+            const bool got = mbar_wait_warp(recv_bar, 0, &no_abort, args.status, 2 * tlim);
+            cluster_arrive_relaxed();
             if (ok && got) {
                 grid_dep_wait();
                 const int r0 = static_cast<int>(rank) * R;
@@ -850,11 +879,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     tc_fence_before();
     __syncthreads();
     // A cluster rank must not exit while a peer may still push partials into its shared
-    // memory (after a timed-out wait on the receive barrier, for instance): every rank
-    // reaches this barrier once its own pushes have been read out, since every earlier
-    // wait is bounded.
+    // memory, or read its own partials out of it: every rank arrives at the exit phase
+    // once the pushes into it have landed (or the bounded wait for them ran out), and
+    // leaves only when all ranks have arrived.  In the normal case the peers arrived
+    // long before this rank's own stores are done, so the wait costs nothing.
     if (args.splits > 1) {
-        cluster_sync_all();
+        cluster_wait_acquire();
         // Every peer has now issued its push into this CTA; if the receive wait above
         // ran out, give those pushes (bounded) time to land before the CTA exits.
         if (threadIdx.x == 0) {
@@ -980,6 +1010,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     if (plan.split_k > 1 && recv_bytes > ring) return -2;
     args.recv_off = ring;
     args.timeout_ns = ctx.timeout_ns;
+    args.l2_ahead = plan.l2_ahead;
     args.epi = epi;
 
     const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;

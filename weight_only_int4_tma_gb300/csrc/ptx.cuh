@@ -223,6 +223,12 @@ __device__ __forceinline__ void tma_tensor_3d_g2s(uint32_t dst, const CUtensorMa
         : "memory");
 }
 
+// Bulk prefetch of a contiguous global range into L2 (a hint: no completion to track;
+// 16-byte aligned address, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -339,6 +345,14 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t caddr) {
 // late (all threads of every CTA of the cluster take part in both).
 __device__ __forceinline__ void cluster_arrive_release() {
     asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+// Arrive without ordering this thread's memory operations: for barrier phases that only
+// signal progress (the memory they protect is ordered by other means, e.g. an mbarrier
+// initialisation fenced with fence.mbarrier_init.release.cluster, or a completed
+// complete_tx).  A release arrive waits for the thread's prior accesses to be performed at
+// cluster scope, which is measurably slower on the critical path.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait_acquire() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
