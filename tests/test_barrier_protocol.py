@@ -160,10 +160,12 @@ def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
 
 
 def configs(interleave):
+    # (2, 2): decode tiles; (1, 1): 64- and 128-row tiles (whole blocks: 2 or 4 groups,
+    # 3 or 6 W buffers); (1, 2): a single-issuer variant of the two-block stage
     for kNMI, kps in ((2, 2), (1, 1), (1, 2)):
-        for T in (2, 3):
+        for T in (2, 3, 6):
             for NWG in (1, 2, 4):
-                for S in (2, 3, 4, 5, 6):
+                for S in (2, 3, 4, 5, 6, 8):
                     # host rule: with whole blocks per group, the ring depth is a multiple
                     # of groups per stage
                     if interleave and NWG > kps and S % (NWG // kps):

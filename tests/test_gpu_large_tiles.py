@@ -1,0 +1,70 @@
+"""GPU parity of the tensor-core kernel's larger tiles, one test per tile instance the
+launch choice can take: 64- and 128-row tiles whose two warpgroups share every block
+(with and without split-K), 128-row tiles alone on an SM with one K slice (four
+warpgroups unpacking whole blocks, six TMEM W buffers, a 4-stage ring), 256-row tiles,
+ragged M, N and K, every group size and both dtypes.  Every element of Y is compared with
+the oracle's fp64 product (|Y - Yd| <= 1e-3 * sum_k |A W| + 1 ulp)."""
+import pytest
+import torch
+
+import synth_inputs as si
+import weight_only_int4_tma_gb300 as w4
+from gpu_util import assert_parity_full, repack_case, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+FP16, BF16 = 0, 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weight_only_int4_tma_gb300 import build
+    build.build()
+    assert w4.w4a16_get_device_status() == 0
+
+
+CASES = [
+    # (M, N, K, group, dtype, tile_m, split_k)
+    (64, 1024, 2048, 128, FP16, 64, 1),
+    (70, 520, 1152, 64, BF16, 64, 1),
+    (64, 1024, 4096, 32, FP16, 64, 2),
+    (128, 1024, 2048, 128, FP16, 128, 1),
+    (200, 776, 1664, 64, BF16, 128, 1),
+    (128, 1024, 4096, 128, FP16, 128, 2),
+    (256, 2048, 2048, 32, BF16, 128, 1),
+    (256, 1024, 2048, 128, FP16, 256, 1),
+    (300, 520, 1152, 64, BF16, 256, 1),
+]
+
+
+@pytest.mark.parametrize("M,N,K,group,dtype,tile_m,split_k", CASES,
+                         ids=[f"M{c[0]}_N{c[1]}_K{c[2]}_g{c[3]}_{'bf16' if c[4] else 'fp16'}"
+                              f"_t{c[5]}_s{c[6]}" for c in CASES])
+def test_large_tile_instance(M, N, K, group, dtype, tile_m, split_k):
+    c = si.make_case(M, N, K, group, dtype, seed=M + N + K + group, asym=(group != 32))
+    plan = w4.w4a16_gemm_plan(M, N, K, group, dtype, kernel=w4.W4A16_KERNEL_TC,
+                              tile_m=tile_m, split_k=split_k)
+    assert plan["tile_m"] == tile_m and plan["split_k"] == split_k
+    Y = run_gemm(c, repack_case(c), kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m, split_k=split_k)
+    assert_parity_full(c, Y)
+
+
+@pytest.mark.parametrize("stages", [2, 4])
+def test_128_row_tile_ring_depths(stages):
+    """A ring of 2 stages gives two warpgroups sharing every block, 4 gives four
+    whole-block warpgroups (each reads its own ring slot); both agree with the oracle."""
+    c = si.make_case(128, 512, 4096, 128, FP16, seed=stages)
+    Y = run_gemm(c, repack_case(c), kernel=w4.W4A16_KERNEL_TC, tile_m=128, split_k=1,
+                 stages=stages)
+    assert_parity_full(c, Y)
+
+
+def test_128_row_tile_rejects_a_ring_that_does_not_fit():
+    """A ring depth above what fits in shared memory is refused on the host; nothing
+    runs."""
+    with pytest.raises(w4.W4A16Error) as e:
+        w4.w4a16_gemm_plan(128, 512, 4096, 128, FP16, kernel=w4.W4A16_KERNEL_TC, tile_m=128,
+                           split_k=1, stages=6)
+    assert e.value.status == w4.W4A16_ERR_UNSUPPORTED

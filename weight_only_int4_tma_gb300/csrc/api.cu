@@ -166,7 +166,27 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     const int recv = split > 1 ? split * bm * ceil_div(kTileN, split) * 4 : 0;
     const int smem_budget = (occ == 2 ? 113 * 1024 : ctx.max_smem_optin) - recv;
     const int max_st = tc_max_stages(bm, M, group, ctx.max_smem_optin - recv);
-    const int mult = tc_stage_multiple(bm);
+    const int stage_b = static_cast<int>(tc_stage_bytes(bm, M, group));
+    // Decode tiles: each dequant warpgroup unpacks whole 128-K blocks.  Larger tiles: a
+    // whole-block group owns ring slots of its own (the ring depth is a multiple of the
+    // group count), so it pays only where the ring is deep enough for that: 128-row tiles
+    // alone on an SM with one K slice take four whole-block groups on a 4-stage ring
+    // (measured M = 256, N = K = 8192: 34.4 against 36.7 us with both groups sharing
+    // every block); with split-K the receive area leaves two stages, one slot per group,
+    // no group can prefetch, and sharing every block is faster (M = 64: 18.3 against
+    // 20.4 us, M = 128: 30.9 against 36.5 us), as it is for 256-row tiles.
+    plan->whole_blocks = bm <= 32;
+    plan->nwg = 2;
+    if (bm == 128 && occ == 1 && split == 1) {
+        int s4 = cfg && cfg->stages ? cfg->stages : tc_max_stages(bm, M, group, smem_budget);
+        if (s4 > 8 && !(cfg && cfg->stages)) s4 = 8;
+        if (!(cfg && cfg->stages)) s4 -= s4 % 4;
+        if (s4 >= 4 && s4 % 4 == 0 && s4 <= max_st) {
+            plan->whole_blocks = true;
+            plan->nwg = 4;
+        }
+    }
+    const int mult = tc_stage_multiple(bm, plan->whole_blocks, plan->nwg);
     if (stages == 0) {
         stages = tc_max_stages(bm, M, group, smem_budget);
         if (stages > 8) stages = 8;
@@ -174,7 +194,6 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     }
     // With split-K a rank first writes its own partials of every slice to the start of
     // the ring (then pushes them to the owners), so the ring must hold recv bytes.
-    const int stage_b = static_cast<int>(tc_stage_bytes(bm, M, group));
     if (split > 1 && stages * stage_b < recv) {
         if (cfg && cfg->stages) return W4A16_ERR_UNSUPPORTED;
         while (stages * stage_b < recv && stages + mult <= max_st) stages += mult;

@@ -87,19 +87,26 @@ struct TcArgs {
     EpilogueArgs epi;     // bias / activation / residual applied to the fp32 result
 };
 
-template <int BM>
+template <int BM, bool kIL>
 struct TcShape {
     // MMA-issuing threads (one per warp).  A 128-row K=16 tcgen05.mma costs its issuing
     // thread tens of cycles whatever N is, so narrow decode tiles (N = 16 or 32) split
     // the blocks over two issuers, even blocks into accumulator 0, odd into 1.
     static constexpr int kNMI = BM <= 32 ? 2 : 1;
     static constexpr int kDq0 = 1 + kNMI;                  // first dequant warp
-    // Decode tiles: each dequant warpgroup unpacks whole blocks (wg, wg + NWG, ...).
-    // Larger tiles: every warpgroup takes its chunks of every block, so that each block
-    // is ready sooner for the longer MMAs.
-    static constexpr bool kInterleave = BM <= 32;
-    static constexpr int kTBuf = BM >= 128 ? 2 : 3;        // TMEM W buffers
+    // kIL: each dequant warpgroup unpacks whole 128-K blocks (wg, wg + NWG, ...), so that
+    // a block costs one warpgroup's per-block overhead (barrier waits, group constants)
+    // and the groups' TMEM-store drains overlap; each group then owns a subset of the
+    // ring slots.  Otherwise every warpgroup takes its chunks of every block (larger
+    // tiles whose ring is too shallow to give each group slots of its own).
+    static constexpr bool kInterleave = kIL;
+    static constexpr int kKps = BM <= 32 ? 2 : 1;          // 128-K blocks per ring stage
     static constexpr int kACol0 = BM < 64 ? 64 : BM;       // first W staging column
+    // TMEM W buffers: whole-block groups get as many as the CTA's TMEM share holds (256
+    // columns when two CTAs share an SM, i.e. tiles of up to 64 rows; 512 columns for
+    // 128-row tiles alone on an SM)
+    static constexpr int kTBuf = kIL ? (BM <= 64 ? 3 : (512 - kACol0) / 64)
+                                     : (BM >= 128 ? 2 : 3);
     static constexpr int kColsUsed = kACol0 + kTBuf * 64;
     static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64
                                    : kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
@@ -271,15 +278,16 @@ __device__ __forceinline__ void unpack_part_of(int wg, int gshift, const uint8_t
 // table of the values 0..15 instead of exponent injection (same results); kDqInt feeds
 // the MMA the exact integers q - z and scales each block's fp32 partial (16-row tiles,
 // groups of 128; the weights are not rounded to the activation dtype).
-template <int BM, int NWG, int DT, int kDq = kDqMagic>
-__global__ void __launch_bounds__(32 * (1 + TcShape<BM>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
+template <int BM, int NWG, int DT, int kDq = kDqMagic, bool kIL = (BM <= 32)>
+__global__ void __launch_bounds__(32 * (1 + TcShape<BM, kIL>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
-    using S = TcShape<BM>;
+    using S = TcShape<BM, kIL>;
     constexpr int kTBuf = S::kTBuf;
     constexpr uint32_t kEpiThreads = 128 * NWG;
     constexpr int kNMI = S::kNMI;
     static_assert(S::kACol0 >= kNMI * BM, "accumulators overlap the W staging columns");
-    static_assert(kNMI * kTBuf <= 8 && NWG * kTBuf <= 16, "control block barrier slots");
+    static_assert(kNMI * kTBuf <= 8 && NWG * kTBuf <= 24, "control block barrier slots");
+    static_assert(!S::kInterleave || NWG % S::kKps == 0, "whole-block groups: NWG % blocks per stage");
     constexpr bool kLut = kDq == kDqLut;
     constexpr bool kInt = kDq == kDqInt;
     static_assert(kDq == kDqMagic || S::kInterleave, "the alternatives exist for decode tiles");
@@ -295,8 +303,9 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const uint32_t ctrl = base + ctrl_off;
     uint8_t* ctrl_ptr = base_ptr + ctrl_off;
     // control block: full[16] (weights of a stage) empty[16] tfull[issuer][W buffer] (8)
-    // tempty[warpgroup][W buffer] (16) accum recv, scalars, then afull[16] (A of a stage)
-    const uint32_t full0 = ctrl, empty0 = ctrl + 128, tfull0 = ctrl + 256, tempty0 = ctrl + 320;
+    // at 256, accum / recv barriers and scalars at 448, kInt's dfull at 496,
+    // tempty[warpgroup][W buffer] (24) at 528, afull[16] (A of a stage) at 768
+    const uint32_t full0 = ctrl, empty0 = ctrl + 128, tfull0 = ctrl + 256, tempty0 = ctrl + 528;
     // Decode tiles give the A part of a stage its own barrier, so the weights can be
     // unpacked into TMEM before the previous kernel has finished (programmatic dependent
     // launch); larger tiles track both parts of a stage on full[].
@@ -586,15 +595,16 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         // every phase of the ring slots it reads (the host keeps the ring depth a
         // multiple of NWG / blocks-per-stage when groups take whole blocks).
         constexpr int kBStep = S::kInterleave ? NWG : 1;         // block stride of a group
-        // Decode tiles hold two blocks per ring stage, so warpgroup wg reads block wg % 2 of
-        // stages wg / 2, wg / 2 + NWG / 2, ... (the host keeps the ring depth a multiple
-        // of NWG / 2) and uses W buffers wg, wg + NWG, ... mod kTBuf.
-        static_assert(!S::kInterleave || NWG % 2 == 0, "decode tiles: an even group count");
+        // With whole blocks per group and kKps blocks per ring stage, warpgroup wg reads
+        // block wg % kKps of stages wg / kKps, wg / kKps + NWG / kKps, ... (the host keeps
+        // the ring depth a multiple of NWG / kKps) and uses W buffers wg, wg + NWG, ...
+        // mod kTBuf.
+        constexpr int kSStep = S::kInterleave ? NWG / S::kKps : 1;  // ring slots per block step
         const int tw = S::kInterleave ? wg : 0;                  // tempty party
-        int s = S::kInterleave ? wg / 2 : 0;  // ring slot of block i, and the parity
-        uint32_t ph = 0;                      // of that use of the slot
-        int b = S::kInterleave ? wg % 2 : 0;  // block i's place in its stage
-        int t = S::kInterleave ? wg % kTBuf : 0;  // its W buffer
+        int s = S::kInterleave ? wg / S::kKps : 0;  // ring slot of block i, and the parity
+        uint32_t ph = 0;                            // of that use of the slot
+        int b = S::kInterleave ? wg % S::kKps : 0;  // block i's place in its stage
+        int t = S::kInterleave ? wg % kTBuf : 0;    // its W buffer
         uint32_t epar = 0;      // bit t: parity of this warp's next wait on tempty[tw][t]
         // kInt: this thread's running sum over its group's blocks (row r, BM columns), the
         // scale of the block unpacked last, and that block's place in the group's order
@@ -650,7 +660,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 ++jn;
             }
             if constexpr (S::kInterleave) {
-                s += NWG / 2;
+                s += kSStep;
                 if (s >= args.stages) { s -= args.stages; ph ^= 1u; }
                 t += NWG % kTBuf;
                 if (t >= kTBuf) t -= kTBuf;
@@ -729,8 +739,27 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 const uint16_t* rp = args.epi.residual;
                 float* T = reinterpret_cast<float*>(base_ptr) + (warp - S::kDq0) * 512;  // [16][32]
                 const int n0w = n_tile * kTileN + q * 32;  // first channel of this warp
+                // The residual of the next 16-row group is loaded while this group is
+                // computed and stored, so that its latency is not paid once per group.
+                // Groups hold disjoint rows, and a thread reads an element of the residual
+                // only before it writes that element of Y, so Y may be the residual itself.
+                auto load_res8 = [&](int e, uint4 (&rv)[2]) {
+#pragma unroll
+                    for (int p = 0; p < 2; ++p) {
+                        const int m = m_tile * BM + e * 16 + p * 8 + (lane >> 2);
+                        const int nn = n0w + (lane & 3) * 8;
+                        rv[p] = (m < args.M && nn < args.N)
+                                    ? *reinterpret_cast<const uint4*>(
+                                          rp + static_cast<size_t>(m) * args.N + nn)
+                                    : make_uint4(0u, 0u, 0u, 0u);
+                    }
+                };
+                uint4 rnext[2] = {make_uint4(0u, 0u, 0u, 0u), make_uint4(0u, 0u, 0u, 0u)};
+                if (rp && wg < BM / 16) load_res8(wg, rnext);
 #pragma unroll 1
                 for (int e = wg; e < BM / 16; e += NWG) {
+                    const uint4 rcur[2] = {rnext[0], rnext[1]};
+                    if (rp && e + NWG < BM / 16) load_res8(e + NWG, rnext);
                     uint32_t v[16];
                     load_d(e, v);  // warp-collective: every lane, padded rows included
 #pragma unroll
@@ -752,7 +781,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                             float f[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
                             const size_t o = static_cast<size_t>(m) * args.N + nn;
                             if (rp) {
-                                const uint4 rv = *reinterpret_cast<const uint4*>(rp + o);
+                                const uint4 rv = rcur[p];
                                 const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
 #pragma unroll
                                 for (int h = 0; h < 8; ++h)
@@ -920,7 +949,7 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BM, int NWG, int DT, int DQ = kDqMagic>
+template <int BM, int NWG, int DT, int DQ = kDqMagic, bool IL = (BM <= 32)>
 int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                        int K, int group, void* Y, const GemmPlan& plan,
                        const EpilogueArgs& epi, cudaStream_t stream) {
@@ -1015,7 +1044,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
 
     const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;
     if (smem > static_cast<size_t>(ctx.max_smem_optin)) return -2;
-    auto kern = w4a16_tc_kernel<BM, NWG, DT, DQ>;
+    auto kern = w4a16_tc_kernel<BM, NWG, DT, DQ, IL>;
     {   // raise the dynamic shared-memory limit once per device (not a stream operation,
         // but kept out of the steady state so that launches can be graph-captured cheaply)
         static std::mutex mu;
@@ -1033,7 +1062,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.split_k), static_cast<unsigned>(tiles_n(N)),
                        static_cast<unsigned>((M + BM - 1) / BM));
-    cfg.blockDim = dim3(32 * TcShape<BM>::kDq0 + 128 * NWG, 1, 1);
+    cfg.blockDim = dim3(32 * TcShape<BM, IL>::kDq0 + 128 * NWG, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -1072,9 +1101,8 @@ uint32_t tc_stage_bytes(int tile_m, int M, int group) {
     return (raw + 1023u) & ~1023u;
 }
 
-int tc_stage_multiple(int tile_m) {
-    if (tile_m > 32) return 1;  // every warpgroup reads every stage
-    const int nwg = W4A16_SMALL_TILE_WG;
+int tc_stage_multiple(int tile_m, bool whole_blocks, int nwg) {
+    if (!whole_blocks) return 1;  // every warpgroup reads every stage
     const int kps = tc_blocks_per_stage(tile_m);
     return nwg > kps ? nwg / kps : 1;
 }
@@ -1118,6 +1146,12 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
                           : launch_tc_instance<16, 2, 1, kDqInt>(ctx, A, packed, M, N, K, group,
                                                                 Y, plan, epi, stream);
     }
+#define W4G_TC_IL(BMV, NWGV)                                                               \
+    return dtype == 0 ? launch_tc_instance<BMV, NWGV, 0, kDqMagic, true>(                   \
+                            ctx, A, packed, M, N, K, group, Y, plan, epi, stream)           \
+                      : launch_tc_instance<BMV, NWGV, 1, kDqMagic, true>(                   \
+                            ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
+    if (plan.whole_blocks && plan.tile_m == 128 && plan.nwg == 4) { W4G_TC_IL(128, 4) }
     switch (plan.tile_m) {
         W4G_TC_CASE(16, W4A16_SMALL_TILE_WG)
         W4G_TC_CASE(32, W4A16_SMALL_TILE_WG)
@@ -1128,6 +1162,7 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
             return -2;
     }
 #undef W4G_TC_CASE
+#undef W4G_TC_IL
 }
 
 }  // namespace w4g

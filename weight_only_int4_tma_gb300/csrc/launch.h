@@ -29,6 +29,8 @@ struct GemmPlan {
                             // 16-entry table, 2 integer operand + fp32 group rescale
     int l2_ahead;           // tensor-core kernel: CTA c < l2_ahead prefetches the weight
                             // slices of CTAs c + l2_ahead, c + 2 l2_ahead, ... into L2
+    bool whole_blocks;      // tensor-core kernel: each dequant warpgroup unpacks whole blocks
+    int nwg;                // tensor-core kernel: dequant warpgroups
 };
 
 // Launchers return a w4a16_status code.
@@ -55,9 +57,10 @@ int tc_a_rows(int tile_m, int M);
 int tc_blocks_per_stage(int tile_m);
 // Bytes of one stage of the tcgen05 ring for a tile of `tile_m` activation rows.
 uint32_t tc_stage_bytes(int tile_m, int M, int group);
-// The ring depth must be a multiple of this (each dequant warpgroup then reads a fixed
-// subset of the ring slots and passes every phase of their barriers).
-int tc_stage_multiple(int tile_m);
+// The ring depth must be a multiple of this (with whole blocks per warpgroup, each
+// dequant warpgroup then reads a fixed subset of the ring slots and passes every phase of
+// their barriers).
+int tc_stage_multiple(int tile_m, bool whole_blocks, int nwg);
 // Largest ring depth that fits `smem_budget` bytes of dynamic shared memory.
 int tc_max_stages(int tile_m, int M, int group, int smem_budget);
 
