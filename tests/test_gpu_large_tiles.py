@@ -68,3 +68,30 @@ def test_128_row_tile_rejects_a_ring_that_does_not_fit():
         w4.w4a16_gemm_plan(128, 512, 4096, 128, FP16, kernel=w4.W4A16_KERNEL_TC, tile_m=128,
                            split_k=1, stages=6)
     assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("act,with_res", [(w4.W4A16_ACT_SILU, True), (w4.W4A16_ACT_SILU, False),
+                                          (w4.W4A16_ACT_NONE, True), (w4.W4A16_ACT_RELU, True)])
+@pytest.mark.parametrize("tile_m", [128, 256])
+def test_large_tile_fused_epilogue(tile_m, act, with_res):
+    """Larger tiles with a fused activation and / or residual take four warpgroups (the
+    staged 16-byte store path, the next group's residual loaded ahead); every element
+    against the oracle's fused epilogue, including an in-place residual (Y aliases it)."""
+    import numpy as np
+    import oracle
+    from gpu_util import to_dev, to_host_u16
+    c = si.make_case(300, 520, 1152, 64, FP16, seed=tile_m + act)
+    packed = repack_case(c)
+    rng = np.random.default_rng(act + tile_m)
+    bias = oracle.encode(rng.normal(size=c.N), c.dtype)
+    res = oracle.encode(rng.normal(size=(c.M, c.N)), c.dtype) if with_res else None
+    Y = to_dev(res) if with_res else torch.empty((c.M, c.N), dtype=torch.int16, device="cuda")
+    w4.w4a16_gemm_epilogue(to_dev(c.A), packed, c.M, c.N, c.K, c.group, c.dtype, to_dev(bias),
+                           Y if with_res else None, act, Y, kernel=w4.W4A16_KERNEL_TC,
+                           tile_m=tile_m, split_k=1)
+    assert w4.w4a16_get_device_status() == 0
+    wd = oracle.dequant(c.qweight, c.scales, c.qzeros, c.N, c.K, c.group, c.dtype)
+    yd, bb, _ = oracle.gemm(c.A, wd, c.M, c.N, c.K, c.dtype)
+    out, bo, _ = oracle.epilogue(yd, bb, bias, res, act, c.M, c.N, c.dtype)
+    bad, first, worst = oracle.check(to_host_u16(Y), out, bo, c.dtype)
+    assert bad == 0, (bad, first, worst)

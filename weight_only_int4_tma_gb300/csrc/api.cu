@@ -68,8 +68,10 @@ int check_shape(int N, int K, int group, int dtype) {
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Kernel / tiling choice for a GEMM.
+// heavy_epilogue: an activation or a residual is fused into the store (more epilogue
+// work per output element, done by the dequant warps).
 int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
-              const w4a16_gemm_config* cfg, GemmPlan* plan) {
+              const w4a16_gemm_config* cfg, GemmPlan* plan, bool heavy_epilogue = false) {
     int kernel = cfg ? cfg->kernel : W4A16_KERNEL_AUTO;
     // Single-row decode of a small matrix (N*K up to 26 Mi weights, at most one 128-channel
     // tile per SM): the CUDA-core GEMV beats the tensor-core kernel there (no split-K
@@ -177,6 +179,13 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     // 20.4 us, M = 128: 30.9 against 36.5 us), as it is for 256-row tiles.
     plan->whole_blocks = bm <= 32;
     plan->nwg = 2;
+    // Shared-block tiles: four warpgroups (16 dequant warps) hide more latency where one
+    // CTA holds an SM: 128-row tiles (transition M = 128, N = K = 8192: 28.7-30.9 against
+    // 30.8-32.1 us), and 256-row tiles whose epilogue applies an activation or a residual
+    // (prefill M = 4096 with bias + SiLU: 311.9 against 338.0 us); for the plain 256-row
+    // store two groups stay faster (273.0 against 280.2 us).  Four groups at two CTAs per
+    // SM would exceed the register file.
+    if ((bm == 128 && occ == 1) || (bm == 256 && heavy_epilogue)) plan->nwg = 4;
     if (bm == 128 && occ == 1 && split == 1) {
         int s4 = cfg && cfg->stages ? cfg->stages : tc_max_stages(bm, M, group, smem_budget);
         if (s4 > 8 && !(cfg && cfg->stages)) s4 = 8;
@@ -268,7 +277,8 @@ int gemm_common(const void* A, const void* packed, int M, int N, int K, int grou
     const DeviceCtx* ctx = nullptr;
     if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
     GemmPlan plan{};
-    if ((rc = make_plan(*ctx, M, N, K, group, cfg, &plan)) != W4A16_OK) return rc;
+    const bool heavy = epi.act != kActNone || epi.residual != nullptr;
+    if ((rc = make_plan(*ctx, M, N, K, group, cfg, &plan, heavy)) != W4A16_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (plan.kernel == W4A16_KERNEL_SIMT)
         return launch_simt_gemm(*ctx, A, packed, M, N, K, group, dtype, Y, plan, epi, s);

@@ -58,9 +58,6 @@ namespace {
 constexpr int kMaxStages = 16;
 constexpr int kCtrlBytes = 1024;
 
-#ifndef W4A16_BIG_TILE_WG
-#define W4A16_BIG_TILE_WG 2    // dequant warpgroups for 256-row tiles
-#endif
 #ifndef W4A16_SMALL_TILE_WG
 #define W4A16_SMALL_TILE_WG 2  // dequant warpgroups for 16- and 32-row tiles
 #endif
@@ -1152,12 +1149,20 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
                       : launch_tc_instance<BMV, NWGV, 1, kDqMagic, true>(                   \
                             ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
     if (plan.whole_blocks && plan.tile_m == 128 && plan.nwg == 4) { W4G_TC_IL(128, 4) }
+    if (plan.nwg == 4) {  // shared-block tiles with four warpgroups
+        switch (plan.tile_m) {
+            W4G_TC_CASE(128, 4)
+            W4G_TC_CASE(256, 4)
+            default:
+                return -2;
+        }
+    }
     switch (plan.tile_m) {
         W4G_TC_CASE(16, W4A16_SMALL_TILE_WG)
         W4G_TC_CASE(32, W4A16_SMALL_TILE_WG)
         W4G_TC_CASE(64, 2)
         W4G_TC_CASE(128, 2)
-        W4G_TC_CASE(256, W4A16_BIG_TILE_WG)
+        W4G_TC_CASE(256, 2)
         default:
             return -2;
     }
