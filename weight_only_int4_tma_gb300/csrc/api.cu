@@ -43,8 +43,6 @@ int get_ctx(const DeviceCtx** out) {
             if (v > 0) ms = static_cast<uint64_t>(v);
         }
         c.timeout_ns = ms * 1000000ull;
-        c.l2_prefetch = false;
-        if (const char* e = std::getenv("W4A16_L2_PREFETCH")) c.l2_prefetch = e[0] == '1';
         g_ctx[dev] = c;
         g_ctx_ready[dev] = true;
     }
@@ -212,11 +210,6 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     plan->tile_m = bm;
     plan->split_k = split;
     plan->stages = stages;
-    // A launch that fits in one wave leaves (slots - CTAs) slots free for its first CTAs
-    // while the previous kernel still runs; the rest start as that kernel's CTAs exit.
-    const int ctas = split * base;
-    const int slots = ctx.num_sms * occ;
-    plan->l2_ahead = (ctx.l2_prefetch && plan->prefetch_weights && ctas < slots) ? slots - ctas : 0;
     return W4A16_OK;
 }
 

@@ -80,7 +80,6 @@ struct TcArgs {
     uint32_t stage_bytes;
     uint32_t recv_off;    // offset of the split-K receive area from the ring base
     uint64_t timeout_ns;
-    int l2_ahead;         // CTA c < l2_ahead prefetches the weights of CTAs c + l2_ahead, ...
     EpilogueArgs epi;     // bias / activation / residual applied to the fp32 result
 };
 
@@ -379,23 +378,6 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             if (flags < 0 && split == 0 && n_tile == 0 && m_tile == 0)
                 record_status(args.status, kStatusFormat);
             prefetch_tensormap(&tmap_a);
-            // The CTAs that start first (in the slots the previous kernel left free) pull
-            // the weight slices of the CTAs that can only start once that kernel's CTAs
-            // exit into L2, so that those find their first bytes in L2 and the weights
-            // stream while the previous kernel finishes (its tail leaves HBM idle).
-            const int nlin = args.splits * static_cast<int>(gridDim.y);  // one m tile's CTAs
-            const int c = split + args.splits * (n_tile + static_cast<int>(gridDim.y) * m_tile);
-            if (flags >= 0 && args.l2_ahead > 0 && c < args.l2_ahead) {
-                const uint32_t bbl = hl.block_bytes;
-                for (int c2 = c + args.l2_ahead; c2 < nlin; c2 += args.l2_ahead) {
-                    const int s2 = c2 % args.splits, t2 = c2 / args.splits;
-                    const int kb2 = s2 * kb_per + (s2 < kb_rem ? s2 : kb_rem);
-                    const int nk2 = kb_per + (s2 < kb_rem ? 1 : 0);
-                    bulk_prefetch_l2(args.packed + kHeaderBytes +
-                                         (static_cast<size_t>(t2) * args.kblocks + kb2) * bbl,
-                                     static_cast<uint32_t>(nk2) * bbl);
-                }
-            }
         }
     }
     if (warp == 1) {
@@ -1036,7 +1018,6 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     if (plan.split_k > 1 && recv_bytes > ring) return -2;
     args.recv_off = ring;
     args.timeout_ns = ctx.timeout_ns;
-    args.l2_ahead = plan.l2_ahead;
     args.epi = epi;
 
     const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;

@@ -15,7 +15,6 @@ struct DeviceCtx {
     int max_smem_optin;     // bytes of dynamic shared memory a CTA may opt into
     int* status;            // device address of this device's status word
     uint64_t timeout_ns;    // limit of every bounded in-kernel wait
-    bool l2_prefetch;       // early CTAs prefetch late CTAs' weights into L2
 };
 
 struct GemmPlan {
@@ -27,8 +26,6 @@ struct GemmPlan {
     bool prefetch_weights;  // read the packed blob before the dependency wait
     int dequant;            // tensor-core decode tiles: 0 exponent injection, 1 the
                             // 16-entry table, 2 integer operand + fp32 group rescale
-    int l2_ahead;           // tensor-core kernel: CTA c < l2_ahead prefetches the weight
-                            // slices of CTAs c + l2_ahead, c + 2 l2_ahead, ... into L2
     bool whole_blocks;      // tensor-core kernel: each dequant warpgroup unpacks whole blocks
     int nwg;                // tensor-core kernel: dequant warpgroups
 };

@@ -223,12 +223,6 @@ __device__ __forceinline__ void tma_tensor_3d_g2s(uint32_t dst, const CUtensorMa
         : "memory");
 }
 
-// Bulk prefetch of a contiguous global range into L2 (a hint: no completion to track;
-// 16-byte aligned address, size a multiple of 16).
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
