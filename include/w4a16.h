@@ -256,6 +256,24 @@ int w4a16_get_device_status(void* stream);
  */
 int w4a16_debug_timeout_probe(unsigned int timeout_us, void* stream);
 
+/*
+ * Failure-path check of the split-K exchange (library infrastructure, no passage of the
+ * pages describes it): runs the tensor-core GEMM with 16-row tiles and the launch
+ * choice's split-K on these arguments (as w4a16_gemm_ex with kernel TC, tile_m 16), except
+ * that cluster rank 0 of every tile pushes none of its fp32 partials.  The other ranks'
+ * waits for those partials are bounded by `timeout_us` microseconds (1..1000000; every
+ * other wait of the launch too): they run out, the kernel records W4A16_ERR_DEVICE_TIMEOUT,
+ * every rank still leaves only after its peers have stopped pushing into it, and the GPU
+ * context stays usable.  Y (device, dtype [M][N], 16-byte aligned) is written only where
+ * a rank received all partials; treat its contents as undefined.  A, packed, M (1..16), N,
+ * K, group and dtype as for w4a16_gemm.  Returns UNSUPPORTED if the shape gives no split
+ * (K too short or N large enough to fill the GPU without it).  Follow with
+ * w4a16_get_device_status().
+ */
+int w4a16_debug_splitk_timeout_probe(const void* A, const void* packed, int M, int N, int K,
+                                     int group, int dtype, void* Y, unsigned int timeout_us,
+                                     void* stream);
+
 #ifdef __cplusplus
 }
 #endif

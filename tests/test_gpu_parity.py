@@ -38,6 +38,24 @@ def test_timeout_probe_reports_and_context_survives():
     assert int(x.sum().item()) == 45
 
 
+def test_splitk_timeout_probe_reports_and_context_survives():
+    """Split-K exchange failure path: cluster rank 0 of every tile pushes none of its
+    partials, so the other ranks' bounded waits for them run out (20 ms).  The kernel
+    reports the timeout, every rank leaves only after its peers stopped pushing into it,
+    and the context stays usable: the same GEMM right after is correct."""
+    c = si.make_case(4, 1024, 4096, 128, FP16, seed=3)
+    packed = repack_case(c)
+    plan = w4.w4a16_gemm_plan(c.M, c.N, c.K, c.group, c.dtype, kernel=w4.W4A16_KERNEL_TC,
+                              tile_m=16)
+    assert plan["split_k"] >= 2
+    Y = torch.zeros((c.M, c.N), dtype=torch.int16, device="cuda")
+    w4.w4a16_debug_splitk_timeout_probe(to_dev(c.A), packed, c.M, c.N, c.K, c.group, c.dtype,
+                                        Y, 20000)
+    assert w4.w4a16_get_device_status() == w4.W4A16_ERR_DEVICE_TIMEOUT
+    assert w4.w4a16_get_device_status() == 0  # cleared by the read
+    assert_parity_full(c, run_gemm(c, packed))
+
+
 # ---- repack + debug dequant: bit-exact ----------------------------------------------
 
 @pytest.mark.parametrize("dtype", [FP16, BF16])

@@ -89,6 +89,8 @@ def lib() -> ctypes.CDLL:
             L.w4a16_get_device_status.restype = I
             L.w4a16_debug_timeout_probe.argtypes = [U, P]
             L.w4a16_debug_timeout_probe.restype = I
+            L.w4a16_debug_splitk_timeout_probe.argtypes = [P, P, I, I, I, I, I, P, U, P]
+            L.w4a16_debug_splitk_timeout_probe.restype = I
             _lib = L
     return _lib
 
@@ -196,6 +198,13 @@ def w4a16_get_device_status(stream=None) -> int:
 def w4a16_debug_timeout_probe(timeout_us: int, stream=None) -> None:
     _check(lib().w4a16_debug_timeout_probe(timeout_us, _stream(stream)),
            "w4a16_debug_timeout_probe")
+
+
+def w4a16_debug_splitk_timeout_probe(A, packed, M: int, N: int, K: int, group: int,
+                                     dtype: int, Y, timeout_us: int, stream=None) -> None:
+    _check(lib().w4a16_debug_splitk_timeout_probe(_ptr(A), _ptr(packed), M, N, K, group, dtype,
+                                                  _ptr(Y), timeout_us, _stream(stream)),
+           "w4a16_debug_splitk_timeout_probe")
 
 
 # ---- torch-friendly helpers (allocation + the calls above) ---------------------------

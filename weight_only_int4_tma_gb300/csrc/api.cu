@@ -349,6 +349,28 @@ int w4a16_get_device_status(void* stream) {
     return v;
 }
 
+int w4a16_debug_splitk_timeout_probe(const void* A, const void* packed, int M, int N, int K,
+                                     int group, int dtype, void* Y, unsigned int timeout_us,
+                                     void* stream) {
+    if (timeout_us < 1 || timeout_us > 1000000) return W4A16_ERR_INVALID_ARG;
+    if (M < 1 || M > 16) return W4A16_ERR_INVALID_ARG;
+    int rc = check_shape(N, K, group, dtype);
+    if (rc != W4A16_OK) return rc;
+    if (!A || !packed || !Y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(Y, 16) || !aligned(packed, 16)) return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
+    w4a16_gemm_config cfg{};
+    cfg.kernel = W4A16_KERNEL_TC;
+    cfg.tile_m = 16;
+    GemmPlan plan{};
+    if ((rc = make_plan(*ctx, M, N, K, group, &cfg, &plan)) != W4A16_OK) return rc;
+    if (plan.split_k < 2) return W4A16_ERR_UNSUPPORTED;
+    return launch_tc_splitk_probe(*ctx, A, packed, M, N, K, group, dtype, Y, plan,
+                                  static_cast<uint64_t>(timeout_us) * 1000ull,
+                                  static_cast<cudaStream_t>(stream));
+}
+
 int w4a16_debug_timeout_probe(unsigned int timeout_us, void* stream) {
     if (timeout_us < 1 || timeout_us > 1000000) return W4A16_ERR_INVALID_ARG;
     const DeviceCtx* ctx = nullptr;

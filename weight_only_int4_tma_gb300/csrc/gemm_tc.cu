@@ -274,7 +274,10 @@ __device__ __forceinline__ void unpack_part_of(int wg, int gshift, const uint8_t
 // table of the values 0..15 instead of exponent injection (same results); kDqInt feeds
 // the MMA the exact integers q - z and scales each block's fp32 partial (16-row tiles,
 // groups of 128; the weights are not rounded to the activation dtype).
-template <int BM, int NWG, int DT, int kDq = kDqMagic, bool kIL = (BM <= 32)>
+// kNoPushProbe: a failure-path check only (w4a16_debug_splitk_timeout_probe): cluster rank
+// 0 pushes none of its partials, so the other ranks' bounded waits for them run out.
+template <int BM, int NWG, int DT, int kDq = kDqMagic, bool kIL = (BM <= 32),
+          bool kNoPushProbe = false>
 __global__ void __launch_bounds__(32 * (1 + TcShape<BM, kIL>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     using S = TcShape<BM, kIL>;
@@ -836,7 +839,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             const uint32_t rank = cluster_ctarank();
             if (warp == S::kDq0) {  // lane p sends the slice of rank p
                 const int p = lane;
-                if (p < args.splits && p != static_cast<int>(rank)) {
+                if (p < args.splits && p != static_cast<int>(rank) &&
+                    !(kNoPushProbe && rank == 0)) {
                     const uint32_t src = base + static_cast<uint32_t>(p) * slice_bytes;
                     const uint32_t dst =
                         map_to_rank(base + args.recv_off + rank * slice_bytes, p);
@@ -928,10 +932,11 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-template <int BM, int NWG, int DT, int DQ = kDqMagic, bool IL = (BM <= 32)>
+template <int BM, int NWG, int DT, int DQ = kDqMagic, bool IL = (BM <= 32), bool PROBE = false>
 int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,
                        int K, int group, void* Y, const GemmPlan& plan,
-                       const EpilogueArgs& epi, cudaStream_t stream) {
+                       const EpilogueArgs& epi, cudaStream_t stream,
+                       uint64_t timeout_ns = 0) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return -3;
     const int a_rows = tc_a_rows(BM, M);
@@ -1017,12 +1022,12 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     // they are pushed; the receive area for the peers' partials follows the ring.
     if (plan.split_k > 1 && recv_bytes > ring) return -2;
     args.recv_off = ring;
-    args.timeout_ns = ctx.timeout_ns;
+    args.timeout_ns = timeout_ns ? timeout_ns : ctx.timeout_ns;
     args.epi = epi;
 
     const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;
     if (smem > static_cast<size_t>(ctx.max_smem_optin)) return -2;
-    auto kern = w4a16_tc_kernel<BM, NWG, DT, DQ, IL>;
+    auto kern = w4a16_tc_kernel<BM, NWG, DT, DQ, IL, PROBE>;
     {   // raise the dynamic shared-memory limit once per device (not a stream operation,
         // but kept out of the steady state so that launches can be graph-captured cheaply)
         static std::mutex mu;
@@ -1149,6 +1154,18 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
     }
 #undef W4G_TC_CASE
 #undef W4G_TC_IL
+}
+
+int launch_tc_splitk_probe(const DeviceCtx& ctx, const void* A, const void* packed, int M,
+                           int N, int K, int group, int dtype, void* Y, const GemmPlan& plan,
+                           uint64_t timeout_ns, cudaStream_t stream) {
+    if (plan.tile_m != 16 || plan.split_k < 2) return -2;
+    const EpilogueArgs none{nullptr, nullptr, kActNone};
+    return dtype == 0
+               ? launch_tc_instance<16, W4A16_SMALL_TILE_WG, 0, kDqMagic, true, true>(
+                     ctx, A, packed, M, N, K, group, Y, plan, none, stream, timeout_ns)
+               : launch_tc_instance<16, W4A16_SMALL_TILE_WG, 1, kDqMagic, true, true>(
+                     ctx, A, packed, M, N, K, group, Y, plan, none, stream, timeout_ns);
 }
 
 }  // namespace w4g

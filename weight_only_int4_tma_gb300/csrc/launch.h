@@ -48,6 +48,13 @@ int launch_simt_gemm(const DeviceCtx& ctx, const void* A, const void* packed, in
 
 int launch_timeout_probe(const DeviceCtx& ctx, uint64_t limit_ns, cudaStream_t stream);
 
+// The tensor-core kernel (16-row tiles, split-K) with cluster rank 0 pushing none of its
+// partials, every bounded wait limited to timeout_ns: a failure-path check of the split-K
+// exchange.
+int launch_tc_splitk_probe(const DeviceCtx& ctx, const void* A, const void* packed, int M,
+                           int N, int K, int group, int dtype, void* Y, const GemmPlan& plan,
+                           uint64_t timeout_ns, cudaStream_t stream);
+
 // Rows of A staged per 64-K chunk (8 or 16 for decode tiles, else the tile height).
 int tc_a_rows(int tile_m, int M);
 // 128-K weight blocks per ring stage (one bulk copy each stage).
