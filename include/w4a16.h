@@ -104,10 +104,12 @@ typedef struct w4a16_gemm_config {
                          cluster.  SIMT: 0 or 1                                          */
     int tile_m;       /* TC: 0 = heuristic; else 16, 32, 64, 128 or 256 rows of A per
                          tile.  SIMT: 0, 16 or 32 output channels per work unit          */
-    int stages;       /* TC: 0 = heuristic; else shared-memory ring depth (2..16).
+    int stages;       /* TC: 0 = heuristic; else depth of the shared-memory ring of A
+                         tiles (2..16); the weight ring beside it is sized by the library.
                          SIMT: must be 0 (fixed 4-stage cp.async ring)                   */
     int flags;        /* W4A16_GEMM_* bits; 0 = defaults                                 */
-    int reserved[3];  /* must be zero                                                   */
+    int reserved[3];  /* must be zero (w4a16_gemm_plan's output: reserved[0] = the weight
+                         ring depth of a TC plan, 0 for SIMT)                            */
 } w4a16_gemm_config;
 
 /* Library ABI version (W4A16_ABI_VERSION). */
@@ -217,7 +219,8 @@ int w4a16_gemm_epilogue(const void* A, const void* packed, int M, int N, int K, 
 /*
  * The kernel and tiling that w4a16_gemm_ex(..., cfg, ...) would launch for this shape on
  * the current device (cfg may be NULL = AUTO), written to *out with every field resolved
- * (kernel TC or SIMT; split_k, tile_m, stages as used; flags as applied).  Host-side
+ * (kernel TC or SIMT; split_k, tile_m, stages as used; flags as applied; reserved[0] =
+ * the weight ring depth of a TC plan).  Host-side
  * only: launches nothing, reads no device memory.  Errors: INVALID_ARG (M < 1, out NULL,
  * bad cfg fields), UNSUPPORTED, CUDA (no usable device).
  */

@@ -2,15 +2,17 @@
 
 The kernel's warps wait on mbarriers with parity waits, which only distinguish the
 current phase from the one before it.  This discrete-event model replays the kernel's
-protocol (producer, MMA issuers, dequant warpgroups, asynchronous copy and MMA
-completions with random latencies; one issuer's MMAs complete in order, the two
+protocol (weight producer, A producer, MMA issuers, dequant warpgroups, asynchronous copy
+and MMA completions with random latencies; one issuer's MMAs complete in order, the two
 issuers' independently) and flags any wait whose intended phase is not the barrier's
 current or immediately preceding phase, and any deadlock.
 
-Layout modelled (as in csrc/gemm_tc.cu): ring slots full[s] / empty[s]; W buffers t
-with tfull[issuer][t] (count: the warps that write the tile) and
-tempty[warpgroup][t] (one MMA commit).  Decode tiles: warpgroup w unpacks blocks
-w, w + NWG, ...; larger tiles: every warpgroup unpacks every block.
+Layout modelled (as in csrc/gemm_tc.cu): a weight ring wfull[s] / wempty[s] (a slot is
+released by the warps that read it, once they have read it) and an A ring afull[s] /
+aempty[s] (released by the MMA commits of its stage), each with its own producer and its
+own depth; W buffers t with tfull[issuer][t] (count: the warps that write the tile) and
+tempty[warpgroup][t] (one MMA commit).  Whole-block tiles: warpgroup w unpacks blocks
+w, w + NWG, ...; shared-block tiles: every warpgroup unpacks every block.
 
 Events carry their own times (the heap key), and every callback is given that time, so
 the random latencies really reorder the agents; the earlier shared layout (one tfull and
@@ -38,24 +40,38 @@ class Bar:
             self.pending = self.count
 
 
-def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
+def simulate(kNMI, NWG, T, kps, SW, SA, nkb, rng, interleave, per_party=True,
+             w_readers=None, one_producer=None):
+    """w_readers: arrivals that release a weight slot (default: the kernel's count, one
+    per warp that reads the slot's blocks).  one_producer: one agent streams both rings
+    (the kernel's choice for two blocks per stage, i.e. decode tiles), always issuing the
+    copy whose slot is released first."""
+    if one_producer is None:
+        one_producer = kps == 2
     nst = (nkb + kps - 1) // kps
-    full = [Bar(1) for _ in range(S)]
-    empty = [Bar(2 if (kNMI == 2 and kps == 2) else 1) for _ in range(S)]
+    wfull = [Bar(1) for _ in range(SW)]
+    if w_readers is None:
+        w_readers = (4 if interleave else 4 * NWG) * kps
+    wempty = [Bar(w_readers) for _ in range(SW)]
+    afull = [Bar(1) for _ in range(SA)]
+    aempty = [Bar(2 if (kNMI == 2 and kps == 2) else 1) for _ in range(SA)]
     n_tparty = kNMI if per_party else 1
     n_eparty = (NWG if interleave else 1) if per_party else 1
     tfull = [[Bar(4 if interleave else 4 * NWG) for _ in range(T)] for _ in range(n_tparty)]
     tempty = [[Bar(1) for _ in range(T)] for _ in range(n_eparty)]
     events, cnt, errors = [], itertools.count(), []
+    # readers of each slot right now: a copy into a slot while someone reads it is a race
+    reading = {"w": [0] * SW, "a": [0] * SA}
 
     def at(t, f):
         heapq.heappush(events, (t, next(cnt), f))
 
-    def producer():
+    def producer(ring, depth, full, empty, lo, hi):
         for p in range(nst):
-            if p >= S:
-                yield ("wait", empty[p % S], p // S - 1)
-            yield ("async", rng.uniform(0.2, 3.0), full[p % S])
+            if p >= depth:
+                yield ("wait", empty[p % depth], p // depth - 1)
+            yield ("write", ring, p % depth)
+            yield ("async", rng.uniform(lo, hi), full[p % depth])
 
     mma_free = [0.0] * kNMI  # MMAs of one issuer complete in order; issuers independently
 
@@ -65,7 +81,7 @@ def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
         for i in range(k, nkb, kNMI):
             p = i // kps
             if p != last_p:
-                yield ("wait", full[p % S], p // S)
+                yield ("wait", afull[p % SA], p // SA)
                 last_p = p
             t = i % T
             party = k if per_party else 0
@@ -82,7 +98,7 @@ def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
         for i in blocks:
             p = i // kps
             if p != last_p:
-                yield ("wait", full[p % S], p // S)
+                yield ("wait", wfull[p % SW], p // SW)
                 last_p = p
             t = i % T
             if i >= T:
@@ -90,10 +106,38 @@ def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
                 q = seen[t] if per_party else i // T - 1
                 yield ("wait", tempty[party][t], q)
                 seen[t] += 1
+            yield ("read", "w", p % SW, +1)
             yield ("delay", rng.uniform(0.05, 0.8))
+            yield ("read", "w", p % SW, -1)
+            yield ("arrive", wempty[p % SW])  # the block's weights are read
             yield ("arrive", tfull[(i % kNMI) if per_party else 0][t])
 
-    agents = [producer()] + [issuer(k) for k in range(kNMI)]
+    def both():
+        wi = ai = 0
+        while wi < nst and wi < SW:  # the weight stages that need no slot back
+            yield ("write", "w", wi % SW)
+            yield ("async", rng.uniform(0.2, 3.0), wfull[wi % SW])
+            wi += 1
+        while wi < nst or ai < nst:
+            if wi < nst and (ai >= nst or wi - SW <= ai - SA):
+                if wi >= SW:
+                    yield ("wait", wempty[wi % SW], wi // SW - 1)
+                yield ("write", "w", wi % SW)
+                yield ("async", rng.uniform(0.2, 3.0), wfull[wi % SW])
+                wi += 1
+            else:
+                if ai >= SA:
+                    yield ("wait", aempty[ai % SA], ai // SA - 1)
+                yield ("write", "a", ai % SA)
+                yield ("async", rng.uniform(0.1, 1.5), afull[ai % SA])
+                ai += 1
+
+    if one_producer:
+        agents = [both()]
+    else:
+        agents = [producer("w", SW, wfull, wempty, 0.2, 3.0),
+                  producer("a", SA, afull, aempty, 0.1, 1.5)]
+    agents += [issuer(k) for k in range(kNMI)]
     agents += [warp(w) for w in range(NWG) for _ in range(4)]
     waiting, finished = {}, set()
 
@@ -129,6 +173,15 @@ def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
                 act[1].arrive()
                 wake(now)
                 continue
+            if kind == "read":
+                reading[act[1]][act[2]] += act[3]
+                continue
+            if kind == "write":
+                if reading[act[1]][act[2]]:
+                    errors.append(f"race: {act[1]} slot {act[2]} refilled while being read")
+                    finished.add(ai)
+                    return
+                continue
             if kind == "async":
                 bar = act[2]
                 at(now + act[1], lambda n, bar=bar: (bar.arrive(), wake(n)))
@@ -137,12 +190,14 @@ def simulate(kNMI, NWG, T, kps, S, nkb, rng, interleave, per_party=True):
                 k, i, p, release = act[1], act[2], act[3], act[4]
                 fin = max(now, mma_free[k]) + rng.uniform(0.05, 0.8)
                 mma_free[k] = fin
+                reading["a"][p % SA] += 1  # the MMA reads its A stage until it completes
 
                 def done(n, i=i, p=p, release=release):
+                    reading["a"][p % SA] -= 1
                     party = ((i + T) % NWG if interleave else 0) if per_party else 0
                     tempty[party][i % T].arrive()
                     if release:
-                        empty[p % S].arrive()
+                        aempty[p % SA].arrive()
                     wake(n)
                 at(fin, done)
                 continue
@@ -165,22 +220,26 @@ def configs(interleave):
     for kNMI, kps in ((2, 2), (1, 1), (1, 2)):
         for T in (2, 3, 6):
             for NWG in (1, 2, 4):
-                for S in (2, 3, 4, 5, 6, 8):
-                    # host rule: with whole blocks per group, the ring depth is a multiple
-                    # of groups per stage
-                    if interleave and NWG > kps and S % (NWG // kps):
+                if interleave and NWG % kps:  # the kernel's static rule for whole blocks
+                    continue
+                for SW in (2, 3, 4, 5, 6, 8):
+                    # host rule: with whole blocks per group, the weight ring depth is a
+                    # multiple of groups per stage
+                    if interleave and NWG > kps and SW % (NWG // kps):
                         continue
-                    for nkb in (1, 2, 3, 5, 7, 11, 16):
-                        yield kNMI, NWG, T, kps, S, nkb
+                    for SA in (2, 3, 5):
+                        for nkb in (1, 2, 3, 5, 7, 11, 16):
+                            yield kNMI, NWG, T, kps, SW, SA, nkb
 
 
+@pytest.mark.parametrize("one_producer", [False, True], ids=["two_producers", "one_producer"])
 @pytest.mark.parametrize("interleave", [True, False], ids=["whole_blocks", "all_chunks"])
-def test_per_party_barriers_never_alias_or_deadlock(interleave):
+def test_per_party_barriers_never_alias_or_deadlock(interleave, one_producer):
     bad = []
     for cfg in configs(interleave):
-        for trial in range(4):
-            rng = random.Random(hash((cfg, trial, interleave)))
-            e = simulate(*cfg, rng, interleave)
+        for trial in range(2):
+            rng = random.Random(hash((cfg, trial, interleave, one_producer)))
+            e = simulate(*cfg, rng, interleave, one_producer=one_producer)
             if e:
                 bad.append((cfg, e))
                 break
@@ -189,13 +248,26 @@ def test_per_party_barriers_never_alias_or_deadlock(interleave):
 
 def test_model_catches_a_ring_depth_that_breaks_the_rule():
     """Sensitivity of the model: four warpgroups taking whole blocks, one block per stage,
-    and a ring depth (3 or 2) that is not a multiple of 4: each group skips phases of
-    slots it shares with the others; the host forbids those depths, and the model must
+    and a weight ring depth (3 or 2) that is not a multiple of 4: each group skips phases
+    of slots it shares with the others; the host forbids those depths, and the model must
     flag them."""
-    for S in (3, 2):
+    for SW in (3, 2):
         hits = sum(1 for trial in range(20)
-                   if simulate(1, 4, 2, 1, S, 16, random.Random(trial), interleave=True))
-        assert hits > 0, S
+                   if simulate(1, 4, 2, 1, SW, 3, 16, random.Random(trial), interleave=True))
+        assert hits > 0, SW
+
+
+def test_model_catches_a_weight_slot_released_too_early():
+    """Sensitivity of the race check: if a weight slot were released after fewer
+    arrivals than the warps that read it (here: one warpgroup's four where every group
+    reads every block), the producer refills it while the other groups still read it; the
+    model must flag that, and must not with the kernel's count."""
+    hits = clean = 0
+    for trial in range(30):
+        e = simulate(1, 2, 3, 1, 4, 3, 16, random.Random(trial), False, w_readers=4)
+        hits += e is not None and e.startswith("race")
+        clean += simulate(1, 2, 3, 1, 4, 3, 16, random.Random(trial), False) is not None
+    assert hits > 0 and clean == 0, (hits, clean)
 
 
 def test_model_reproduces_the_shared_layout_failure():
@@ -213,9 +285,9 @@ def test_model_reproduces_the_shared_layout_failure():
     shared = per_party = 0
     for S in (2, 4, 6):
         for trial in range(40):
-            e = simulate(2, 2, 3, 2, S, 16, random.Random(trial), True, per_party=False)
+            e = simulate(2, 2, 3, 2, S, S, 16, random.Random(trial), True, per_party=False)
             shared += e is not None and e.startswith("parity alias")
-            per_party += simulate(2, 2, 3, 2, S, 16, random.Random(trial), True) is not None
+            per_party += simulate(2, 2, 3, 2, S, S, 16, random.Random(trial), True) is not None
     assert shared > 20, shared
     assert per_party == 0, per_party
 

@@ -1,7 +1,8 @@
 """GPU parity of the tensor-core kernel's larger tiles, one test per tile instance the
 launch choice can take: 64- and 128-row tiles whose two warpgroups share every block
 (with and without split-K), 128-row tiles alone on an SM with one K slice (four
-warpgroups unpacking whole blocks, six TMEM W buffers, a 4-stage ring), 256-row tiles,
+warpgroups unpacking whole blocks, six TMEM W buffers, each group owning every fourth
+slot of the weight ring), 256-row tiles,
 ragged M, N and K, every group size and both dtypes.  Every element of Y is compared with
 the oracle's fp64 product (|Y - Yd| <= 1e-3 * sum_k |A W| + 1 ulp)."""
 import pytest
@@ -51,13 +52,33 @@ def test_large_tile_instance(M, N, K, group, dtype, tile_m, split_k):
     assert_parity_full(c, Y)
 
 
-@pytest.mark.parametrize("stages", [2, 4])
+@pytest.mark.parametrize("stages", [2, 3, 4])
 def test_128_row_tile_ring_depths(stages):
-    """A ring of 2 stages gives two warpgroups sharing every block, 4 gives four
-    whole-block warpgroups (each reads its own ring slot); both agree with the oracle."""
-    c = si.make_case(128, 512, 4096, 128, FP16, seed=stages)
+    """Four whole-block warpgroups with A rings of 2, 3 and 4 stages beside a weight ring
+    whose depth is a multiple of 4 (each group reads every fourth weight slot); K = 8192
+    makes both rings wrap many times at depths that differ from each other."""
+    p = w4.w4a16_gemm_plan(128, 256, 8192, 128, FP16, kernel=w4.W4A16_KERNEL_TC, tile_m=128,
+                           split_k=1, stages=stages)
+    assert p["stages"] == stages and p["w_stages"] % 4 == 0 and p["w_stages"] >= 4
+    c = si.make_case(128, 256, 8192, 128, FP16, seed=stages)
     Y = run_gemm(c, repack_case(c), kernel=w4.W4A16_KERNEL_TC, tile_m=128, split_k=1,
                  stages=stages)
+    assert_parity_full(c, Y)
+
+
+@pytest.mark.parametrize("tile_m,split_k,stages", [(64, 1, 2), (64, 2, 3), (128, 2, 2),
+                                                   (256, 1, 2), (256, 1, 3), (32, 1, 2)])
+def test_rings_of_different_depths_wrap(tile_m, split_k, stages):
+    """The A ring (depth `stages`) and the weight ring (depth chosen by the library) are
+    independent: long K so that both wrap many times, with and without split-K, against
+    every element of the oracle's product."""
+    M = min(tile_m, 100) if tile_m > 32 else 24
+    p = w4.w4a16_gemm_plan(M, 256, 8192, 64, BF16, kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m,
+                           split_k=split_k, stages=stages)
+    assert p["stages"] == stages and p["w_stages"] >= 2
+    c = si.make_case(M, 256, 8192, 64, BF16, seed=tile_m + stages, asym=True)
+    Y = run_gemm(c, repack_case(c), kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m,
+                 split_k=split_k, stages=stages)
     assert_parity_full(c, Y)
 
 
@@ -66,7 +87,7 @@ def test_128_row_tile_rejects_a_ring_that_does_not_fit():
     runs."""
     with pytest.raises(w4.W4A16Error) as e:
         w4.w4a16_gemm_plan(128, 512, 4096, 128, FP16, kernel=w4.W4A16_KERNEL_TC, tile_m=128,
-                           split_k=1, stages=6)
+                           split_k=1, stages=7)
     assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
 
 

@@ -128,8 +128,8 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     const int m_tiles = ceil_div(M, bm);
     if (m_tiles > 65535) return W4A16_ERR_UNSUPPORTED;
     const int base = n_tiles * m_tiles;
-    // CTAs per SM the ring is sized for: decode tiles always pair up; 128-row tiles pair
-    // up (2-stage rings) when there are enough tiles to fill two per SM.
+    // CTAs per SM the rings are sized for: decode tiles always pair up; 128-row tiles pair
+    // up (shallower rings) when there are enough tiles to fill two per SM.
     const int occ = bm <= 64 ? 2 : (bm == 128 && base >= 2 * ctx.num_sms ? 2 : 1);
 
     int split = cfg && cfg->split_k ? cfg->split_k : 0;
@@ -153,28 +153,19 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
         if (split > 8) split = 8;
         if (split > kblocks) split = kblocks;
         if (split < 1) split = 1;
-        // the split-K receive area must leave room for a ring of at least two stages
-        while (split > 1 &&
-               tc_max_stages(bm, M, group, ctx.max_smem_optin -
-                             split * bm * ceil_div(kTileN, split) * 4) < 2)
-            --split;
+        // the split-K receive area must leave room for rings of at least two stages each
+        const size_t lim = occ == 2 ? 113 * 1024 : static_cast<size_t>(ctx.max_smem_optin);
+        while (split > 1 && tc_layout(bm, M, group, split, 2, 2).smem > lim) --split;
     }
     if (split < 1 || split > 8 || split > kblocks) return W4A16_ERR_UNSUPPORTED;
 
-    int stages = cfg && cfg->stages ? cfg->stages : 0;
-    // split-K receive area (fp32 partials of the other cluster ranks), outside the ring
-    const int recv = split > 1 ? split * bm * ceil_div(kTileN, split) * 4 : 0;
-    const int smem_budget = (occ == 2 ? 113 * 1024 : ctx.max_smem_optin) - recv;
-    const int max_st = tc_max_stages(bm, M, group, ctx.max_smem_optin - recv);
-    const int stage_b = static_cast<int>(tc_stage_bytes(bm, M, group));
-    // Decode tiles: each dequant warpgroup unpacks whole 128-K blocks.  Larger tiles: a
-    // whole-block group owns ring slots of its own (the ring depth is a multiple of the
-    // group count), so it pays only where the ring is deep enough for that: 128-row tiles
-    // alone on an SM with one K slice take four whole-block groups on a 4-stage ring
-    // (measured M = 256, N = K = 8192: 34.4 against 36.7 us with both groups sharing
-    // every block); with split-K the receive area leaves two stages, one slot per group,
-    // no group can prefetch, and sharing every block is faster (M = 64: 18.3 against
-    // 20.4 us, M = 128: 30.9 against 36.5 us), as it is for 256-row tiles.
+    // Decode tiles: each dequant warpgroup unpacks whole 128-K blocks.  128-row tiles
+    // alone on an SM with one K slice: four whole-block groups, each owning every fourth
+    // weight slot (measured M = 256, N = K = 8192: 34.4 against 36.7 us with the groups
+    // sharing every block, on a ring that held weights and A together).  Otherwise every
+    // warpgroup takes its chunks of every block (with split-K the receive area leaves too
+    // little room for group-owned slots: M = 64: 18.3 against 20.4 us, M = 128: 30.9
+    // against 36.5 us, same rings).
     plan->whole_blocks = bm <= 32;
     plan->nwg = 2;
     // Shared-block tiles: four warpgroups (16 dequant warps) hide more latency where one
@@ -184,32 +175,46 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     // store two groups stay faster (273.0 against 280.2 us).  Four groups at two CTAs per
     // SM would exceed the register file.
     if ((bm == 128 && occ == 1) || (bm == 256 && heavy_epilogue)) plan->nwg = 4;
-    if (bm == 128 && occ == 1 && split == 1) {
-        int s4 = cfg && cfg->stages ? cfg->stages : tc_max_stages(bm, M, group, smem_budget);
-        if (s4 > 8 && !(cfg && cfg->stages)) s4 = 8;
-        if (!(cfg && cfg->stages)) s4 -= s4 % 4;
-        if (s4 >= 4 && s4 % 4 == 0 && s4 <= max_st) {
-            plan->whole_blocks = true;
-            plan->nwg = 4;
-        }
-    }
+    if (bm == 128 && occ == 1 && split == 1) plan->whole_blocks = true;
     const int mult = tc_stage_multiple(bm, plan->whole_blocks, plan->nwg);
-    if (stages == 0) {
-        stages = tc_max_stages(bm, M, group, smem_budget);
-        if (stages > 8) stages = 8;
-        stages -= stages % mult;
+
+    // Rings: A stages are freed when their MMAs complete, weight stages as soon as they
+    // are unpacked (into TMEM), so the weight ring needs only a few slots per reading
+    // group.  Decode tiles favour weight stages (the HBM stream; their A tiles are small
+    // and stay in L2), larger tiles A stages (up to 4; they feed the MMAs).
+    const size_t limit = occ == 2 ? 113 * 1024 : static_cast<size_t>(ctx.max_smem_optin);
+    auto fits = [&](int a, int w) { return tc_layout(bm, M, group, split, a, w).smem <= limit; };
+    const int sw_min = mult > 2 ? mult : 2;
+    const int sw_max = 2 * mult > 4 ? 2 * mult : 4;
+    const int sa_fixed = cfg && cfg->stages ? cfg->stages : 0;
+    const int sa_max = sa_fixed ? sa_fixed : 4, sa_min = sa_fixed ? sa_fixed : 2;
+    int sa = 0, sw = 0;
+    if (bm <= 32) {
+        for (int w = sw_max; w >= sw_min && !sa; w -= mult)
+            for (int a = sa_max; a >= sa_min; --a)
+                if (fits(a, w)) { sa = a; sw = w; break; }
+    } else {
+        for (int a = sa_max; a >= sa_min && !sa; --a)
+            for (int w = sw_max; w >= sw_min; w -= mult)
+                if (fits(a, w)) { sa = a; sw = w; break; }
     }
+    if (!sa) return W4A16_ERR_UNSUPPORTED;
     // With split-K a rank first writes its own partials of every slice to the start of
-    // the ring (then pushes them to the owners), so the ring must hold recv bytes.
-    if (split > 1 && stages * stage_b < recv) {
-        if (cfg && cfg->stages) return W4A16_ERR_UNSUPPORTED;
-        while (stages * stage_b < recv && stages + mult <= max_st) stages += mult;
-    }
-    if (split > 1 && stages * stage_b < recv) return W4A16_ERR_UNSUPPORTED;
-    if (stages < 2 || stages > max_st || stages % mult != 0) return W4A16_ERR_UNSUPPORTED;
+    // the rings (then pushes them to the owners), so the rings must hold recv bytes.
+    auto rings_hold_partials = [&](int a, int w) {
+        const TcLayout L = tc_layout(bm, M, group, split, a, w);
+        return L.recv_off >= L.recv_bytes;
+    };
+    while (split > 1 && !rings_hold_partials(sa, sw) && sw + mult <= kTcMaxStages &&
+           fits(sa, sw + mult))
+        sw += mult;
+    if (sa < 2 || sa > kTcMaxStages || sw < sw_min || sw > kTcMaxStages || sw % mult != 0 ||
+        !fits(sa, sw) || !rings_hold_partials(sa, sw))
+        return W4A16_ERR_UNSUPPORTED;
     plan->tile_m = bm;
     plan->split_k = split;
-    plan->stages = stages;
+    plan->stages = sa;
+    plan->w_stages = sw;
     return W4A16_OK;
 }
 
@@ -310,6 +315,7 @@ int w4a16_gemm_plan(int M, int N, int K, int group, int dtype, const w4a16_gemm_
     r.split_k = plan.split_k;
     r.tile_m = plan.tile_m;
     r.stages = plan.stages;
+    r.reserved[0] = plan.kernel == W4A16_KERNEL_TC ? plan.w_stages : 0;
     r.flags = (plan.pdl ? 0 : W4A16_GEMM_NO_PDL) |
               (plan.prefetch_weights ? 0 : W4A16_GEMM_NO_WEIGHT_PREFETCH) |
               (plan.dequant == 1 ? W4A16_GEMM_DEQUANT_LUT : 0) |

@@ -2,9 +2,10 @@
 //
 // One CTA computes a 128-channel x BM-row tile of Y^T = W . A^T over a K slice:
 //
-//   HBM --TMA bulk copy--> SMEM ring stage: [A tile (128B swizzle) | packed 128x128 block]
+//   HBM --TMA bulk copy--> SMEM weight ring stage: packed 128x128 block(s)
 //        (weights stream once, evict-first; "量化开销对比" §6.5; "W4A16 GEMM 算子浅析"
 //         §"计算流水线的核心哲学", the HBM -> SMEM step)
+//   L2/HBM --TMA tensor copy--> SMEM A ring stage: A tile (128-byte swizzle)
 //   SMEM --dequant warps: LOP3 magic-bias unpack, sub/mul per pair--> TMEM (A operand)
 //        ("W4A16 GEMM 算子浅析" §"寄存器解包黑魔法"; the group scale is applied here, on the
 //         weight operand, as "量化开销对比" §6.2 requires)
@@ -17,23 +18,28 @@
 //        factor -> optional + bias, activation, + residual -> round to dtype -> Y
 //        ("量化开销对比" §6.2 "最后：累加器 × s_x → +bias → 写出", §6.6, §6.7 folding)
 //
-// Warp roles: warp 0 = TMA producer; warps 1..NMI = MMA issuers (two for decode tiles of
-// <= 32 rows, taking even / odd 128-K blocks into two accumulators; warp 1 also allocates
-// TMEM); then the dequant warps, 4 per warpgroup (warp w may only touch TMEM lanes
-// 32*(w%4)..+31, so each warpgroup covers all 128 lanes), which also run the epilogue.
-// The producer and issuer warps run their loops with all 32 lanes and let lane 0 issue,
-// and the warp index and TMEM base are broadcast from lane 0, so that control flow and
-// operand arithmetic are warp-uniform (uniform registers, fewer instructions per block).
-// Decode tiles: warpgroup g unpacks whole blocks g, g + NWG, ...; larger tiles: every
-// warpgroup unpacks its chunks of every block; both through unpack routines templated on
-// the group layout.  Each mbarrier has a single waiting party that passes every one of its
-// phases (tfull per issuer and W buffer, tempty per warpgroup and W buffer), because a
-// parity wait only tells the current phase from the one before it; for decode tiles the
-// A part of a ring stage has its own barrier so that weights can be unpacked before the
-// previous kernel has finished.
+// The weights and the A tiles travel in two rings with their own producers and barriers:
+// a weight slot is free again as soon as the dequant warps have read it (the unpacked
+// tile lives in TMEM from then on), an A slot once the MMAs that read it have completed.
+// So the weight stream runs ahead of the MMAs by the TMEM W buffers plus the weight ring,
+// and neither waits for the other's slots to come back.
+//
+// Warp roles: warp 0 = weight producer; warps 1..NMI = MMA issuers (two for decode tiles
+// of <= 32 rows, taking even / odd 128-K blocks into two accumulators; warp 1 also
+// allocates TMEM); warp NMI + 1 = A producer; then the dequant warps, 4 per warpgroup
+// (warp w may only touch TMEM lanes 32*(w%4)..+31, so each warpgroup covers all 128
+// lanes), which also run the epilogue.  The producer and issuer warps run their loops
+// with all 32 lanes and let lane 0 issue, and the warp index and TMEM base are broadcast
+// from lane 0, so that control flow and operand arithmetic are warp-uniform (uniform
+// registers, fewer instructions per block).  Whole-block tiles: warpgroup g unpacks whole
+// blocks g, g + NWG, ...; shared-block tiles: every warpgroup unpacks its chunks of every
+// block; both through unpack routines templated on the group layout.  Each mbarrier has a
+// single waiting party that passes every one of its phases (tfull per issuer and W buffer,
+// tempty per warpgroup and W buffer), because a parity wait only tells the current phase
+// from the one before it.
 //
 // Programmatic dependent launch: the prologue (barriers, TMEM, descriptor prefetch and,
-// unless disabled, the header check and the first ring stages of packed weights) runs
+// unless disabled, the header check), the weight stream and the unpack into TMEM run
 // while the previous kernel in the stream finishes; A is read and Y written only after
 // griddepcontrol.wait.  Every mbarrier wait is bounded; on expiry the CTA records a
 // timeout, drains what it issued and exits.
@@ -55,7 +61,6 @@ namespace w4g {
 
 namespace {
 
-constexpr int kMaxStages = 16;
 constexpr int kCtrlBytes = 1024;
 
 #ifndef W4A16_SMALL_TILE_WG
@@ -71,38 +76,48 @@ struct TcArgs {
     int M, N, K, group;
     int kblocks;          // K / 128
     int splits;           // K slices = cluster size along x
-    int stages;           // ring depth
+    int a_stages;         // depth of the A ring
+    int w_stages;         // depth of the weight ring
     int a_rows;           // rows per A chunk in shared memory (8, 16 or BM)
-    int kps;              // 128-K blocks per ring stage (1 or 2)
+    int kps;              // 128-K blocks per stage of either ring (1 or 2)
     int a_2d;             // A loaded as one 2-D box per 64-K chunk (K not a multiple of 64)
     int slice_rows;       // channels owned per cluster rank (ceil(128 / splits))
     int flags;
-    uint32_t stage_bytes;
-    uint32_t recv_off;    // offset of the split-K receive area from the ring base
+    uint32_t a_stage_bytes;
+    uint32_t w_stage_bytes;
+    uint32_t w_off;       // offset of the weight ring from the shared base (the A ring is at 0)
+    uint32_t recv_off;    // offset of the split-K receive area from the shared base
     uint64_t timeout_ns;
     EpilogueArgs epi;     // bias / activation / residual applied to the fp32 result
 };
 
-template <int BM, bool kIL>
+template <int BM, bool kIL, int NWG>
 struct TcShape {
     // MMA-issuing threads (one per warp).  A 128-row K=16 tcgen05.mma costs its issuing
     // thread tens of cycles whatever N is, so narrow decode tiles (N = 16 or 32) split
     // the blocks over two issuers, even blocks into accumulator 0, odd into 1.
     static constexpr int kNMI = BM <= 32 ? 2 : 1;
-    static constexpr int kDq0 = 1 + kNMI;                  // first dequant warp
+    static constexpr int kKps = BM <= 32 ? 2 : 1;          // 128-K blocks per ring stage
+    // Decode tiles stream both rings from warp 0 (their A tiles are small and their K
+    // slices short; an extra warp cost ~0.25 us per launch); larger tiles give the A ring
+    // a producer warp of its own, so neither stream waits for the other's slots.
+    static constexpr bool kOneProd = kKps == 2;
+    static constexpr int kAProd = kOneProd ? 0 : 1 + kNMI;  // A producer warp
+    static constexpr int kDq0 = (kOneProd ? 1 : 2) + kNMI;  // first dequant warp
     // kIL: each dequant warpgroup unpacks whole 128-K blocks (wg, wg + NWG, ...), so that
     // a block costs one warpgroup's per-block overhead (barrier waits, group constants)
     // and the groups' TMEM-store drains overlap; each group then owns a subset of the
-    // ring slots.  Otherwise every warpgroup takes its chunks of every block (larger
-    // tiles whose ring is too shallow to give each group slots of its own).
+    // weight ring's slots.  Otherwise every warpgroup takes its chunks of every block.
     static constexpr bool kInterleave = kIL;
-    static constexpr int kKps = BM <= 32 ? 2 : 1;          // 128-K blocks per ring stage
+    // warps that read each weight stage (and arrive on its empty barrier): one warpgroup
+    // per block with whole-block groups, every warpgroup otherwise
+    static constexpr int kWReaders(int nwg) { return (kIL ? 4 : 4 * nwg) * kKps; }
     static constexpr int kACol0 = BM < 64 ? 64 : BM;       // first W staging column
-    // TMEM W buffers: whole-block groups get as many as the CTA's TMEM share holds (256
-    // columns when two CTAs share an SM, i.e. tiles of up to 64 rows; 512 columns for
-    // 128-row tiles alone on an SM)
-    static constexpr int kTBuf = kIL ? (BM <= 64 ? 3 : (512 - kACol0) / 64)
-                                     : (BM >= 128 ? 2 : 3);
+    // TMEM W buffers: as many as the CTA's TMEM share holds: 256 columns when two CTAs
+    // share an SM (tiles of up to 64 rows, and 128-row tiles with two warpgroups), 512
+    // for a CTA alone on an SM (128-row tiles with four warpgroups, 256-row tiles)
+    static constexpr bool kShared = BM <= 64 || (BM == 128 && NWG == 2);
+    static constexpr int kTBuf = (kShared ? 256 - kACol0 : 512 - kACol0) / 64;
     static constexpr int kColsUsed = kACol0 + kTBuf * 64;
     static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64
                                    : kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
@@ -278,9 +293,9 @@ __device__ __forceinline__ void unpack_part_of(int wg, int gshift, const uint8_t
 // 0 pushes none of its partials, so the other ranks' bounded waits for them run out.
 template <int BM, int NWG, int DT, int kDq = kDqMagic, bool kIL = (BM <= 32),
           bool kNoPushProbe = false>
-__global__ void __launch_bounds__(32 * (1 + TcShape<BM, kIL>::kNMI) + 128 * NWG, BM <= 64 ? 2 : 1)
+__global__ void __launch_bounds__(32 * TcShape<BM, kIL, NWG>::kDq0 + 128 * NWG, BM <= 64 ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
-    using S = TcShape<BM, kIL>;
+    using S = TcShape<BM, kIL, NWG>;
     constexpr int kTBuf = S::kTBuf;
     constexpr uint32_t kEpiThreads = 128 * NWG;
     constexpr int kNMI = S::kNMI;
@@ -295,20 +310,18 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* base_ptr = smem_raw + (base - raw);
-    const uint32_t ring_bytes = static_cast<uint32_t>(args.stages) * args.stage_bytes;
-    const uint32_t ctrl_off = args.splits > 1
-        ? args.recv_off + static_cast<uint32_t>(args.splits * BM * args.slice_rows * 4)
-        : ring_bytes;
+    // shared layout: [A ring][weight ring][split-K receive area][control block]
+    const uint32_t ctrl_off = args.recv_off +
+        (args.splits > 1 ? static_cast<uint32_t>(args.splits * BM * args.slice_rows * 4) : 0u);
     const uint32_t ctrl = base + ctrl_off;
     uint8_t* ctrl_ptr = base_ptr + ctrl_off;
-    // control block: full[16] (weights of a stage) empty[16] tfull[issuer][W buffer] (8)
-    // at 256, accum / recv barriers and scalars at 448, kInt's dfull at 496,
-    // tempty[warpgroup][W buffer] (24) at 528, afull[16] (A of a stage) at 768
-    const uint32_t full0 = ctrl, empty0 = ctrl + 128, tfull0 = ctrl + 256, tempty0 = ctrl + 528;
-    // Decode tiles give the A part of a stage its own barrier, so the weights can be
-    // unpacked into TMEM before the previous kernel has finished (programmatic dependent
-    // launch); larger tiles track both parts of a stage on full[].
-    const uint32_t afull0 = S::kInterleave ? ctrl + 768 : full0;
+    const uint32_t wbase = base + args.w_off;
+    // control block: wfull[16] (a weight stage landed) at 0, wempty[16] (a weight stage
+    // read) at 128, tfull[issuer][W buffer] (8) at 256, aempty[16] (the MMAs that read an
+    // A stage completed) at 320, accum / recv barriers and scalars at 448, kInt's dfull at
+    // 496, tempty[warpgroup][W buffer] (24) at 528, afull[16] (an A stage landed) at 768
+    const uint32_t wfull0 = ctrl, wempty0 = ctrl + 128, tfull0 = ctrl + 256;
+    const uint32_t aempty0 = ctrl + 320, tempty0 = ctrl + 528, afull0 = ctrl + 768;
     uint16_t* lut = reinterpret_cast<uint16_t*>(ctrl_ptr + 960);  // 16 entries (kLut)
     // kInt: dfull[issuer][slot], the block's fp32 partial in D slot (issuer, slot) is done
     const uint32_t dfull0 = ctrl + 496;
@@ -344,11 +357,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         if (lane == 0) {
             *abort_flag = 0;
         }
-        for (int s = lane; s < args.stages; s += 32) {
-            mbar_init(full0 + 8 * s, 1);
-            if (S::kInterleave) mbar_init(afull0 + 8 * s, 1);
-            // a stage is free once every issuer that read it has committed
-            mbar_init(empty0 + 8 * s, (kNMI == 2 && args.kps == 2) ? 2 : 1);
+        for (int s = lane; s < args.w_stages; s += 32) {
+            mbar_init(wfull0 + 8 * s, 1);
+            mbar_init(wempty0 + 8 * s, S::kWReaders(NWG));  // one arrival per reading warp
+        }
+        for (int s = lane; s < args.a_stages; s += 32) {
+            mbar_init(afull0 + 8 * s, 1);
+            // an A stage is free once every issuer that read it has committed
+            mbar_init(aempty0 + 8 * s, (kNMI == 2 && args.kps == 2) ? 2 : 1);
         }
         for (int t = lane; t < kNMI * kTBuf; t += 32)  // the warps that write a block's W tile
             mbar_init(tfull0 + 8 * t, S::kInterleave ? 4 : 4 * NWG);
@@ -406,77 +422,113 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     const uint32_t a_bytes = 2u * static_cast<uint32_t>(kps) * a_chunk;  // A part of a stage
     const int nst = (nkb + kps - 1) / kps;                                // ring stages to stream
 
-    if (warp == 0) {
-        // ---------------- TMA producer ----------------
-        // The whole warp runs the loop (warp-uniform control and address arithmetic);
-        // lane 0 arms the barriers and issues the copies.
+    // Drain after an abort: the last `depth` issued stages of a ring (every earlier one
+    // was consumed, so it has landed) must land before the CTA may exit.
+    auto drain = [&](uint32_t full_bars, int depth, int issued) {
+        const int first = issued > depth ? issued - depth : 0;
+        for (int i = first; i < issued; ++i) {
+            int dummy = 0;
+            (void)mbar_wait_bounded(full_bars + 8 * (i % depth),
+                                    static_cast<uint32_t>(i / depth) & 1u, &dummy, nullptr, tlim);
+        }
+    };
+
+    if (warp == 0 || warp == S::kAProd) {
+        // ---------------- producers ----------------
+        // Warp 0 streams the weight ring, warp kAProd the A ring (the same warp for decode
+        // tiles).  The whole warp runs the loops (warp-uniform control and address
+        // arithmetic); lane 0 arms the barriers and issues the copies.  Weight stage i =
+        // blocks [i*kps, i*kps + nblk) as ONE bulk copy; A stage i = the 2*kps 64-K chunks
+        // of A of those blocks as ONE 3-D box (or one 2-D box per chunk).  The packed
+        // weights do not depend on the previous kernel (unless weight prefetch is off, in
+        // which case the header was read after the dependency wait); A is written
+        // upstream, so it is read only after the dependency wait.
         if (run) {
+            const bool do_w = warp == 0, do_a = warp == S::kAProd;
             const uint64_t pol_w = policy_evict_first();
             const uint64_t pol_a = policy_evict_last();
-            const uint8_t* src = args.packed + kHeaderBytes +
-                                 (static_cast<size_t>(n_tile) * args.kblocks + kb0) * bb;
+            const uint8_t* wsrc = args.packed + kHeaderBytes +
+                                  (static_cast<size_t>(n_tile) * args.kblocks + kb0) * bb;
             const int m0 = m_tile * BM;
-            // stage i: blocks [i*kps, i*kps + nblk) as ONE bulk copy + ONE 3-D A box
-            const int pre = prefetch_w ? (nst < args.stages ? nst : args.stages) : 0;
-            for (int i = 0; i < pre && lane == 0; ++i) {  // weights do not depend on the previous grid
-                const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
-                const int nblk = min(kps, nkb - i * kps);
-                mbar_arrive_expect_tx(full0 + 8 * i, nblk * bb + (S::kInterleave ? 0u : a_bytes));
-                tma_bulk_g2s(st + a_bytes, src + static_cast<size_t>(i) * kps * bb, nblk * bb,
-                             full0 + 8 * i, pol_w);
-            }
-            if (prefetch_w) grid_dep_wait();
-            auto load_a = [&](uint32_t st, int kchunk, uint32_t bar) {
-                if (args.a_2d) {  // chunk q of the stage at st + q * a_chunk; K tail zero-filled
+            bool ok = true;
+            // lane 0: the copies of weight / A stage i into ring slot `slot`
+            auto copy_w = [&](int i, int slot) {
+                const uint32_t fb = wfull0 + 8 * slot;
+                const int left = nkb - i * kps;
+                const uint32_t bytes = static_cast<uint32_t>(left < kps ? left : kps) * bb;
+                mbar_arrive_expect_tx(fb, bytes);
+                tma_bulk_g2s(wbase + static_cast<uint32_t>(slot) * args.w_stage_bytes,
+                             wsrc + static_cast<size_t>(i) * kps * bb, bytes, fb, pol_w);
+            };
+            auto copy_a = [&](int i, int slot) {
+                const uint32_t st = base + static_cast<uint32_t>(slot) * args.a_stage_bytes;
+                const uint32_t ab = afull0 + 8 * slot;
+                const int kchunk = (kb0 + i * kps) * 2;  // first 64-K chunk of the stage
+                mbar_arrive_expect_tx(ab, a_bytes);
+                if (args.a_2d) {  // chunk q at st + q * a_chunk; the K tail zero-filled
                     for (int q = 0; q < 2 * kps; ++q)
                         tma_tensor_2d_g2s(st + static_cast<uint32_t>(q) * a_chunk, &tmap_a,
-                                          (kchunk + q) * 64, m0, bar, pol_a);
+                                          (kchunk + q) * 64, m0, ab, pol_a);
                 } else {
-                    tma_tensor_3d_g2s(st, &tmap_a, 0, m0, kchunk, bar, pol_a);
+                    tma_tensor_3d_g2s(st, &tmap_a, 0, m0, kchunk, ab, pol_a);
                 }
             };
-            for (int i = 0; i < pre && lane == 0; ++i) {
-                const uint32_t st = base + static_cast<uint32_t>(i) * args.stage_bytes;
-                if (S::kInterleave) mbar_arrive_expect_tx(afull0 + 8 * i, a_bytes);
-                load_a(st, (kb0 + i * kps) * 2, afull0 + 8 * i);
+            // warp-wide: wait for the slot (after its first use), then lane 0 copies
+            int wi = 0, ws = 0;  // next weight stage, its slot and the parity of that use
+            uint32_t wph = 0;
+            auto issue_w = [&]() {
+                if (wi >= args.w_stages)
+                    ok = ok && mbar_wait_warp(wempty0 + 8 * ws, wph ^ 1u, abort_flag,
+                                              args.status, tlim);
+                if (!ok) return;
+                if (lane == 0) copy_w(wi, ws);
+                ++wi;
+                if (++ws == args.w_stages) { ws = 0; wph ^= 1u; }
+            };
+            int ai = 0, as = 0;  // the same for the A ring
+            uint32_t aph = 0;
+            auto issue_a = [&]() {
+                if (ai >= args.a_stages)
+                    ok = ok && mbar_wait_warp(aempty0 + 8 * as, aph ^ 1u, abort_flag,
+                                              args.status, tlim);
+                if (!ok) return;
+                if (lane == 0) copy_a(ai, as);
+                ++ai;
+                if (++as == args.a_stages) { as = 0; aph ^= 1u; }
+            };
+            // Lane 0 first issues the weight stages that need no slot back and, after the
+            // dependency wait, the A stages that need none, in straight loops (0.1 us per
+            // decode launch faster than issuing them warp-wide).  Then the warp always
+            // takes the copy whose slot is released first: weight stage wi waits for the
+            // unpack of stage wi - w_stages, A stage ai for the MMAs of stage ai -
+            // a_stages; a stage's unpack precedes its MMAs, so the lower stage index (the
+            // weight stage on a tie) goes first.  With one warp for both rings every wait
+            // is then for a stage whose own copies were issued earlier: no wait can block
+            // a copy that it depends on.
+            const int nw = do_w ? nst : 0, na = do_a ? nst : 0;  // stages this warp streams
+            const int pw = nw < args.w_stages ? nw : args.w_stages;
+            const int pa = na < args.a_stages ? na : args.a_stages;
+            if (lane == 0)
+                for (int i = 0; i < pw; ++i) copy_w(i, i);
+            if (do_a) {
+                grid_dep_wait();
+                if (lane == 0)
+                    for (int i = 0; i < pa; ++i) copy_a(i, i);
             }
-            int issued = pre;
-            int s = pre;              // ring slot of stage i, and the parity of its use
-            uint32_t ph = 0;
-            if (s == args.stages) { s = 0; ph = 1; }
-            const uint8_t* wsrc = src + static_cast<size_t>(pre) * kps * bb;
-            int kchunk = (kb0 + pre * kps) * 2;  // first 64-K chunk of A for stage i
-            int left = nkb - pre * kps;          // blocks not yet issued
-            for (int i = pre; i < nst; ++i) {
-                if (i >= args.stages &&
-                    !mbar_wait_warp(empty0 + 8 * s, ph ^ 1u, abort_flag, args.status, tlim))
-                    break;
-                const uint32_t st = base + static_cast<uint32_t>(s) * args.stage_bytes;
-                const uint32_t fb = full0 + 8 * s, ab = afull0 + 8 * s;
-                const int nblk = left < kps ? left : kps;
-                if (lane == 0) {
-                    mbar_arrive_expect_tx(fb, nblk * bb + (S::kInterleave ? 0u : a_bytes));
-                    tma_bulk_g2s(st + a_bytes, wsrc, nblk * bb, fb, pol_w);
-                    if (S::kInterleave) mbar_arrive_expect_tx(ab, a_bytes);
-                    load_a(st, kchunk, ab);
-                }
-                ++issued;
-                left -= kps;
-                wsrc += static_cast<size_t>(kps) * bb;
-                kchunk += 2 * kps;
-                if (++s == args.stages) { s = 0; ph ^= 1u; }
+            __syncwarp();
+            wi = ws = pw;
+            if (ws == args.w_stages) { ws = 0; wph = 1u; }
+            ai = as = pa;
+            if (as == args.a_stages) { as = 0; aph = 1u; }
+            while (ok && (wi < nw || ai < na)) {
+                if (wi < nw && (ai >= na || wi - args.w_stages <= ai - args.a_stages))
+                    issue_w();
+                else
+                    issue_a();
             }
-            if (lane == 0 && (issued < nst || *abort_flag)) {
-                // Drain: every issued copy must land before the CTA may exit.
-                const int first = issued > args.stages ? issued - args.stages : 0;
-                for (int i = first; i < issued; ++i) {
-                    const int s = i % args.stages;
-                    const uint32_t ph = static_cast<uint32_t>(i / args.stages) & 1u;
-                    int dummy = 0;
-                    (void)mbar_wait_bounded(full0 + 8 * s, ph, &dummy, nullptr, tlim);
-                    if (S::kInterleave)
-                        (void)mbar_wait_bounded(afull0 + 8 * s, ph, &dummy, nullptr, tlim);
-                }
+            if (lane == 0 && (!ok || *abort_flag)) {
+                if (do_w) drain(wfull0, args.w_stages, wi);
+                if (do_a) drain(afull0, args.a_stages, ai);
             }
         }
         __syncwarp();
@@ -502,8 +554,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             uint32_t ph = 0;
             uint32_t fpar = 0;  // bit t: parity of this issuer's next wait on tfull[k][t]
             for (int i = k; i < nkb; i += kNMI) {   // i: 128-K block
-                // the weights of block i are known to have landed through tfull (its
-                // dequant waited for them); this wait is for the stage's A
+                // the A stage of block i (its weights are in TMEM once tfull completes)
                 ok = (kNMI == 1 && b != 0) ||
                      mbar_wait_spin_warp(afull0 + 8 * s, ph, abort_flag, args.status, tlim);
                 ok = ok && mbar_wait_spin_warp(tfull0 + 8 * (k * kTBuf + t), (fpar >> t) & 1u,
@@ -511,7 +562,7 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 fpar ^= 1u << t;
                 if (!ok) break;
                 tc_fence_after();
-                const uint64_t d0 = sw128_desc(base + static_cast<uint32_t>(s) * args.stage_bytes) +
+                const uint64_t d0 = sw128_desc(base + static_cast<uint32_t>(s) * args.a_stage_bytes) +
                                     static_cast<uint64_t>(2 * b) * chunk16;
                 const uint64_t d1 = d0 + chunk16;
                 const uint32_t a0 = tmem + S::kACol0 + t * 64;
@@ -534,13 +585,13 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     tc_mma_ts(dd, a0 + 56, d1 + 6, idesc, 1u);
                     tc_commit(te);
                     if (kInt) tc_commit(dfull0 + dslot / 2);  // 8 bytes per (k, slot)
-                    if (stage_done) tc_commit(empty0 + 8 * s);
+                    if (stage_done) tc_commit(aempty0 + 8 * s);
                 }
                 __syncwarp();
                 t += kNMI;
                 if (t >= kTBuf) t -= kTBuf;
                 if (kNMI == 1) b = stage_done ? 0 : b + 1;
-                if (stage_done && ++s == args.stages) { s = 0; ph ^= 1u; }
+                if (stage_done && ++s == args.a_stages) { s = 0; ph ^= 1u; }
             }
             if (lane == 0) {
                 tc_commit(accum_bar);
@@ -574,16 +625,16 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         // phases: issuer k waits on tfull[k][t] (its own blocks in W buffer t), warpgroup
         // w on tempty[w][t] (the MMA of the block before its own next use of buffer t;
         // one shared party when all groups unpack every block), and each warpgroup passes
-        // every phase of the ring slots it reads (the host keeps the ring depth a
-        // multiple of NWG / blocks-per-stage when groups take whole blocks).
+        // every phase of the weight ring slots it reads (the host keeps the weight ring
+        // depth a multiple of NWG / blocks-per-stage when groups take whole blocks).
         constexpr int kBStep = S::kInterleave ? NWG : 1;         // block stride of a group
         // With whole blocks per group and kKps blocks per ring stage, warpgroup wg reads
-        // block wg % kKps of stages wg / kKps, wg / kKps + NWG / kKps, ... (the host keeps
-        // the ring depth a multiple of NWG / kKps) and uses W buffers wg, wg + NWG, ...
-        // mod kTBuf.
+        // block wg % kKps of weight stages wg / kKps, wg / kKps + NWG / kKps, ... (the host
+        // keeps the weight ring depth a multiple of NWG / kKps) and uses W buffers wg,
+        // wg + NWG, ... mod kTBuf.
         constexpr int kSStep = S::kInterleave ? NWG / S::kKps : 1;  // ring slots per block step
         const int tw = S::kInterleave ? wg : 0;                  // tempty party
-        int s = S::kInterleave ? wg / S::kKps : 0;  // ring slot of block i, and the parity
+        int s = S::kInterleave ? wg / S::kKps : 0;  // weight slot of block i, and the parity
         uint32_t ph = 0;                            // of that use of the slot
         int b = S::kInterleave ? wg % S::kKps : 0;  // block i's place in its stage
         int t = S::kInterleave ? wg % kTBuf : 0;    // its W buffer
@@ -612,14 +663,15 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
         };
         for (int i = S::kInterleave ? wg : 0; i < nkb && ok; i += kBStep) {   // 128-K block
             if (S::kInterleave || b == 0)  // (s, b, t) advance at the loop end
-                ok = mbar_wait_warp(full0 + 8 * s, ph, abort_flag, args.status, tlim);
+                ok = mbar_wait_warp(wfull0 + 8 * s, ph, abort_flag, args.status, tlim);
             if (ok && i >= kTBuf) {
                 ok = mbar_wait_warp(tempty0 + 8 * (tw * kTBuf + t), (epar >> t) & 1u, abort_flag,
                                     args.status, tlim);
                 epar ^= 1u << t;
             }
             if (!ok) break;
-            const uint8_t* wb = base_ptr + a_bytes + static_cast<size_t>(s) * args.stage_bytes +
+            const uint8_t* wb = base_ptr + args.w_off +
+                                static_cast<size_t>(s) * args.w_stage_bytes +
                                 static_cast<size_t>(b) * bb;
             float s_cur = 0.0f;  // kInt: the block's scale for row r
             if constexpr (S::kInterleave) {  // whole block by this warpgroup
@@ -632,6 +684,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 unpack_part_of<DT, NWG>(wg, gshift, wb, r, zoff, has_z,
                                         tmem + lane_base + S::kACol0 + t * 64);
             }
+            // every lane's shared-memory reads of the block are done (their values are in
+            // the TMEM stores): the weight slot may be refilled
+            __syncwarp();
+            if (lane == 0) mbar_arrive(wempty0 + 8 * s);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -643,14 +699,14 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             }
             if constexpr (S::kInterleave) {
                 s += kSStep;
-                if (s >= args.stages) { s -= args.stages; ph ^= 1u; }
+                if (s >= args.w_stages) { s -= args.w_stages; ph ^= 1u; }
                 t += NWG % kTBuf;
                 if (t >= kTBuf) t -= kTBuf;
             } else {
                 if (++t == kTBuf) t = 0;
                 if (++b == args.kps) {
                     b = 0;
-                    if (++s == args.stages) { s = 0; ph ^= 1u; }
+                    if (++s == args.w_stages) { s = 0; ph ^= 1u; }
                 }
             }
         }
@@ -1008,24 +1064,26 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     args.group = group;
     args.kblocks = blocks_k(K);
     args.splits = plan.split_k;
-    args.stages = plan.stages;
+    args.a_stages = plan.stages;
+    args.w_stages = plan.w_stages;
     args.a_rows = a_rows;
     args.kps = kps;
     args.a_2d = a_2d ? 1 : 0;
     args.slice_rows = (kTileN + plan.split_k - 1) / plan.split_k;
     args.flags = plan.prefetch_weights ? kFlagPrefetchW : 0;
-    args.stage_bytes = tc_stage_bytes(BM, M, group);
-    const uint32_t ring = static_cast<uint32_t>(plan.stages) * args.stage_bytes;
-    const uint32_t recv_bytes = plan.split_k > 1
-        ? static_cast<uint32_t>(plan.split_k * BM * args.slice_rows * 4) : 0u;
-    // This rank's own partials (all slices) are written to the start of the ring before
-    // they are pushed; the receive area for the peers' partials follows the ring.
-    if (plan.split_k > 1 && recv_bytes > ring) return -2;
-    args.recv_off = ring;
+    const TcLayout L = tc_layout(BM, M, group, plan.split_k, plan.stages, plan.w_stages);
+    // This rank's own partials (all slices) are written to the start of the rings before
+    // they are pushed; the receive area for the peers' partials follows the rings.
+    if (plan.split_k > 1 && L.recv_bytes > L.recv_off) return -2;
+    if (plan.w_stages % tc_stage_multiple(BM, IL, NWG) != 0) return -2;
+    args.a_stage_bytes = L.a_stage;
+    args.w_stage_bytes = L.w_stage;
+    args.w_off = L.w_off;
+    args.recv_off = L.recv_off;
     args.timeout_ns = timeout_ns ? timeout_ns : ctx.timeout_ns;
     args.epi = epi;
 
-    const size_t smem = static_cast<size_t>(ring) + recv_bytes + kCtrlBytes + 1024;
+    const size_t smem = L.smem;
     if (smem > static_cast<size_t>(ctx.max_smem_optin)) return -2;
     auto kern = w4a16_tc_kernel<BM, NWG, DT, DQ, IL, PROBE>;
     {   // raise the dynamic shared-memory limit once per device (not a stream operation,
@@ -1045,7 +1103,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.split_k), static_cast<unsigned>(tiles_n(N)),
                        static_cast<unsigned>((M + BM - 1) / BM));
-    cfg.blockDim = dim3(32 * TcShape<BM, IL>::kDq0 + 128 * NWG, 1, 1);
+    cfg.blockDim = dim3(32 * TcShape<BM, IL, NWG>::kDq0 + 128 * NWG, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -1077,23 +1135,26 @@ int tc_a_rows(int tile_m, int M) {
 
 int tc_blocks_per_stage(int tile_m) { return tile_m <= 32 ? 2 : 1; }
 
-uint32_t tc_stage_bytes(int tile_m, int M, int group) {
+TcLayout tc_layout(int tile_m, int M, int group, int split_k, int a_stages, int w_stages) {
     const int kps = tc_blocks_per_stage(tile_m);
-    const uint32_t raw = static_cast<uint32_t>(2 * kps * tc_a_rows(tile_m, M)) * 128u +
-                         static_cast<uint32_t>(kps) * block_bytes(group, true);
-    return (raw + 1023u) & ~1023u;
+    TcLayout L;
+    // 2*kps chunks of 64 K x a_rows rows, 128 bytes per row: a multiple of 1024 bytes, so
+    // every A stage keeps the alignment of the 128-byte swizzle pattern
+    L.a_stage = static_cast<uint32_t>(2 * kps * tc_a_rows(tile_m, M)) * 128u;
+    L.w_stage = (static_cast<uint32_t>(kps) * block_bytes(group, true) + 127u) & ~127u;
+    L.w_off = static_cast<uint32_t>(a_stages) * L.a_stage;
+    L.recv_off = (L.w_off + static_cast<uint32_t>(w_stages) * L.w_stage + 127u) & ~127u;
+    const int slice = (kTileN + split_k - 1) / split_k;
+    L.recv_bytes = split_k > 1 ? static_cast<uint32_t>(split_k * tile_m * slice * 4) : 0u;
+    // + the control block + slack for aligning the dynamic shared base to 1024 bytes
+    L.smem = static_cast<size_t>(L.recv_off) + L.recv_bytes + kCtrlBytes + 1024;
+    return L;
 }
 
 int tc_stage_multiple(int tile_m, bool whole_blocks, int nwg) {
     if (!whole_blocks) return 1;  // every warpgroup reads every stage
     const int kps = tc_blocks_per_stage(tile_m);
     return nwg > kps ? nwg / kps : 1;
-}
-
-int tc_max_stages(int tile_m, int M, int group, int smem_budget) {
-    const int avail = smem_budget - kCtrlBytes - 1024;
-    int s = avail / static_cast<int>(tc_stage_bytes(tile_m, M, group));
-    return s > kMaxStages ? kMaxStages : s;
 }
 
 int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int M, int N,

@@ -21,7 +21,8 @@ struct GemmPlan {
     int kernel;   // 1 = tcgen05, 2 = SIMT
     int tile_m;   // activation rows per tile (tcgen05 kernel); channels per unit (SIMT)
     int split_k;  // K slices (cluster size for the tcgen05 kernel)
-    int stages;   // shared-memory ring depth
+    int stages;   // tcgen05 kernel: depth of the A ring
+    int w_stages; // tcgen05 kernel: depth of the weight ring
     bool pdl;               // launch with programmatic dependent launch
     bool prefetch_weights;  // read the packed blob before the dependency wait
     int dequant;            // tensor-core decode tiles: 0 exponent injection, 1 the
@@ -59,13 +60,22 @@ int launch_tc_splitk_probe(const DeviceCtx& ctx, const void* A, const void* pack
 int tc_a_rows(int tile_m, int M);
 // 128-K weight blocks per ring stage (one bulk copy each stage).
 int tc_blocks_per_stage(int tile_m);
-// Bytes of one stage of the tcgen05 ring for a tile of `tile_m` activation rows.
-uint32_t tc_stage_bytes(int tile_m, int M, int group);
-// The ring depth must be a multiple of this (with whole blocks per warpgroup, each
-// dequant warpgroup then reads a fixed subset of the ring slots and passes every phase of
-// their barriers).
+// Deepest ring of either kind (the control block holds 16 barriers per ring).
+constexpr int kTcMaxStages = 16;
+// Shared-memory layout of the tcgen05 kernel: [A ring][weight ring][split-K receive
+// area][control block], offsets from the 1024-byte aligned dynamic shared base.
+struct TcLayout {
+    uint32_t a_stage;     // bytes of one A stage
+    uint32_t w_stage;     // bytes of one weight stage
+    uint32_t w_off;       // weight ring
+    uint32_t recv_off;    // receive area (end of the rings)
+    uint32_t recv_bytes;  // receive area size (0 without split-K)
+    size_t smem;          // dynamic shared memory to request
+};
+TcLayout tc_layout(int tile_m, int M, int group, int split_k, int a_stages, int w_stages);
+// The weight ring depth must be a multiple of this (with whole blocks per warpgroup, each
+// dequant warpgroup then reads a fixed subset of the weight slots and passes every phase
+// of their barriers).
 int tc_stage_multiple(int tile_m, bool whole_blocks, int nwg);
-// Largest ring depth that fits `smem_budget` bytes of dynamic shared memory.
-int tc_max_stages(int tile_m, int M, int group, int smem_budget);
 
 }  // namespace w4g
