@@ -1,9 +1,10 @@
 """GPU parity of the tensor-core kernel's larger tiles, one test per tile instance the
-launch choice can take: 64- and 128-row tiles whose two warpgroups share every block
-(with and without split-K), 128-row tiles alone on an SM with one K slice (four
-warpgroups unpacking whole blocks, six TMEM W buffers, each group owning every fourth
-slot of the weight ring), 256-row tiles,
-ragged M, N and K, every group size and both dtypes.  Every element of Y is compared with
+launch choice can take: 64-row tiles whose two warpgroups share every block (with and
+without split-K), 128-row tiles two to an SM (two warpgroups sharing every block),
+128-row tiles alone on an SM (four warpgroups unpacking whole blocks, six TMEM W
+buffers, each group owning every fourth slot of the weight ring; with and without
+split-K), 256-row tiles with two and four warpgroups, ragged M, N and K, every group
+size and both dtypes.  Every element of Y is compared with
 the oracle's fp64 product (|Y - Yd| <= 1e-3 * sum_k |A W| + 1 ulp)."""
 import pytest
 import torch
@@ -35,6 +36,7 @@ CASES = [
     (200, 776, 1664, 64, BF16, 128, 1),
     (128, 1024, 4096, 128, FP16, 128, 2),
     (256, 2048, 2048, 32, BF16, 128, 1),
+    (300, 13056, 256, 128, FP16, 128, 1),  # 306 tiles: two per SM, two warpgroups
     (256, 1024, 2048, 128, FP16, 256, 1),
     (300, 520, 1152, 64, BF16, 256, 1),
 ]

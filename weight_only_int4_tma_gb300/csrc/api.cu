@@ -160,12 +160,10 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     if (split < 1 || split > 8 || split > kblocks) return W4A16_ERR_UNSUPPORTED;
 
     // Decode tiles: each dequant warpgroup unpacks whole 128-K blocks.  128-row tiles
-    // alone on an SM with one K slice: four whole-block groups, each owning every fourth
-    // weight slot (measured M = 256, N = K = 8192: 34.4 against 36.7 us with the groups
-    // sharing every block, on a ring that held weights and A together).  Otherwise every
-    // warpgroup takes its chunks of every block (with split-K the receive area leaves too
-    // little room for group-owned slots: M = 64: 18.3 against 20.4 us, M = 128: 30.9
-    // against 36.5 us, same rings).
+    // alone on an SM: four whole-block groups, each owning every fourth weight slot
+    // (measured N = K = 8192: M = 256 34.4 against 36.7 us, M = 128 with split-K 2 25.5
+    // against 28.1 us, with the groups sharing every block).  64-row tiles: both
+    // arrangements measured equal (M = 64: 18.2 us), the shared one is kept.
     plan->whole_blocks = bm <= 32;
     plan->nwg = 2;
     // Shared-block tiles: four warpgroups (16 dequant warps) hide more latency where one
@@ -175,7 +173,7 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     // store two groups stay faster (273.0 against 280.2 us).  Four groups at two CTAs per
     // SM would exceed the register file.
     if ((bm == 128 && occ == 1) || (bm == 256 && heavy_epilogue)) plan->nwg = 4;
-    if (bm == 128 && occ == 1 && split == 1) plan->whole_blocks = true;
+    if (bm == 128 && occ == 1) plan->whole_blocks = true;
     const int mult = tc_stage_multiple(bm, plan->whole_blocks, plan->nwg);
 
     // Rings: A stages are freed when their MMAs complete, weight stages as soon as they

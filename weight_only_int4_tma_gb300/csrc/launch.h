@@ -60,6 +60,10 @@ int launch_tc_splitk_probe(const DeviceCtx& ctx, const void* A, const void* pack
 int tc_a_rows(int tile_m, int M);
 // 128-K weight blocks per ring stage (one bulk copy each stage).
 int tc_blocks_per_stage(int tile_m);
+// Channels of a 128-channel tile owned by each cluster rank under split-K: ceil(128 /
+// split_k) rounded up to a multiple of 4, so that every rank's slice of the partials is
+// read and stored 4 channels at a time (the last rank may own fewer).
+inline int tc_slice_rows(int split_k) { return ((128 + split_k - 1) / split_k + 3) & ~3; }
 // Deepest ring of either kind (the control block holds 16 barriers per ring).
 constexpr int kTcMaxStages = 16;
 // Shared-memory layout of the tcgen05 kernel: [A ring][weight ring][split-K receive
