@@ -216,9 +216,11 @@ def simulate(kNMI, NWG, T, kps, SW, SA, nkb, rng, interleave, per_party=True,
 
 def configs(interleave):
     # (2, 2): decode tiles; (1, 1): 64- and 128-row tiles (whole blocks: 2 or 4 groups,
-    # 3 or 6 W buffers); (1, 2): a single-issuer variant of the two-block stage
-    for kNMI, kps in ((2, 2), (1, 1), (1, 2)):
-        for T in (2, 3, 6):
+    # 3 or 6 W buffers); (2, 1): 128-row whole-block tiles with two issuers taking
+    # alternate blocks (one block per stage); (1, 2): a single-issuer variant of the
+    # two-block stage
+    for kNMI, kps in ((2, 2), (1, 1), (2, 1), (1, 2)):
+        for T in (2, 3, 4, 6):
             for NWG in (1, 2, 4):
                 if interleave and NWG % kps:  # the kernel's static rule for whole blocks
                     continue
@@ -227,7 +229,11 @@ def configs(interleave):
                     # multiple of groups per stage
                     if interleave and NWG > kps and SW % (NWG // kps):
                         continue
-                    for SA in (2, 3, 5):
+                    for SA in (2, 3, 4, 5):
+                        # host rule: two issuers with one block per stage each read
+                        # every other A stage, so the A ring depth is even
+                        if kNMI == 2 and kps == 1 and SA % 2:
+                            continue
                         for nkb in (1, 2, 3, 5, 7, 11, 16):
                             yield kNMI, NWG, T, kps, SW, SA, nkb
 
@@ -268,6 +274,18 @@ def test_model_catches_a_weight_slot_released_too_early():
         hits += e is not None and e.startswith("race")
         clean += simulate(1, 2, 3, 1, 4, 3, 16, random.Random(trial), False) is not None
     assert hits > 0 and clean == 0, (hits, clean)
+
+
+def test_model_catches_an_odd_a_ring_with_two_issuers_of_single_block_stages():
+    """Two issuers taking alternate blocks of one block per stage share the A slots of an
+    odd-depth ring between them (two waiting parties per barrier); the host keeps that
+    depth even, and the model must flag the odd depths."""
+    hits = 0
+    for SA in (3, 5):
+        for trial in range(30):
+            e = simulate(2, 4, 4, 1, 8, SA, 16, random.Random(trial), True, one_producer=False)
+            hits += e is not None
+    assert hits > 0, hits
 
 
 def test_model_reproduces_the_shared_layout_failure():

@@ -54,11 +54,12 @@ def test_large_tile_instance(M, N, K, group, dtype, tile_m, split_k):
     assert_parity_full(c, Y)
 
 
-@pytest.mark.parametrize("stages", [2, 3, 4])
+@pytest.mark.parametrize("stages", [2, 4])
 def test_128_row_tile_ring_depths(stages):
-    """Four whole-block warpgroups with A rings of 2, 3 and 4 stages beside a weight ring
-    whose depth is a multiple of 4 (each group reads every fourth weight slot); K = 8192
-    makes both rings wrap many times at depths that differ from each other."""
+    """Four whole-block warpgroups and two MMA issuers taking alternate blocks, with A
+    rings of 2 and 4 stages beside a weight ring whose depth is a multiple of 4 (each
+    group reads every fourth weight slot); K = 8192 makes both rings wrap many times at
+    depths that differ from each other."""
     p = w4.w4a16_gemm_plan(128, 256, 8192, 128, FP16, kernel=w4.W4A16_KERNEL_TC, tile_m=128,
                            split_k=1, stages=stages)
     assert p["stages"] == stages and p["w_stages"] % 4 == 0 and p["w_stages"] >= 4
@@ -84,12 +85,21 @@ def test_rings_of_different_depths_wrap(tile_m, split_k, stages):
     assert_parity_full(c, Y)
 
 
+def test_128_row_tile_rejects_an_odd_a_ring():
+    """The two issuers of 128-row whole-block tiles take every other A stage, so an odd
+    A ring depth would give an A slot two waiting issuers; the host refuses it."""
+    with pytest.raises(w4.W4A16Error) as e:
+        w4.w4a16_gemm_plan(128, 512, 4096, 128, FP16, kernel=w4.W4A16_KERNEL_TC, tile_m=128,
+                           split_k=1, stages=3)
+    assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
+
+
 def test_128_row_tile_rejects_a_ring_that_does_not_fit():
     """A ring depth above what fits in shared memory is refused on the host; nothing
     runs."""
     with pytest.raises(w4.W4A16Error) as e:
         w4.w4a16_gemm_plan(128, 512, 4096, 128, FP16, kernel=w4.W4A16_KERNEL_TC, tile_m=128,
-                           split_k=1, stages=7)
+                           split_k=1, stages=8)
     assert e.value.status == w4.W4A16_ERR_UNSUPPORTED
 
 

@@ -175,6 +175,7 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     if ((bm == 128 && occ == 1) || (bm == 256 && heavy_epilogue)) plan->nwg = 4;
     if (bm == 128 && occ == 1) plan->whole_blocks = true;
     const int mult = tc_stage_multiple(bm, plan->whole_blocks, plan->nwg);
+    const int amult = tc_a_stage_multiple(bm, plan->whole_blocks);
 
     // Rings: A stages are freed when their MMAs complete, weight stages as soon as they
     // are unpacked (into TMEM), so the weight ring needs only a few slots per reading
@@ -190,11 +191,11 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     if (bm <= 32) {
         for (int w = sw_max; w >= sw_min && !sa; w -= mult)
             for (int a = sa_max; a >= sa_min; --a)
-                if (fits(a, w)) { sa = a; sw = w; break; }
+                if (a % amult == 0 && fits(a, w)) { sa = a; sw = w; break; }
     } else {
         for (int a = sa_max; a >= sa_min && !sa; --a)
             for (int w = sw_max; w >= sw_min; w -= mult)
-                if (fits(a, w)) { sa = a; sw = w; break; }
+                if (a % amult == 0 && fits(a, w)) { sa = a; sw = w; break; }
     }
     if (!sa) return W4A16_ERR_UNSUPPORTED;
     // With split-K a rank first writes its own partials of every slice to the start of
@@ -206,7 +207,8 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     while (split > 1 && !rings_hold_partials(sa, sw) && sw + mult <= kTcMaxStages &&
            fits(sa, sw + mult))
         sw += mult;
-    if (sa < 2 || sa > kTcMaxStages || sw < sw_min || sw > kTcMaxStages || sw % mult != 0 ||
+    if (sa < 2 || sa > kTcMaxStages || sa % amult != 0 || sw < sw_min || sw > kTcMaxStages ||
+        sw % mult != 0 ||
         !fits(sa, sw) || !rings_hold_partials(sa, sw))
         return W4A16_ERR_UNSUPPORTED;
     plan->tile_m = bm;

@@ -94,9 +94,10 @@ struct TcArgs {
 template <int BM, bool kIL, int NWG>
 struct TcShape {
     // MMA-issuing threads (one per warp).  A 128-row K=16 tcgen05.mma costs its issuing
-    // thread tens of cycles whatever N is, so narrow decode tiles (N = 16 or 32) split
-    // the blocks over two issuers, even blocks into accumulator 0, odd into 1.
-    static constexpr int kNMI = BM <= 32 ? 2 : 1;
+    // thread tens of cycles, so narrow decode tiles (N = 16 or 32) and the 128-row
+    // whole-block tiles split the blocks over two issuers, even blocks into accumulator
+    // 0, odd into 1 (one issuer kept the tensor pipe of a 128-row tile ~70 % busy).
+    static constexpr int kNMI = (BM <= 32 || (BM == 128 && kIL)) ? 2 : 1;
     static constexpr int kKps = BM <= 32 ? 2 : 1;          // 128-K blocks per ring stage
     // Decode tiles stream both rings from warp 0 (their A tiles are small and their K
     // slices short; an extra warp cost ~0.25 us per launch); larger tiles give the A ring
@@ -112,7 +113,10 @@ struct TcShape {
     // warps that read each weight stage (and arrive on its empty barrier): one warpgroup
     // per block with whole-block groups, every warpgroup otherwise
     static constexpr int kWReaders(int nwg) { return (kIL ? 4 : 4 * nwg) * kKps; }
-    static constexpr int kACol0 = BM < 64 ? 64 : BM;       // first W staging column
+    static constexpr int kACol0 = kNMI * BM < 64 ? 64 : kNMI * BM;  // first W staging column
+    // A stages an issuer advances per block it issues (two issuers with one block per
+    // stage take every other stage)
+    static constexpr int kSSteps = kNMI / kKps;
     // TMEM W buffers: as many as the CTA's TMEM share holds: 256 columns when two CTAs
     // share an SM (tiles of up to 64 rows, and 128-row tiles with two warpgroups), 512
     // for a CTA alone on an SM (128-row tiles with four warpgroups, 256-row tiles)
@@ -548,9 +552,12 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
             const uint64_t chunk16 = a_chunk >> 4;
             const uint32_t dacc = tmem + static_cast<uint32_t>(k * BM);  // this issuer's D
             bool ok = true;
-            // kNMI == 2 implies two blocks per stage: issuer k owns block b = k of every
-            // stage, so the stage advances once per issued block.
-            int s = 0, b = kNMI == 2 ? k : 0, t = k;
+            // Two issuers and two blocks per stage: issuer k owns block b = k of every
+            // stage.  Two issuers and one block per stage: issuer k takes stages k, k + 2,
+            // ... (the host keeps the A ring depth even, so each A slot has one waiting
+            // issuer).
+            int s = (kNMI == 2 && S::kKps == 1) ? k : 0;
+            int b = (kNMI == 2 && S::kKps == 2) ? k : 0, t = k;
             uint32_t ph = 0;
             uint32_t fpar = 0;  // bit t: parity of this issuer's next wait on tfull[k][t]
             for (int i = k; i < nkb; i += kNMI) {   // i: 128-K block
@@ -591,7 +598,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 t += kNMI;
                 if (t >= kTBuf) t -= kTBuf;
                 if (kNMI == 1) b = stage_done ? 0 : b + 1;
-                if (stage_done && ++s == args.a_stages) { s = 0; ph ^= 1u; }
+                if (stage_done) {
+                    s += S::kSSteps;
+                    if (s >= args.a_stages) { s -= args.a_stages; ph ^= 1u; }
+                }
             }
             if (lane == 0) {
                 tc_commit(accum_bar);
@@ -1128,6 +1138,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     // they are pushed; the receive area for the peers' partials follows the rings.
     if (plan.split_k > 1 && L.recv_bytes > L.recv_off) return -2;
     if (plan.w_stages % tc_stage_multiple(BM, IL, NWG) != 0) return -2;
+    if (plan.stages % tc_a_stage_multiple(BM, IL) != 0) return -2;
     args.a_stage_bytes = L.a_stage;
     args.w_stage_bytes = L.w_stage;
     args.w_off = L.w_off;
@@ -1201,6 +1212,10 @@ TcLayout tc_layout(int tile_m, int M, int group, int split_k, int a_stages, int 
     // + the control block + slack for aligning the dynamic shared base to 1024 bytes
     L.smem = static_cast<size_t>(L.recv_off) + L.recv_bytes + kCtrlBytes + 1024;
     return L;
+}
+
+int tc_a_stage_multiple(int tile_m, bool whole_blocks) {
+    return TcShape<128, true, 4>::kSSteps == 2 && tile_m == 128 && whole_blocks ? 2 : 1;
 }
 
 int tc_stage_multiple(int tile_m, bool whole_blocks, int nwg) {

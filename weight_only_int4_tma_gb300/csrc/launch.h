@@ -81,5 +81,8 @@ TcLayout tc_layout(int tile_m, int M, int group, int split_k, int a_stages, int 
 // dequant warpgroup then reads a fixed subset of the weight slots and passes every phase
 // of their barriers).
 int tc_stage_multiple(int tile_m, bool whole_blocks, int nwg);
+// The A ring depth must be a multiple of this (2 where two MMA issuers take every other
+// stage, so that each A slot has one waiting issuer).
+int tc_a_stage_multiple(int tile_m, bool whole_blocks);
 
 }  // namespace w4g
