@@ -136,8 +136,9 @@ def test_gemm_tc_tilings(tile_m, split_k):
     M = {16: 13, 32: 30, 64: 64, 128: 129, 256: 200}[tile_m]
     c = si.make_case(M, 256, 1024, 128, FP16, seed=tile_m + split_k)
     packed = repack_case(c)
-    if tile_m == 256 and split_k > 1:
-        # the split-K receive area of a 256-row tile does not fit beside its ring
+    if tile_m == 256 and split_k > 2:
+        # the split-K receive area of a 256-row tile fits beside its rings for two
+        # K slices only
         with pytest.raises(w4.W4A16Error) as e:
             run_gemm(c, packed, kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m, split_k=split_k)
         assert e.value.status == w4.W4A16_ERR_UNSUPPORTED

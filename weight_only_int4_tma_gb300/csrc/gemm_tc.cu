@@ -316,7 +316,8 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     uint8_t* base_ptr = smem_raw + (base - raw);
     // shared layout: [A ring][weight ring][split-K receive area][control block]
     const uint32_t ctrl_off = args.recv_off +
-        (args.splits > 1 ? static_cast<uint32_t>(args.splits * BM * args.slice_rows * 4) : 0u);
+        (args.splits > 1 ? static_cast<uint32_t>((args.splits - 1) * BM * args.slice_rows * 4)
+                         : 0u);
     const uint32_t ctrl = base + ctrl_off;
     uint8_t* ctrl_ptr = base_ptr + ctrl_off;
     const uint32_t wbase = base + args.w_off;
@@ -908,8 +909,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 if (p < args.splits && p != static_cast<int>(rank) &&
                     !(kNoPushProbe && rank == 0)) {
                     const uint32_t src = base + static_cast<uint32_t>(p) * slice_bytes;
+                    // rank's slot in p's receive area (one slot per other rank)
+                    const uint32_t slot = rank < static_cast<uint32_t>(p) ? rank : rank - 1u;
                     const uint32_t dst =
-                        map_to_rank(base + args.recv_off + rank * slice_bytes, p);
+                        map_to_rank(base + args.recv_off + slot * slice_bytes, p);
                     bulk_s2cluster(dst, src, slice_bytes, map_to_rank(recv_bar, p));
                     bulk_commit();
                     bulk_wait_read_all();
@@ -948,9 +951,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                         const int j = e - ml * nr;
                         float acc = 0.0f;
                         for (int p = 0; p < args.splits; ++p) {
+                            const int slot = p < static_cast<int>(rank) ? p : p - 1;
                             const float* src = p == static_cast<int>(rank)
                                                    ? part + (static_cast<int>(rank) * BM + ml) * R
-                                                   : recvp + (p * BM + ml) * R;
+                                                   : recvp + (slot * BM + ml) * R;
                             acc += src[j];
                         }
                         const int n = n_tile * kTileN + r0 + j;
@@ -977,9 +981,10 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                     for (int ml = mfirst; ml < mvalid; ml += mstep) {
                         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
                         for (int p = 0; p < args.splits; ++p) {  // rank order
+                            const int slot = p < static_cast<int>(rank) ? p : p - 1;
                             const float* src = p == static_cast<int>(rank)
                                                    ? part + (static_cast<int>(rank) * BM + ml) * R
-                                                   : recvp + (p * BM + ml) * R;
+                                                   : recvp + (slot * BM + ml) * R;
                             const float4 v = *reinterpret_cast<const float4*>(src + j);
                             acc[0] += v.x;
                             acc[1] += v.y;
@@ -1136,7 +1141,7 @@ int launch_tc_instance(const DeviceCtx& ctx, const void* A, const void* packed, 
     const TcLayout L = tc_layout(BM, M, group, plan.split_k, plan.stages, plan.w_stages);
     // This rank's own partials (all slices) are written to the start of the rings before
     // they are pushed; the receive area for the peers' partials follows the rings.
-    if (plan.split_k > 1 && L.recv_bytes > L.recv_off) return -2;
+    if (plan.split_k > 1 && L.part_bytes > L.recv_off) return -2;
     if (plan.w_stages % tc_stage_multiple(BM, IL, NWG) != 0) return -2;
     if (plan.stages % tc_a_stage_multiple(BM, IL) != 0) return -2;
     args.a_stage_bytes = L.a_stage;
@@ -1208,7 +1213,8 @@ TcLayout tc_layout(int tile_m, int M, int group, int split_k, int a_stages, int 
     L.w_off = static_cast<uint32_t>(a_stages) * L.a_stage;
     L.recv_off = (L.w_off + static_cast<uint32_t>(w_stages) * L.w_stage + 127u) & ~127u;
     const int slice = tc_slice_rows(split_k);
-    L.recv_bytes = split_k > 1 ? static_cast<uint32_t>(split_k * tile_m * slice * 4) : 0u;
+    L.part_bytes = split_k > 1 ? static_cast<uint32_t>(split_k * tile_m * slice * 4) : 0u;
+    L.recv_bytes = split_k > 1 ? static_cast<uint32_t>((split_k - 1) * tile_m * slice * 4) : 0u;
     // + the control block + slack for aligning the dynamic shared base to 1024 bytes
     L.smem = static_cast<size_t>(L.recv_off) + L.recv_bytes + kCtrlBytes + 1024;
     return L;

@@ -73,7 +73,9 @@ struct TcLayout {
     uint32_t w_stage;     // bytes of one weight stage
     uint32_t w_off;       // weight ring
     uint32_t recv_off;    // receive area (end of the rings)
-    uint32_t recv_bytes;  // receive area size (0 without split-K)
+    uint32_t recv_bytes;  // receive area: one slice per other rank (0 without split-K)
+    uint32_t part_bytes;  // this rank's partials of every slice, staged at the start of
+                          // the rings before they are pushed (0 without split-K)
     size_t smem;          // dynamic shared memory to request
 };
 TcLayout tc_layout(int tile_m, int M, int group, int split_k, int a_stages, int w_stages);
