@@ -49,6 +49,12 @@ RAGGED = [
     (40, 392, 1120, 32, FP16, True, {}),                     # 64-row tile, 2-D A boxes
     (130, 200, 640, 128, BF16, True, {}),                    # 128-row tiles, N tail
     (300, 456, 352, 32, FP16, False, dict(kernel=1, tile_m=256)),
+    # split-K owners of larger tiles sum four channels per thread; slices of 44 / 28 /
+    # 20 channels (split 3 / 5 / 7) with the last tile ending inside a slice or before it
+    (64, 392, 2048, 64, FP16, True, dict(kernel=1, tile_m=64, split_k=3)),
+    (100, 264, 2048, 128, BF16, True, dict(kernel=1, tile_m=128, split_k=5)),
+    (64, 200, 1792, 32, FP16, False, dict(kernel=1, tile_m=64, split_k=7)),
+    (128, 136, 4096, 128, FP16, True, dict(kernel=1, tile_m=128, split_k=2)),
 ]
 
 
@@ -79,6 +85,30 @@ def test_epilogue_ragged_n(kernel):
     yd, bb, _ = oracle.gemm(c.A, wd, M, N, K, FP16)
     out, bo, _ = oracle.epilogue(yd, bb, bias, res, w4.W4A16_ACT_SILU, M, N, FP16)
     bad, first, worst = oracle.check(to_host_u16(Y), out, bo, FP16)
+    assert bad == 0, (bad, first, worst)
+
+
+@pytest.mark.parametrize("tile_m,split_k", [(64, 3), (128, 2)])
+def test_epilogue_split_k_larger_tiles_ragged_n(tile_m, split_k):
+    """Bias, SiLU, residual and the per-channel factor applied by the split-K owner of a
+    larger tile (four channels per thread) on a ragged N, against the oracle's fused
+    epilogue."""
+    M, N, K, g = 70, 392, 2048, 64
+    c = si.make_case(M, N, K, g, BF16, seed=tile_m + split_k, channel_scale=(0.5, 2.0))
+    packed = repack_case(c)
+    rng = np.random.default_rng(tile_m)
+    bias = oracle.encode(rng.normal(size=N), BF16)
+    res = oracle.encode(rng.normal(size=(M, N)), BF16)
+    A = to_dev(c.A)
+    Y = torch.empty((M, N), dtype=torch.int16, device="cuda")
+    w4.w4a16_gemm_epilogue(A, packed, M, N, K, g, BF16, to_dev(bias), to_dev(res),
+                           w4.W4A16_ACT_SILU, Y, kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m,
+                           split_k=split_k)
+    assert w4.w4a16_get_device_status() == 0
+    wd = oracle.dequant(c.qweight, c.scales, c.qzeros, N, K, g, BF16)
+    yd, bb, _ = oracle.gemm(c.A, wd, M, N, K, BF16, cscale=c.cscale)
+    out, bo, _ = oracle.epilogue(yd, bb, bias, res, w4.W4A16_ACT_SILU, M, N, BF16)
+    bad, first, worst = oracle.check(to_host_u16(Y), out, bo, BF16)
     assert bad == 0, (bad, first, worst)
 
 
