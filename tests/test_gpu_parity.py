@@ -157,6 +157,19 @@ def test_gemm_tc_launch_flags(flags, split_k):
     assert_parity_full(c, Y)
 
 
+@pytest.mark.parametrize("flags", [w4.W4A16_GEMM_NO_PDL, w4.W4A16_GEMM_NO_WEIGHT_PREFETCH])
+@pytest.mark.parametrize("tile_m,split_k", [(64, 2), (128, 1), (256, 1)])
+def test_gemm_tc_launch_flags_larger_tiles(flags, tile_m, split_k):
+    """The larger tiles stream weights and A from two producer warps; without weight
+    prefetch the weight producer starts only after the dependency wait, without PDL the
+    launch waits for the previous kernel."""
+    c = si.make_case(tile_m - 5, 384, 2048, 64, BF16, seed=flags + tile_m)
+    packed = repack_case(c)
+    Y = run_gemm(c, packed, kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m, split_k=split_k,
+                 flags=flags)
+    assert_parity_full(c, Y)
+
+
 def test_back_to_back_gemms_share_nothing():
     """Consecutive launches overlap under programmatic dependent launch: the second
     GEMM reads the first one's output as its A, so a missing dependency wait would
