@@ -25,8 +25,9 @@
 // and neither waits for the other's slots to come back.
 //
 // Warp roles: warp 0 = weight producer; warps 1..NMI = MMA issuers (two for decode tiles
-// of <= 32 rows, taking even / odd 128-K blocks into two accumulators; warp 1 also
-// allocates TMEM); warp NMI + 1 = A producer; then the dequant warps, 4 per warpgroup
+// of <= 32 rows and for 128-row whole-block tiles, taking even / odd 128-K blocks into two
+// accumulators; warp 1 also allocates TMEM); warp NMI + 1 = A producer (decode tiles
+// stream both rings from warp 0); then the dequant warps, 4 per warpgroup
 // (warp w may only touch TMEM lanes 32*(w%4)..+31, so each warpgroup covers all 128
 // lanes), which also run the epilogue.  The producer and issuer warps run their loops
 // with all 32 lanes and let lane 0 issue, and the warp index and TMEM base are broadcast
