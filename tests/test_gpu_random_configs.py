@@ -1,0 +1,73 @@
+"""GPU parity over seeded random launch configurations of the tensor-core kernel: tile
+height, split-K, A ring depth, launch flags, group size, dtype, zeros, channel factor and
+ragged N / K drawn together, so that ring depths, K slices and tile edges meet in
+combinations the hand-written cases do not list.  A configuration the host refuses
+(W4A16_ERR_UNSUPPORTED: its rings or receive area do not fit) is checked to be refused by
+the plan as well and skipped; every other one is compared with the oracle on every
+element."""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as si
+import weight_only_int4_tma_gb300 as w4
+from gpu_util import assert_parity_full, repack_case, run_gemm
+
+pytestmark = pytest.mark.gpu
+
+FP16, BF16 = 0, 1
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from weight_only_int4_tma_gb300 import build
+    build.build()
+    assert w4.w4a16_get_device_status() == 0
+
+
+def _configs(n=120, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    while len(out) < n:
+        tile = int(rng.choice([16, 32, 64, 128, 256]))
+        M = int(rng.integers(max(1, tile // 2 - 7), tile + 1)) if tile > 16 else int(rng.integers(1, 17))
+        group = int(rng.choice([32, 64, 128]))
+        K = group * int(rng.integers(1, max(2, 3072 // group)))
+        N = 8 * int(rng.integers(1, 97))
+        if M * N * K > 4e8:
+            continue
+        split = int(rng.choice([1, 1, 2, 3, 4, 8]))
+        stages = int(rng.choice([0, 0, 2, 3, 4]))
+        flags = int(rng.choice([0, 0, w4.W4A16_GEMM_NO_PDL, w4.W4A16_GEMM_NO_WEIGHT_PREFETCH]))
+        out.append(dict(M=M, N=N, K=K, group=group, dtype=int(rng.integers(0, 2)),
+                        asym=bool(rng.integers(0, 2)), cscale=bool(rng.integers(0, 2)),
+                        tile_m=tile, split_k=min(split, -(-K // 128)), stages=stages,
+                        flags=flags, seed=int(rng.integers(0, 1 << 20))))
+    return out
+
+
+CONFIGS = _configs()
+
+
+@pytest.mark.parametrize("cfg", CONFIGS, ids=[
+    "M{M}_N{N}_K{K}_g{group}_{dt}_t{tile_m}_s{split_k}_a{stages}_f{flags}".format(
+        dt="bf16" if c["dtype"] else "fp16", **c) for c in CONFIGS])
+def test_random_launch_configuration(cfg):
+    c = si.make_case(cfg["M"], cfg["N"], cfg["K"], cfg["group"], cfg["dtype"],
+                     seed=cfg["seed"], asym=cfg["asym"],
+                     channel_scale=(0.5, 2.0) if cfg["cscale"] else None)
+    ex = dict(kernel=w4.W4A16_KERNEL_TC, tile_m=cfg["tile_m"], split_k=cfg["split_k"],
+              stages=cfg["stages"], flags=cfg["flags"])
+    try:
+        plan = w4.w4a16_gemm_plan(c.M, c.N, c.K, c.group, c.dtype, **ex)
+    except w4.W4A16Error as e:
+        assert e.status == w4.W4A16_ERR_UNSUPPORTED
+        with pytest.raises(w4.W4A16Error):
+            run_gemm(c, repack_case(c), **ex)
+        pytest.skip("refused by the host (rings or receive area do not fit)")
+    assert plan["tile_m"] == cfg["tile_m"] and plan["split_k"] == cfg["split_k"]
+    if cfg["stages"]:
+        assert plan["stages"] == cfg["stages"]
+    assert_parity_full(c, run_gemm(c, repack_case(c), **ex))
