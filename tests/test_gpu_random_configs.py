@@ -1,7 +1,8 @@
 """GPU parity over seeded random launch configurations of the tensor-core kernel: tile
 height, split-K, A ring depth, launch flags, group size, dtype, zeros, channel factor and
 ragged N / K drawn together, so that ring depths, K slices and tile edges meet in
-combinations the hand-written cases do not list.  A configuration the host refuses
+combinations the hand-written cases do not list, with and without a fused epilogue
+(bias, activation, in-place residual).  A configuration the host refuses
 (W4A16_ERR_UNSUPPORTED: its rings or receive area do not fit) is checked to be refused by
 the plan as well and skipped; every other one is compared with the oracle on every
 element."""
@@ -41,10 +42,11 @@ def _configs(n=120, seed=2024):
         split = int(rng.choice([1, 1, 2, 3, 4, 8]))
         stages = int(rng.choice([0, 0, 2, 3, 4]))
         flags = int(rng.choice([0, 0, w4.W4A16_GEMM_NO_PDL, w4.W4A16_GEMM_NO_WEIGHT_PREFETCH]))
+        epi = int(rng.choice([0, 0, 1, 2, 3]))  # none, bias + ReLU, bias + SiLU + residual, residual
         out.append(dict(M=M, N=N, K=K, group=group, dtype=int(rng.integers(0, 2)),
                         asym=bool(rng.integers(0, 2)), cscale=bool(rng.integers(0, 2)),
                         tile_m=tile, split_k=min(split, -(-K // 128)), stages=stages,
-                        flags=flags, seed=int(rng.integers(0, 1 << 20))))
+                        flags=flags, epi=epi, seed=int(rng.integers(0, 1 << 20))))
     return out
 
 
@@ -52,7 +54,7 @@ CONFIGS = _configs()
 
 
 @pytest.mark.parametrize("cfg", CONFIGS, ids=[
-    "M{M}_N{N}_K{K}_g{group}_{dt}_t{tile_m}_s{split_k}_a{stages}_f{flags}".format(
+    "M{M}_N{N}_K{K}_g{group}_{dt}_t{tile_m}_s{split_k}_a{stages}_f{flags}_e{epi}".format(
         dt="bf16" if c["dtype"] else "fp16", **c) for c in CONFIGS])
 def test_random_launch_configuration(cfg):
     c = si.make_case(cfg["M"], cfg["N"], cfg["K"], cfg["group"], cfg["dtype"],
@@ -70,4 +72,23 @@ def test_random_launch_configuration(cfg):
     assert plan["tile_m"] == cfg["tile_m"] and plan["split_k"] == cfg["split_k"]
     if cfg["stages"]:
         assert plan["stages"] == cfg["stages"]
-    assert_parity_full(c, run_gemm(c, repack_case(c), **ex))
+    if cfg["epi"] == 0:
+        assert_parity_full(c, run_gemm(c, repack_case(c), **ex))
+        return
+    # fused epilogue: y = act(v * c[n] + bias[n]) + residual[m, n], in place on the residual
+    import oracle
+    from gpu_util import to_dev, to_host_u16
+    act = {1: w4.W4A16_ACT_RELU, 2: w4.W4A16_ACT_SILU, 3: w4.W4A16_ACT_NONE}[cfg["epi"]]
+    rng = np.random.default_rng(cfg["seed"])
+    bias = oracle.encode(rng.normal(size=c.N), c.dtype) if cfg["epi"] in (1, 2) else None
+    res = oracle.encode(rng.normal(size=(c.M, c.N)), c.dtype) if cfg["epi"] in (2, 3) else None
+    Y = to_dev(res) if res is not None else torch.empty((c.M, c.N), dtype=torch.int16,
+                                                       device="cuda")
+    w4.w4a16_gemm_epilogue(to_dev(c.A), repack_case(c), c.M, c.N, c.K, c.group, c.dtype,
+                           to_dev(bias), Y if res is not None else None, act, Y, **ex)
+    assert w4.w4a16_get_device_status() == 0
+    wd = oracle.dequant(c.qweight, c.scales, c.qzeros, c.N, c.K, c.group, c.dtype)
+    yd, bb, _ = oracle.gemm(c.A, wd, c.M, c.N, c.K, c.dtype, cscale=c.cscale)
+    out, bo, _ = oracle.epilogue(yd, bb, bias, res, act, c.M, c.N, c.dtype)
+    bad, first, worst = oracle.check(to_host_u16(Y), out, bo, c.dtype)
+    assert bad == 0, (bad, first, worst)
