@@ -92,3 +92,35 @@ def test_random_launch_configuration(cfg):
     out, bo, _ = oracle.epilogue(yd, bb, bias, res, act, c.M, c.N, c.dtype)
     bad, first, worst = oracle.check(to_host_u16(Y), out, bo, c.dtype)
     assert bad == 0, (bad, first, worst)
+
+
+def _simt_configs(n=40, seed=77):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        group = int(rng.choice([32, 64, 128]))
+        out.append(dict(M=int(rng.integers(1, 9)), N=8 * int(rng.integers(1, 257)),
+                        K=group * int(rng.integers(1, max(2, 4096 // group))), group=group,
+                        dtype=int(rng.integers(0, 2)), asym=bool(rng.integers(0, 2)),
+                        cscale=bool(rng.integers(0, 2)), rows=int(rng.choice([0, 16, 32])),
+                        flags=int(rng.choice([0, w4.W4A16_GEMM_NO_PDL,
+                                              w4.W4A16_GEMM_NO_WEIGHT_PREFETCH])),
+                        seed=int(rng.integers(0, 1 << 20))))
+    return out
+
+
+SIMT = _simt_configs()
+
+
+@pytest.mark.parametrize("cfg", SIMT, ids=[
+    "M{M}_N{N}_K{K}_g{group}_{dt}_r{rows}_f{flags}".format(
+        dt="bf16" if c["dtype"] else "fp16", **c) for c in SIMT])
+def test_random_simt_configuration(cfg):
+    """The CUDA-core GEMV (M <= 8) over random shapes, unit heights and flags."""
+    c = si.make_case(cfg["M"], cfg["N"], cfg["K"], cfg["group"], cfg["dtype"],
+                     seed=cfg["seed"], asym=cfg["asym"],
+                     channel_scale=(0.5, 2.0) if cfg["cscale"] else None)
+    ex = dict(kernel=w4.W4A16_KERNEL_SIMT, tile_m=cfg["rows"], flags=cfg["flags"])
+    assert w4.w4a16_gemm_plan(c.M, c.N, c.K, c.group, c.dtype, **ex)["kernel"] == \
+        w4.W4A16_KERNEL_SIMT
+    assert_parity_full(c, run_gemm(c, repack_case(c), **ex))
