@@ -108,8 +108,10 @@ typedef struct w4a16_gemm_config {
                          tiles (2..16); the weight ring beside it is sized by the library.
                          SIMT: must be 0 (fixed 4-stage cp.async ring)                   */
     int flags;        /* W4A16_GEMM_* bits; 0 = defaults                                 */
-    int reserved[3];  /* must be zero (w4a16_gemm_plan's output: reserved[0] = the weight
-                         ring depth of a TC plan, 0 for SIMT)                            */
+    int reserved[3];  /* must be zero (w4a16_gemm_plan's output, TC plans: reserved[0] =
+                         the weight ring depth, reserved[1] = the dequant warpgroups,
+                         reserved[2] = 1 if each warpgroup unpacks whole 128-K blocks,
+                         0 if they share every block; all 0 for SIMT)                   */
 } w4a16_gemm_config;
 
 /* Library ABI version (W4A16_ABI_VERSION). */
@@ -219,8 +221,8 @@ int w4a16_gemm_epilogue(const void* A, const void* packed, int M, int N, int K, 
 /*
  * The kernel and tiling that w4a16_gemm_ex(..., cfg, ...) would launch for this shape on
  * the current device (cfg may be NULL = AUTO), written to *out with every field resolved
- * (kernel TC or SIMT; split_k, tile_m, stages as used; flags as applied; reserved[0] =
- * the weight ring depth of a TC plan).  Host-side
+ * (kernel TC or SIMT; split_k, tile_m, stages as used; flags as applied; reserved[0..2]
+ * = a TC plan's weight ring depth, dequant warpgroups and whole-block flag).  Host-side
  * only: launches nothing, reads no device memory.  Errors: INVALID_ARG (M < 1, out NULL,
  * bad cfg fields), UNSUPPORTED, CUDA (no usable device).
  */

@@ -215,10 +215,10 @@ def simulate(kNMI, NWG, T, kps, SW, SA, nkb, rng, interleave, per_party=True,
 
 
 def configs(interleave):
-    # (2, 2): decode tiles; (1, 1): 64- and 128-row tiles (whole blocks: 2 or 4 groups,
-    # 3 or 6 W buffers); (2, 1): 128-row whole-block tiles with two issuers taking
-    # alternate blocks (one block per stage); (1, 2): a single-issuer variant of the
-    # two-block stage
+    # (2, 2): decode tiles; (1, 1): the shared-block 64- to 256-row tiles (and a
+    # single-issuer whole-block variant); (2, 1): 64- and 128-row whole-block tiles with
+    # two issuers taking alternate blocks (one block per stage); (1, 2): a single-issuer
+    # variant of the two-block stage
     for kNMI, kps in ((2, 2), (1, 1), (2, 1), (1, 2)):
         for T in (2, 3, 4, 6):
             for NWG in (1, 2, 4):

@@ -1,6 +1,8 @@
 """GPU parity of the tensor-core kernel's larger tiles, one test per tile instance the
-launch choice can take: 64-row tiles whose two warpgroups share every block (with and
-without split-K), 128-row tiles two to an SM (two warpgroups sharing every block),
+launch choice can take: 64-row tiles two to an SM whose two warpgroups share every block
+(with and without split-K), 64-row tiles alone on an SM (four warpgroups unpacking whole
+blocks, two MMA issuers taking alternate blocks; with and without split-K), 128-row tiles
+two to an SM (two warpgroups sharing every block),
 128-row tiles alone on an SM (four warpgroups unpacking whole blocks, six TMEM W
 buffers, each group owning every fourth slot of the weight ring; with and without
 split-K), 256-row tiles with two and four warpgroups, ragged M, N and K, every group
@@ -32,6 +34,11 @@ CASES = [
     (64, 1024, 2048, 128, FP16, 64, 1),
     (70, 520, 1152, 64, BF16, 64, 1),
     (64, 1024, 4096, 32, FP16, 64, 2),
+    # 64-row tiles alone on an SM (enough tiles x K slices to fill the SMs one CTA each)
+    (64, 8192, 1024, 128, FP16, 64, 2),
+    (50, 8192, 1152, 64, BF16, 64, 2),   # 9 K blocks over 2 slices
+    (40, 16000, 640, 64, BF16, 64, 1),   # 125 tiles, no split-K
+    (64, 4096, 2048, 32, FP16, 64, 4),
     (128, 1024, 2048, 128, FP16, 128, 1),
     (200, 776, 1664, 64, BF16, 128, 1),
     (128, 1024, 4096, 128, FP16, 128, 2),
@@ -51,6 +58,40 @@ def test_large_tile_instance(M, N, K, group, dtype, tile_m, split_k):
                               tile_m=tile_m, split_k=split_k)
     assert plan["tile_m"] == tile_m and plan["split_k"] == split_k
     Y = run_gemm(c, repack_case(c), kernel=w4.W4A16_KERNEL_TC, tile_m=tile_m, split_k=split_k)
+    assert_parity_full(c, Y)
+
+
+@pytest.mark.parametrize("M,N,K,split_k,alone", [
+    (64, 8192, 1024, 2, True), (50, 8192, 1152, 2, True), (40, 16000, 640, 1, True),
+    (64, 4096, 2048, 4, True), (64, 1024, 2048, 1, False), (64, 1024, 4096, 2, False),
+    (64, 11008, 4096, 0, False)])
+def test_64_row_tile_arrangement(M, N, K, split_k, alone):
+    """64-row tiles run alone on an SM (four whole-block warpgroups) where one CTA per SM
+    fills at least 4/5 of the SMs, else two to an SM with two warpgroups sharing every
+    block (here with 132 or more SMs: 64 or 125 tiles fill them, 8 or 86 do not)."""
+    if torch.cuda.get_device_properties(0).multi_processor_count < 132:
+        pytest.skip("arrangement thresholds assume a GPU with 132 or more SMs")
+    p = w4.w4a16_gemm_plan(M, N, K, 128 if K % 128 == 0 else 64, FP16,
+                           kernel=w4.W4A16_KERNEL_TC, tile_m=64, split_k=split_k)
+    assert p["whole_blocks"] == alone and p["groups"] == (4 if alone else 2), p
+    if alone:
+        assert p["stages"] % 2 == 0 and p["w_stages"] % 4 == 0, p
+
+
+@pytest.mark.parametrize("stages", [2, 3, 4, 6])
+def test_64_row_whole_block_ring_depths(stages):
+    """64-row tiles alone on an SM with A rings of 2, 4 and 6 stages beside a weight ring
+    whose depth is a multiple of 4 (each group reads every fourth weight slot), K long
+    enough that both rings wrap many times; an odd A ring (3) keeps the shared-block
+    arrangement instead (the two issuers take alternate A stages)."""
+    p = w4.w4a16_gemm_plan(64, 8192, 4096, 128, FP16, kernel=w4.W4A16_KERNEL_TC, tile_m=64,
+                           split_k=2, stages=stages)
+    assert p["stages"] == stages and p["whole_blocks"] == (stages % 2 == 0), p
+    if stages % 2 == 0:
+        assert p["w_stages"] % 4 == 0 and p["groups"] == 4, p
+    c = si.make_case(64, 8192, 4096, 128, FP16, seed=100 + stages)
+    Y = run_gemm(c, repack_case(c), kernel=w4.W4A16_KERNEL_TC, tile_m=64, split_k=2,
+                 stages=stages)
     assert_parity_full(c, Y)
 
 

@@ -181,7 +181,8 @@ def w4a16_gemm_plan(M: int, N: int, K: int, group: int, dtype: int, *,
     _check(lib().w4a16_gemm_plan(M, N, K, group, dtype, ctypes.byref(cfg), ctypes.byref(out)),
            "w4a16_gemm_plan")
     return {"kernel": out.kernel, "split_k": out.split_k, "tile_m": out.tile_m,
-            "stages": out.stages, "w_stages": out.reserved[0], "flags": out.flags}
+            "stages": out.stages, "w_stages": out.reserved[0], "groups": out.reserved[1],
+            "whole_blocks": bool(out.reserved[2]), "flags": out.flags}
 
 
 def w4a16_dequant_debug(packed, N: int, K: int, group: int, dtype: int, W_out,

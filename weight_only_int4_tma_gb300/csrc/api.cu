@@ -128,9 +128,22 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     const int m_tiles = ceil_div(M, bm);
     if (m_tiles > 65535) return W4A16_ERR_UNSUPPORTED;
     const int base = n_tiles * m_tiles;
-    // CTAs per SM the rings are sized for: decode tiles always pair up; 128-row tiles pair
-    // up (shallower rings) when there are enough tiles to fill two per SM.
-    const int occ = bm <= 64 ? 2 : (bm == 128 && base >= 2 * ctx.num_sms ? 2 : 1);
+    // 64-row tiles alone on an SM (four whole-block groups, two MMA issuers) where one
+    // CTA per SM, with the K slices that fit, still fills at least 4/5 of the SMs; an odd
+    // A ring forced by the caller keeps the shared-block arrangement (two issuers take
+    // alternate A stages).
+    bool il64 = false;
+    if (bm == 64 && plan->dequant == 0 && !(cfg && cfg->stages % 2 != 0)) {
+        int s1 = cfg && cfg->split_k ? cfg->split_k : ctx.num_sms / base;
+        if (s1 > 8) s1 = 8;
+        if (s1 > kblocks) s1 = kblocks;
+        il64 = s1 >= 1 && base * s1 <= ctx.num_sms && base * s1 * 5 >= ctx.num_sms * 4;
+    }
+    // CTAs per SM the rings are sized for: decode tiles always pair up, 64-row tiles
+    // unless they run alone (above); 128-row tiles pair up (shallower rings) when there
+    // are enough tiles to fill two per SM.
+    const int occ = bm <= 32 ? 2 : bm == 64 ? (il64 ? 1 : 2)
+                  : (bm == 128 && base >= 2 * ctx.num_sms ? 2 : 1);
 
     int split = cfg && cfg->split_k ? cfg->split_k : 0;
     if (split == 0) {
@@ -162,8 +175,11 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     // Decode tiles: each dequant warpgroup unpacks whole 128-K blocks.  128-row tiles
     // alone on an SM: four whole-block groups, each owning every fourth weight slot
     // (measured N = K = 8192: M = 256 34.4 against 36.7 us, M = 128 with split-K 2 25.5
-    // against 28.1 us, with the groups sharing every block).  64-row tiles: both
-    // arrangements measured equal (M = 64: 18.2 us), the shared one is kept.
+    // against 28.1 us, with the groups sharing every block).  64-row tiles two to an SM:
+    // both arrangements measured equal (M = 64: 18.2 us), the shared one is kept; alone
+    // on an SM (il64, above): four whole-block groups and two issuers (M = 64, N = K =
+    // 8192, split-K 2: 15.3-15.7 us against 16.4-18.0 two to an SM; M = 40, N = 2432:
+    // 8.5 against 10.1 us).
     plan->whole_blocks = bm <= 32;
     plan->nwg = 2;
     // Shared-block tiles: four warpgroups (16 dequant warps) hide more latency where one
@@ -172,8 +188,8 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     // (prefill M = 4096 with bias + SiLU: 311.9 against 338.0 us); for the plain 256-row
     // store two groups stay faster (273.0 against 280.2 us).  Four groups at two CTAs per
     // SM would exceed the register file.
-    if ((bm == 128 && occ == 1) || (bm == 256 && heavy_epilogue)) plan->nwg = 4;
-    if (bm == 128 && occ == 1) plan->whole_blocks = true;
+    if ((bm == 128 && occ == 1) || (bm == 256 && heavy_epilogue) || il64) plan->nwg = 4;
+    if ((bm == 128 && occ == 1) || il64) plan->whole_blocks = true;
     const int mult = tc_stage_multiple(bm, plan->whole_blocks, plan->nwg);
     const int amult = tc_a_stage_multiple(bm, plan->whole_blocks);
 
@@ -186,7 +202,9 @@ int make_plan(const DeviceCtx& ctx, int M, int N, int K, int group,
     const int sw_min = mult > 2 ? mult : 2;
     const int sw_max = 2 * mult > 4 ? 2 * mult : 4;
     const int sa_fixed = cfg && cfg->stages ? cfg->stages : 0;
-    const int sa_max = sa_fixed ? sa_fixed : 4, sa_min = sa_fixed ? sa_fixed : 2;
+    // 64-row tiles alone on an SM: an 8-stage A ring (M = 64, N = K = 8192: 15.3-15.7 us
+    // against 15.9-16.4 with 4 stages)
+    const int sa_max = sa_fixed ? sa_fixed : (il64 ? 8 : 4), sa_min = sa_fixed ? sa_fixed : 2;
     int sa = 0, sw = 0;
     if (bm <= 32) {
         for (int w = sw_max; w >= sw_min && !sa; w -= mult)
@@ -320,7 +338,11 @@ int w4a16_gemm_plan(int M, int N, int K, int group, int dtype, const w4a16_gemm_
     r.split_k = plan.split_k;
     r.tile_m = plan.tile_m;
     r.stages = plan.stages;
-    r.reserved[0] = plan.kernel == W4A16_KERNEL_TC ? plan.w_stages : 0;
+    if (plan.kernel == W4A16_KERNEL_TC) {
+        r.reserved[0] = plan.w_stages;
+        r.reserved[1] = plan.nwg;
+        r.reserved[2] = plan.whole_blocks ? 1 : 0;
+    }
     r.flags = (plan.pdl ? 0 : W4A16_GEMM_NO_PDL) |
               (plan.prefetch_weights ? 0 : W4A16_GEMM_NO_WEIGHT_PREFETCH) |
               (plan.dequant == 1 ? W4A16_GEMM_DEQUANT_LUT : 0) |

@@ -25,8 +25,8 @@
 // and neither waits for the other's slots to come back.
 //
 // Warp roles: warp 0 = weight producer; warps 1..NMI = MMA issuers (two for decode tiles
-// of <= 32 rows and for 128-row whole-block tiles, taking even / odd 128-K blocks into two
-// accumulators; warp 1 also allocates TMEM); warp NMI + 1 = A producer (decode tiles
+// of <= 32 rows and for 64- and 128-row whole-block tiles, taking even / odd 128-K blocks
+// into two accumulators; warp 1 also allocates TMEM); warp NMI + 1 = A producer (decode tiles
 // stream both rings from warp 0); then the dequant warps, 4 per warpgroup
 // (warp w may only touch TMEM lanes 32*(w%4)..+31, so each warpgroup covers all 128
 // lanes), which also run the epilogue.  The producer and issuer warps run their loops
@@ -95,10 +95,11 @@ struct TcArgs {
 template <int BM, bool kIL, int NWG>
 struct TcShape {
     // MMA-issuing threads (one per warp).  A 128-row K=16 tcgen05.mma costs its issuing
-    // thread tens of cycles, so narrow decode tiles (N = 16 or 32) and the 128-row
-    // whole-block tiles split the blocks over two issuers, even blocks into accumulator
-    // 0, odd into 1 (one issuer kept the tensor pipe of a 128-row tile ~70 % busy).
-    static constexpr int kNMI = (BM <= 32 || (BM == 128 && kIL)) ? 2 : 1;
+    // thread tens of cycles, so narrow decode tiles (N = 16 or 32) and the 64- and
+    // 128-row whole-block tiles split the blocks over two issuers, even blocks into
+    // accumulator 0, odd into 1 (one issuer kept the tensor pipe of a 128-row tile ~70 %
+    // busy).
+    static constexpr int kNMI = (BM <= 32 || (kIL && (BM == 64 || BM == 128))) ? 2 : 1;
     static constexpr int kKps = BM <= 32 ? 2 : 1;          // 128-K blocks per ring stage
     // Decode tiles stream both rings from warp 0 (their A tiles are small and their K
     // slices short; an extra warp cost ~0.25 us per launch); larger tiles give the A ring
@@ -118,11 +119,12 @@ struct TcShape {
     // A stages an issuer advances per block it issues (two issuers with one block per
     // stage take every other stage)
     static constexpr int kSSteps = kNMI / kKps;
-    // TMEM W buffers: as many as the CTA's TMEM share holds: 256 columns when two CTAs
-    // share an SM (tiles of up to 64 rows, and 128-row tiles with two warpgroups), 512
-    // for a CTA alone on an SM (128-row tiles with four warpgroups, 256-row tiles)
-    static constexpr bool kShared = BM <= 64 || (BM == 128 && NWG == 2);
-    static constexpr int kTBuf = (kShared ? 256 - kACol0 : 512 - kACol0) / 64;
+    // TMEM W buffers: as many as the CTA's TMEM share holds (256 columns when two CTAs
+    // share an SM: tiles of up to 128 rows with two warpgroups; 512 for a CTA alone on an
+    // SM: four warpgroups, or 256-row tiles), at most the control block's tfull slots
+    static constexpr bool kShared = BM <= 128 && NWG <= 2;
+    static constexpr int kTBufFit = (kShared ? 256 - kACol0 : 512 - kACol0) / 64;
+    static constexpr int kTBuf = kTBufFit < 8 / kNMI ? kTBufFit : 8 / kNMI;
     static constexpr int kColsUsed = kACol0 + kTBuf * 64;
     static constexpr int kTmemCols = kColsUsed <= 32 ? 32 : kColsUsed <= 64 ? 64
                                    : kColsUsed <= 128 ? 128 : kColsUsed <= 256 ? 256 : 512;
@@ -298,7 +300,8 @@ __device__ __forceinline__ void unpack_part_of(int wg, int gshift, const uint8_t
 // 0 pushes none of its partials, so the other ranks' bounded waits for them run out.
 template <int BM, int NWG, int DT, int kDq = kDqMagic, bool kIL = (BM <= 32),
           bool kNoPushProbe = false>
-__global__ void __launch_bounds__(32 * TcShape<BM, kIL, NWG>::kDq0 + 128 * NWG, BM <= 64 ? 2 : 1)
+__global__ void __launch_bounds__(32 * TcShape<BM, kIL, NWG>::kDq0 + 128 * NWG,
+                                  (BM <= 64 && NWG <= 2) ? 2 : 1)
 w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
     using S = TcShape<BM, kIL, NWG>;
     constexpr int kTBuf = S::kTBuf;
@@ -1222,7 +1225,9 @@ TcLayout tc_layout(int tile_m, int M, int group, int split_k, int a_stages, int 
 }
 
 int tc_a_stage_multiple(int tile_m, bool whole_blocks) {
-    return TcShape<128, true, 4>::kSSteps == 2 && tile_m == 128 && whole_blocks ? 2 : 1;
+    static_assert(TcShape<64, true, 4>::kSSteps == 2 && TcShape<128, true, 4>::kSSteps == 2,
+                  "whole-block 64- and 128-row tiles: two issuers take alternate A stages");
+    return (tile_m == 64 || tile_m == 128) && whole_blocks ? 2 : 1;
 }
 
 int tc_stage_multiple(int tile_m, bool whole_blocks, int nwg) {
@@ -1270,6 +1275,7 @@ int launch_tc_gemm(const DeviceCtx& ctx, const void* A, const void* packed, int 
                       : launch_tc_instance<BMV, NWGV, 1, kDqMagic, true>(                   \
                             ctx, A, packed, M, N, K, group, Y, plan, epi, stream);
     if (plan.whole_blocks && plan.tile_m == 128 && plan.nwg == 4) { W4G_TC_IL(128, 4) }
+    if (plan.whole_blocks && plan.tile_m == 64 && plan.nwg == 4) { W4G_TC_IL(64, 4) }
     if (plan.nwg == 4) {  // shared-block tiles with four warpgroups
         switch (plan.tile_m) {
             W4G_TC_CASE(256, 4)
