@@ -586,18 +586,26 @@ w4a16_tc_kernel(const __grid_constant__ CUtensorMap tmap_a, const TcArgs args) {
                 // kInt: block i's own fp32 partial, in D slot (k, (i / kNMI) & 1)
                 const uint32_t dslot = (k * 2 + ((i / kNMI) & 1)) * BM;
                 const uint32_t dd = kInt ? tmem + dslot : dacc;
-                if (lane == 0) {
-                    tc_mma_ts(dd, a0, d0, idesc, (!kInt && i >= kNMI) ? 1u : 0u);
-                    tc_mma_ts(dd, a0 + 8, d0 + 2, idesc, 1u);
-                    tc_mma_ts(dd, a0 + 16, d0 + 4, idesc, 1u);
-                    tc_mma_ts(dd, a0 + 24, d0 + 6, idesc, 1u);
-                    tc_mma_ts(dd, a0 + 32, d1, idesc, 1u);
-                    tc_mma_ts(dd, a0 + 40, d1 + 2, idesc, 1u);
-                    tc_mma_ts(dd, a0 + 48, d1 + 4, idesc, 1u);
-                    tc_mma_ts(dd, a0 + 56, d1 + 6, idesc, 1u);
-                    tc_commit(te);
-                    if (kInt) tc_commit(dfull0 + dslot / 2);  // 8 bytes per (k, slot)
-                    if (stage_done) tc_commit(aempty0 + 8 * s);
+                if constexpr (kInt) {
+                    if (lane == 0) {
+                        tc_mma_ts(dd, a0, d0, idesc, 0u);
+                        tc_mma_ts(dd, a0 + 8, d0 + 2, idesc, 1u);
+                        tc_mma_ts(dd, a0 + 16, d0 + 4, idesc, 1u);
+                        tc_mma_ts(dd, a0 + 24, d0 + 6, idesc, 1u);
+                        tc_mma_ts(dd, a0 + 32, d1, idesc, 1u);
+                        tc_mma_ts(dd, a0 + 40, d1 + 2, idesc, 1u);
+                        tc_mma_ts(dd, a0 + 48, d1 + 4, idesc, 1u);
+                        tc_mma_ts(dd, a0 + 56, d1 + 6, idesc, 1u);
+                        tc_commit(te);
+                        tc_commit(dfull0 + dslot / 2);  // 8 bytes per (k, slot)
+                        if (stage_done) tc_commit(aempty0 + 8 * s);
+                    }
+                } else {  // the whole warp executes it, lane 0 issues and commits
+                    const uint32_t av[8] = {a0, a0 + 8, a0 + 16, a0 + 24,
+                                            a0 + 32, a0 + 40, a0 + 48, a0 + 56};
+                    const uint64_t bv[8] = {d0, d0 + 2, d0 + 4, d0 + 6, d1, d1 + 2, d1 + 4, d1 + 6};
+                    tc_mma_block_lane0(dd, av, bv, idesc, i >= kNMI ? 1u : 0u, te,
+                                       stage_done ? aempty0 + 8 * s : 0u);
                 }
                 __syncwarp();
                 t += kNMI;

@@ -257,6 +257,40 @@ __device__ __forceinline__ void tc_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint
         : "memory");
 }
 
+// The eight K = 16 MMAs of one 128-K block and the commits that track them, issued by
+// lane 0 while the whole warp executes the statement (no branch around it, so the operands,
+// computed by every lane, stay warp-uniform): D[d] (+)= A[a_j] . B[b_j]^T for j = 0..7, the
+// first accumulating only if `accumulate`; then an arrive on bar0 and, unless bar1 is 0,
+// on bar1 once they are done.  Lane 0 is the issuing thread of every block, so its later
+// commits track all of them.
+__device__ __forceinline__ void tc_mma_block_lane0(uint32_t d_tmem, const uint32_t (&a)[8],
+                                                   const uint64_t (&b)[8], uint32_t idesc,
+                                                   uint32_t accumulate, uint32_t bar0,
+                                                   uint32_t bar1) {
+    asm volatile(
+        "{\n\t.reg .pred p, q, e, c;\n\t.reg .b32 l;\n\t"
+        "mov.u32 l, %%laneid;\n\t"
+        "setp.eq.u32 e, l, 0;\n\t"
+        "setp.ne.b32 p, %18, 0;\n\t"
+        "setp.ne.b32 q, %17, 0;\n\t"  // idesc is never 0: a true predicate
+        "setp.ne.b32 c, %20, 0;\n\t"
+        "and.pred c, c, e;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %9, %17, p;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%2], %10, %17, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%3], %11, %17, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%4], %12, %17, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%5], %13, %17, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%6], %14, %17, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%7], %15, %17, q;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%8], %16, %17, q;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%19];\n\t"
+        "@c tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%20];\n\t}"
+        ::"r"(d_tmem), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]),
+          "r"(a[6]), "r"(a[7]), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]),
+          "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(idesc), "r"(accumulate), "r"(bar0), "r"(bar1)
+        : "memory");
+}
+
 // Arrive (once) on an mbarrier when every tcgen05 op issued so far by this thread is done.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile(
