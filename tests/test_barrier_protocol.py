@@ -5,7 +5,8 @@ current phase from the one before it.  This discrete-event model replays the ker
 protocol (weight producer, A producer, MMA issuers, dequant warpgroups, asynchronous copy
 and MMA completions with random latencies; one issuer's MMAs complete in order, the two
 issuers' independently) and flags any wait whose intended phase is not the barrier's
-current or immediately preceding phase, and any deadlock.
+current or immediately preceding phase, any weight slot, A slot or TMEM W buffer
+rewritten while a warp or an MMA still reads it, and any deadlock.
 
 Layout modelled (as in csrc/gemm_tc.cu): a weight ring wfull[s] / wempty[s] (a slot is
 released by the warps that read it, once they have read it) and an A ring afull[s] /
@@ -41,11 +42,13 @@ class Bar:
 
 
 def simulate(kNMI, NWG, T, kps, SW, SA, nkb, rng, interleave, per_party=True,
-             w_readers=None, one_producer=None):
+             w_readers=None, one_producer=None, tempty_wait=True):
     """w_readers: arrivals that release a weight slot (default: the kernel's count, one
     per warp that reads the slot's blocks).  one_producer: one agent streams both rings
     (the kernel's choice for two blocks per stage, i.e. decode tiles), always issuing the
-    copy whose slot is released first."""
+    copy whose slot is released first.  tempty_wait=False drops the dequant warps' wait
+    for a W buffer's previous MMAs (for the sensitivity test of the W-buffer race
+    check)."""
     if one_producer is None:
         one_producer = kps == 2
     nst = (nkb + kps - 1) // kps
@@ -61,7 +64,7 @@ def simulate(kNMI, NWG, T, kps, SW, SA, nkb, rng, interleave, per_party=True,
     tempty = [[Bar(1) for _ in range(T)] for _ in range(n_eparty)]
     events, cnt, errors = [], itertools.count(), []
     # readers of each slot right now: a copy into a slot while someone reads it is a race
-    reading = {"w": [0] * SW, "a": [0] * SA}
+    reading = {"w": [0] * SW, "a": [0] * SA, "t": [0] * T}
 
     def at(t, f):
         heapq.heappush(events, (t, next(cnt), f))
@@ -101,11 +104,12 @@ def simulate(kNMI, NWG, T, kps, SW, SA, nkb, rng, interleave, per_party=True,
                 yield ("wait", wfull[p % SW], p // SW)
                 last_p = p
             t = i % T
-            if i >= T:
+            if i >= T and tempty_wait:
                 party = (w if interleave else 0) if per_party else 0
                 q = seen[t] if per_party else i // T - 1
                 yield ("wait", tempty[party][t], q)
                 seen[t] += 1
+            yield ("write", "t", t)  # the unpack stores into W buffer t
             yield ("read", "w", p % SW, +1)
             yield ("delay", rng.uniform(0.05, 0.8))
             yield ("read", "w", p % SW, -1)
@@ -191,9 +195,11 @@ def simulate(kNMI, NWG, T, kps, SW, SA, nkb, rng, interleave, per_party=True,
                 fin = max(now, mma_free[k]) + rng.uniform(0.05, 0.8)
                 mma_free[k] = fin
                 reading["a"][p % SA] += 1  # the MMA reads its A stage until it completes
+                reading["t"][i % T] += 1   # and its W buffer
 
                 def done(n, i=i, p=p, release=release):
                     reading["a"][p % SA] -= 1
+                    reading["t"][i % T] -= 1
                     party = ((i + T) % NWG if interleave else 0) if per_party else 0
                     tempty[party][i % T].arrive()
                     if release:
@@ -351,3 +357,19 @@ def test_split_k_exit_waits_for_every_push():
             late = trial % ranks
             assert exchange_model(ranks, random.Random(trial), True, late_rank=late) == 0
     assert sum(exchange_model(3, random.Random(t), False, late_rank=0) for t in range(20)) > 0
+
+
+
+def test_model_catches_a_w_buffer_rewritten_under_its_mma():
+    """Sensitivity of the W-buffer race check: if the dequant warps did not wait for the
+    MMAs that last read a W buffer before unpacking the next block into it, they would
+    overwrite operands an MMA still reads; the model must flag that, and must not with
+    the kernel's wait."""
+    hits = clean = 0
+    for trial in range(30):
+        e = simulate(2, 2, 3, 2, 4, 4, 16, random.Random(trial), True, one_producer=True,
+                     tempty_wait=False)
+        hits += e is not None and "race: t" in e
+        clean += simulate(2, 2, 3, 2, 4, 4, 16, random.Random(trial), True,
+                          one_producer=True) is not None
+    assert hits > 0 and clean == 0, (hits, clean)
