@@ -169,3 +169,34 @@ def test_large_tile_fused_epilogue(tile_m, act, with_res):
     out, bo, _ = oracle.epilogue(yd, bb, bias, res, act, c.M, c.N, c.dtype)
     bad, first, worst = oracle.check(to_host_u16(Y), out, bo, c.dtype)
     assert bad == 0, (bad, first, worst)
+
+
+@pytest.mark.parametrize("M,N,K,split_k", [(40, 16000, 640, 1), (64, 8192, 1024, 2)],
+                         ids=["no_split_staged_store", "split2_owner_reduction"])
+@pytest.mark.parametrize("act,with_res", [(w4.W4A16_ACT_SILU, True), (w4.W4A16_ACT_RELU, False)])
+def test_64_row_tiles_alone_fused_epilogue(M, N, K, split_k, act, with_res):
+    """64-row tiles alone on an SM (four whole-block groups, two issuers) with a fused
+    bias, activation and in-place residual: through the staged 16-byte store without
+    split-K and through the owner's reduction with it; every element against the
+    oracle's fused epilogue."""
+    import numpy as np
+    import oracle
+    from gpu_util import to_dev, to_host_u16
+    c = si.make_case(M, N, K, 64, BF16, seed=M + split_k + act, asym=True)
+    p = w4.w4a16_gemm_plan(M, N, K, 64, BF16, kernel=w4.W4A16_KERNEL_TC, tile_m=64,
+                           split_k=split_k)
+    if torch.cuda.get_device_properties(0).multi_processor_count >= 132:
+        assert p["whole_blocks"] and p["groups"] == 4, p
+    rng = np.random.default_rng(act + M)
+    bias = oracle.encode(rng.normal(size=c.N), c.dtype)
+    res = oracle.encode(rng.normal(size=(c.M, c.N)), c.dtype) if with_res else None
+    Y = to_dev(res) if with_res else torch.empty((c.M, c.N), dtype=torch.int16, device="cuda")
+    w4.w4a16_gemm_epilogue(to_dev(c.A), repack_case(c), c.M, c.N, c.K, c.group, c.dtype,
+                           to_dev(bias), Y if with_res else None, act, Y,
+                           kernel=w4.W4A16_KERNEL_TC, tile_m=64, split_k=split_k)
+    assert w4.w4a16_get_device_status() == 0
+    wd = oracle.dequant(c.qweight, c.scales, c.qzeros, c.N, c.K, c.group, c.dtype)
+    yd, bb, _ = oracle.gemm(c.A, wd, c.M, c.N, c.K, c.dtype)
+    out, bo, _ = oracle.epilogue(yd, bb, bias, res, act, c.M, c.N, c.dtype)
+    bad, first, worst = oracle.check(to_host_u16(Y), out, bo, c.dtype)
+    assert bad == 0, (bad, first, worst)

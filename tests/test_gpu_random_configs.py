@@ -124,3 +124,55 @@ def test_random_simt_configuration(cfg):
     assert w4.w4a16_gemm_plan(c.M, c.N, c.K, c.group, c.dtype, **ex)["kernel"] == \
         w4.W4A16_KERNEL_SIMT
     assert_parity_full(c, run_gemm(c, repack_case(c), **ex))
+
+
+def _alone64_configs(n=12, seed=404):
+    """Shapes whose 64-row tiles run alone on an SM: 64 or more channel tiles, so that one
+    CTA per SM (with the K slices that fit) fills most of a 152-SM GPU."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        group = int(rng.choice([32, 64, 128]))
+        out.append(dict(M=int(rng.integers(33, 65)), N=128 * int(rng.integers(61, 76)) - 8 * int(rng.integers(0, 15)),
+                        K=group * int(rng.integers(1, max(2, 1536 // group))), group=group,
+                        dtype=int(rng.integers(0, 2)), asym=bool(rng.integers(0, 2)),
+                        split_k=int(rng.choice([0, 2])), stages=int(rng.choice([0, 2, 4, 6])),
+                        epi=int(rng.choice([0, 0, 2])), seed=int(rng.integers(0, 1 << 20))))
+    return out
+
+
+ALONE64 = _alone64_configs()
+
+
+@pytest.mark.parametrize("cfg", ALONE64, ids=[
+    "M{M}_N{N}_K{K}_g{group}_{dt}_s{split_k}_a{stages}_e{epi}".format(
+        dt="bf16" if c["dtype"] else "fp16", **c) for c in ALONE64])
+def test_random_64_row_tiles_alone(cfg):
+    """64-row tiles with four whole-block warpgroups over random ragged shapes, K slices,
+    A ring depths and (e2) a fused bias + SiLU + in-place residual."""
+    c = si.make_case(cfg["M"], cfg["N"], cfg["K"], cfg["group"], cfg["dtype"],
+                     seed=cfg["seed"], asym=cfg["asym"])
+    split = min(cfg["split_k"], -(-c.K // 128)) if cfg["split_k"] else 0
+    ex = dict(kernel=w4.W4A16_KERNEL_TC, tile_m=64, split_k=split, stages=cfg["stages"])
+    try:
+        w4.w4a16_gemm_plan(c.M, c.N, c.K, c.group, c.dtype, **ex)
+    except w4.W4A16Error as e:
+        assert e.status == w4.W4A16_ERR_UNSUPPORTED
+        pytest.skip("refused by the host")
+    if cfg["epi"] == 0:
+        assert_parity_full(c, run_gemm(c, repack_case(c), **ex))
+        return
+    import oracle
+    from gpu_util import to_dev, to_host_u16
+    rng = np.random.default_rng(cfg["seed"])
+    bias = oracle.encode(rng.normal(size=c.N), c.dtype)
+    res = oracle.encode(rng.normal(size=(c.M, c.N)), c.dtype)
+    Y = to_dev(res)
+    w4.w4a16_gemm_epilogue(to_dev(c.A), repack_case(c), c.M, c.N, c.K, c.group, c.dtype,
+                           to_dev(bias), Y, w4.W4A16_ACT_SILU, Y, **ex)
+    assert w4.w4a16_get_device_status() == 0
+    wd = oracle.dequant(c.qweight, c.scales, c.qzeros, c.N, c.K, c.group, c.dtype)
+    yd, bb, _ = oracle.gemm(c.A, wd, c.M, c.N, c.K, c.dtype)
+    out, bo, _ = oracle.epilogue(yd, bb, bias, res, w4.W4A16_ACT_SILU, c.M, c.N, c.dtype)
+    bad, first, worst = oracle.check(to_host_u16(Y), out, bo, c.dtype)
+    assert bad == 0, (bad, first, worst)
