@@ -12,6 +12,14 @@ Canonical input format (the user-facing layout, before the library's repack):
            None means symmetric weights, zero = 8.
   cscale   optional per-channel factor, dtype bits uint16 [N].
 
+W4A8 canonical inputs (make_w4a8_case; groups of 128 along K):
+  A        activations, dtype bits uint16 [M, K] (quantised to int8 by the library).
+  qweight  uint32 [N, K/8], 4-bit codes in the same nibble order as above.
+  s_u8     uint8 [N, K/128], the group's integer step, 1..16.
+  a        uint8 [N, K/128], the group's offset, drawn in 0 .. 255 - 15 s_u8 (the range in
+           which every code keeps its value inside a byte).
+  s_w      float32 [N], the per-channel scale.
+
 Recipe (one independent PCG64 stream per tensor, keyed by (seed, tensor id)):
   A ~ N(0, 1) drawn in float64; optional outlier columns (a fraction of K, chosen
   without replacement) are multiplied by a factor; then rounded to float32 and to the
@@ -30,6 +38,7 @@ BF16 = 1
 DTYPE_NAMES = {FP16: "fp16", BF16: "bf16"}
 
 _STREAM_A, _STREAM_Q, _STREAM_Z, _STREAM_S, _STREAM_OUT, _STREAM_C = 1, 2, 3, 4, 5, 6
+_STREAM_STEP, _STREAM_OFF, _STREAM_SW = 7, 8, 9
 
 
 def _rng(seed: int, stream: int) -> np.random.Generator:
@@ -83,6 +92,47 @@ def make_case(M: int, N: int, K: int, group: int, dtype: int = FP16, seed: int =
         cscale = to_dtype_bits(_rng(seed, _STREAM_C).uniform(*channel_scale, size=N), dtype)
     return Case(M, N, K, group, dtype, A, qweight, scales, qzeros, cscale,
                 meta={"seed": seed, "outlier_cols": cols})
+
+
+@dataclass
+class W4A8Case:
+    M: int
+    N: int
+    K: int
+    dtype: int
+    A: np.ndarray
+    qweight: np.ndarray
+    s_u8: np.ndarray
+    a: np.ndarray
+    s_w: np.ndarray
+    meta: dict = field(default_factory=dict)
+
+
+def make_w4a8_case(M: int, N: int, K: int, dtype: int = FP16, seed: int = 0, *,
+                   zero_rows: tuple = (), sw_lo: float = 5e-5, sw_hi: float = 2e-4,
+                   steps: tuple[int, int] = (1, 16)) -> W4A8Case:
+    """W4A8 inputs: A ~ N(0, 1) (rows listed in zero_rows all zero), uniform 4-bit codes,
+    per group a step uniform in `steps` and an offset uniform in 0 .. 255 - 15 step,
+    per-channel scales ~ U[sw_lo, sw_hi] in float32."""
+    assert K % 128 == 0 and N % 8 == 0
+    G = K // 128
+    a = _rng(seed, _STREAM_A).standard_normal((M, K))
+    for m in zero_rows:
+        a[m, :] = 0.0
+    A = to_dtype_bits(a, dtype)
+    qweight = _rng(seed, _STREAM_Q).integers(0, 1 << 32, size=(N, K // 8), dtype=np.uint32)
+    s_u8 = _rng(seed, _STREAM_STEP).integers(steps[0], steps[1] + 1, size=(N, G)).astype(np.uint8)
+    hi = 255 - 15 * s_u8.astype(np.int64)  # inclusive upper end of the offset
+    off = np.floor(_rng(seed, _STREAM_OFF).uniform(size=(N, G)) * (hi + 1)).astype(np.int64)
+    off = np.minimum(off, hi).astype(np.uint8)
+    s_w = _rng(seed, _STREAM_SW).uniform(sw_lo, sw_hi, size=N).astype(np.float32)
+    return W4A8Case(M, N, K, dtype, A, qweight, s_u8, off, s_w, meta={"seed": seed})
+
+
+def w4a8_algorithmic_bytes(M: int, N: int, K: int) -> int:
+    """Bytes a W4A8 GEMM moves at least once: codes, steps and offsets, channel scales,
+    int8 A with its row scales, and Y (16-bit)."""
+    return K * N // 2 + 2 * (K // 128) * N + 4 * N + M * K + 4 * M + 2 * M * N
 
 
 # ---- the workloads -------------------------------------------------------------------
