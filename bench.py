@@ -123,6 +123,9 @@ def parse():
                          "groups of 128; unrounded weights)")
     ap.add_argument("--shape", action="append", default=[],
                     help="restrict the workload to this shape tag (repeatable; profiling)")
+    ap.add_argument("--w4a8-only", action="store_true",
+                    help="time only the W4A8 decode workload (w4a8_ffn70b_decode_bf16) and "
+                         "print its line")
     ap.add_argument("--no-extra-workloads", dest="extra_workloads", action="store_false",
                     help="time only --workload (by default the 70B-shaped decode, the batch "
                          "transition and the prefill workloads are timed beside it)")
@@ -703,6 +706,185 @@ def measure_workload(a, w4, device, stream, sampler, workload, shapes, ex, steps
     return m
 
 
+def measure_w4a8(a, w4, device, stream, sampler, workload, steps, warmup):
+    """The W4A8 (LiquidQuant) decode path: per shape one w4a8_quantize_act and one
+    w4a8_gemm per step.  The step's value is its algorithmic bytes (the GEMM's: codes,
+    steps and offsets, channel scales, int8 A with its row scales, Y; plus the quantiser's
+    read of A and write of the int8 A and row scales) over the step time; the roofline is
+    that of the GEMM kernel over its own algorithmic bytes and launch time."""
+    import torch
+
+    ws, rank, _ = dist_info()
+    shapes = si.W4A8_WORKLOADS[workload]
+    cases = [si.make_w4a8_case(**p) for p in shapes]
+
+    def dev(x):
+        v = x.view(np.int16) if x.dtype == np.uint16 else (
+            x.view(np.int32) if x.dtype == np.uint32 else x)
+        return torch.from_numpy(np.ascontiguousarray(v)).to(device)
+
+    gemm_bytes = [si.w4a8_algorithmic_bytes(c.M, c.N, c.K) for c in cases]
+    quant_bytes = [2 * c.M * c.K + c.M * c.K + 4 * c.M for c in cases]
+    step_bytes = sum(gemm_bytes) + sum(quant_bytes)
+    shape_packed = [w4.w4a8_packed_bytes(c.N, c.K) for c in cases]
+    copies = max(2, -(-3 * L2_BYTES // max(1, sum(shape_packed))))
+    bufs = []
+    for c, nb in zip(cases, shape_packed):
+        first = torch.empty(nb, dtype=torch.uint8, device=device)
+        w4.w4a8_repack(dev(c.qweight), dev(c.s_u8), dev(c.a), dev(c.s_w), c.N, c.K, first)
+        reps = [first] + [first.clone() for _ in range(copies - 1)]
+        A = dev(c.A)
+        A_i8 = torch.empty((c.M, c.K), dtype=torch.int8, device=device)
+        s_a = torch.empty(c.M, dtype=torch.float32, device=device)
+        Y = torch.empty((c.M, c.N), dtype=torch.int16, device=device)
+        bufs.append((c, reps, A, A_i8, s_a, Y))
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"{workload}: device status after repack: {w4.status_string(st)}")
+
+    def launch_step(i):
+        for c, reps, A, A_i8, s_a, Y in bufs:
+            w4.w4a8_quantize_act(A, c.M, c.K, c.dtype, A_i8, s_a, stream)
+            w4.w4a8_gemm(A_i8, s_a, reps[i % copies], c.M, c.N, c.K, c.dtype, Y, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, warmup)):
+            launch_step(i)
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"{workload}: device status after warm-up: {w4.status_string(st)}")
+
+    # per-shape pass: back-to-back GEMM launches of one shape in a graph, rotating over at
+    # least 3 x L2 of that shape's own weight copies
+    per_shape_us = []
+    for j, (c, reps, A, A_i8, s_a, Y) in enumerate(bufs):
+        cs = max(3, -(-3 * L2_BYTES // max(1, shape_packed[j])))
+        own = list(reps[:cs]) + [reps[0].clone() for _ in range(cs - len(reps))]
+        nl = max(20, cs)
+        gj = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gj, stream=stream):
+                for i in range(nl):
+                    w4.w4a8_gemm(A_i8, s_a, own[i % cs], c.M, c.N, c.K, c.dtype, Y, stream)
+            gj.replay()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for _ in range(3):
+                gj.replay()
+            f1.record(stream)
+        stream.synchronize()
+        per_shape_us.append(f0.elapsed_time(f1) * 1e3 / (3 * nl))
+        del gj, own
+
+    G = max(1, min(a.graph_steps, steps))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for g in range(G):
+                launch_step(g)
+        graph.replay()
+    stream.synchronize()
+    full_replays, tail = steps // G, steps % G
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(full_replays):
+            graph.replay()
+        for i in range(tail):
+            launch_step(i)
+        e1.record(stream)
+    stream.synchronize()
+    barrier(device)
+    t_wall1 = time.time()
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"{workload}: device status after timed region: {w4.status_string(st)}")
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), device)
+    del graph
+
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    dom_bytes = sum(gemm_bytes) / len(gemm_bytes)
+    dom_s = sum(per_shape_us) * 1e-6 / len(per_shape_us)
+    achieved = dom_bytes / dom_s / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                "kernel": "w4a8_gemm_kernel", "launches_per_step": len(cases),
+                "algorithmic_bytes_per_launch": dom_bytes}
+    value = step_bytes * steps * ws / (elapsed_ms * 1e-3) / 1e12
+
+    # end to end through the public calls: per step one pinned-host copy of all shapes' A
+    # in, the quantiser and the GEMM per shape, one copy of all Y out, on one stream
+    a_sizes = [c.M * c.K for c in cases]
+    y_sizes = [c.M * c.N for c in cases]
+    hostA = torch.cat([torch.from_numpy(np.ascontiguousarray(c.A.view(np.int16)).ravel())
+                       for c in cases]).pin_memory()
+    hostY = torch.empty(sum(y_sizes), dtype=torch.int16).pin_memory()
+    devA = torch.empty(sum(a_sizes), dtype=torch.int16, device=device)
+    devY = torch.empty(sum(y_sizes), dtype=torch.int16, device=device)
+    a_views, y_views, oa, oy = [], [], 0, 0
+    for na, ny in zip(a_sizes, y_sizes):
+        a_views.append(devA[oa:oa + na])
+        y_views.append(devY[oy:oy + ny])
+        oa, oy = oa + na, oy + ny
+
+    def e2e_step(i):
+        devA.copy_(hostA, non_blocking=True)
+        for j, (c, reps, _, A_i8, s_a, _) in enumerate(bufs):
+            w4.w4a8_quantize_act(a_views[j], c.M, c.K, c.dtype, A_i8, s_a, stream)
+            w4.w4a8_gemm(A_i8, s_a, reps[i % copies], c.M, c.N, c.K, c.dtype, y_views[j],
+                         stream)
+        hostY.copy_(devY, non_blocking=True)
+
+    e2e_steps = max(1, min(a.e2e_steps, steps))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+        stream.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        f1.record(stream)
+    stream.synchronize()
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"{workload}: device status after end-to-end region: "
+                         f"{w4.status_string(st)}")
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), device)
+    unit = "TB/s"
+    per_shape = [{"shape": si.w4a8_shape_tag(p), "kernel": "w4a8_gemm_kernel",
+                  "us": round(us, 3), "gbs": round(b / (us * 1e-6) / 1e9, 1),
+                  "hbm_frac": round(b / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+                 for p, us, b in zip(shapes, per_shape_us, gemm_bytes)]
+    out = {
+        "workload": workload, "metric": f"W4A8 GEMM achieved HBM TB/s ({workload})",
+        "value": value, "unit": unit, "ms_per_step": elapsed_ms / steps, "steps": steps,
+        "shapes": len(shapes), "step_bytes": step_bytes, "step_flops": sum(
+            si.flops(c.M, c.N, c.K) for c in cases),
+        "l2": f"inputs larger than L2: {copies} rotating copies of the packed weights "
+              f"({copies * sum(shape_packed) / 2**20:.0f} MiB per rotation)",
+        "roofline": roofline, "per_shape": per_shape,
+        "e2e": {"value": step_bytes * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12, "unit": unit,
+                "h2d_bytes_per_step": 2 * sum(a_sizes), "d2h_bytes_per_step": 2 * sum(y_sizes),
+                "steps": e2e_steps,
+                "note": "per step: one pinned-host copy of all shapes' A in, "
+                        "w4a8_quantize_act + w4a8_gemm per shape, one copy of all Y out, "
+                        "one stream; packed weights resident"},
+        "kernels_per_step": {"w4a8_quantize_kernel": len(cases), "w4a8_gemm_kernel": len(cases)},
+        "gpu_launches": 2 * len(cases) * steps,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "dtype": "int8 products, int32 sums, fp32 scaling",
+        "note": "dp4a on the CUDA cores: sm_103a has no int8 tensor-core MMA"}
+    del bufs, devA, devY, hostA, hostY
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    return out
+
+
 # Workloads timed beside the headline in a default run (M <= 16 decode at 70B scale, the
 # batch transition and prefill: the rest of the metric), each with its own roofline.
 EXTRA_WORKLOADS = ["ffn70b_decode_bf16", "transition_k8192_n8192",
@@ -732,6 +914,24 @@ def run_ours(a):
     sampler.start()
     time.sleep(0.3)
 
+    if a.w4a8_only:
+        name = next(iter(si.W4A8_WORKLOADS))
+        x = measure_w4a8(a, w4, device, stream, sampler, name, a.steps, a.warmup)
+        sampler.stop()
+        if rank == 0:
+            print(json.dumps({
+                "metric": x["metric"], "value": x["value"], "unit": x["unit"], "n_gpus": ws,
+                "steps": a.steps, "warmup": a.warmup, "ms_per_step": x["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "i8", "data": "synthetic",
+                "config": {"workload": name, "shapes": x["shapes"], "step_bytes": x["step_bytes"],
+                           "l2": x["l2"], "parallelism": f"replicas{ws}"},
+                "roofline": x["roofline"], "per_shape": x["per_shape"], "cpu_baseline": None,
+                "e2e": x["e2e"], "kernel": "w4a8_gemm_kernel",
+                "kernels_per_step": x["kernels_per_step"], "gpu_launches": x["gpu_launches"],
+                "clocks": x["clocks"], "note": x["note"]}), flush=True)
+        return
+
     shapes = workload_shapes(a)
     m = measure_workload(a, w4, device, stream, sampler, a.workload, shapes, ex, a.steps,
                          a.warmup, a.epilogue)
@@ -752,6 +952,8 @@ def run_ours(a):
                 "roofline": x.roofline, "per_shape": x.per_shape, "e2e": x.e2e,
                 "kernels_per_step": x.counts, "gpu_launches": x.gpu_launches,
                 "clocks": x.clocks})
+        for name in si.W4A8_WORKLOADS:
+            extra.append(measure_w4a8(a, w4, device, stream, sampler, name, a.steps, a.warmup))
     time.sleep(0.3)
     sampler.stop()
 

@@ -110,13 +110,19 @@ class W4A8Case:
 
 def make_w4a8_case(M: int, N: int, K: int, dtype: int = FP16, seed: int = 0, *,
                    zero_rows: tuple = (), sw_lo: float = 5e-5, sw_hi: float = 2e-4,
-                   steps: tuple[int, int] = (1, 16)) -> W4A8Case:
-    """W4A8 inputs: A ~ N(0, 1) (rows listed in zero_rows all zero), uniform 4-bit codes,
-    per group a step uniform in `steps` and an offset uniform in 0 .. 255 - 15 step,
-    per-channel scales ~ U[sw_lo, sw_hi] in float32."""
+                   steps: tuple[int, int] = (1, 16), outlier_frac: float = 0.0,
+                   outlier_gain: float = 20.0) -> W4A8Case:
+    """W4A8 inputs: A ~ N(0, 1) (rows listed in zero_rows all zero; optional outlier
+    columns as in make_case), uniform 4-bit codes, per group a step uniform in `steps`
+    and an offset uniform in 0 .. 255 - 15 step, per-channel scales ~ U[sw_lo, sw_hi] in
+    float32."""
     assert K % 128 == 0 and N % 8 == 0
     G = K // 128
     a = _rng(seed, _STREAM_A).standard_normal((M, K))
+    if outlier_frac > 0.0:
+        n_out = int(round(outlier_frac * K))
+        cols = np.sort(_rng(seed, _STREAM_OUT).choice(K, size=n_out, replace=False))
+        a[:, cols] *= outlier_gain
     for m in zero_rows:
         a[m, :] = 0.0
     A = to_dtype_bits(a, dtype)
@@ -179,6 +185,22 @@ WORKLOADS = {
     "prefill_m4096_k4096_n11008": [dict(M=4096, N=11008, K=4096, group=128, dtype=FP16,
                                         seed=4, asym=True, s_lo=0.005, s_hi=0.02)],
 }
+
+
+def _w4a8_ffn70b():
+    return [dict(M=m, N=n, K=k, dtype=BF16, seed=2, outlier_frac=0.001, outlier_gain=20.0)
+            for (k, n) in ((8192, 28672), (28672, 8192)) for m in (1, 8, 16)]
+
+
+# W4A8 workloads (make_w4a8_case arguments): the 70B-shaped decode FFN shapes with bf16
+# activations and 0.1% outlier columns x20, M in {1, 8, 16}.
+W4A8_WORKLOADS = {
+    "w4a8_ffn70b_decode_bf16": _w4a8_ffn70b(),
+}
+
+
+def w4a8_shape_tag(p: dict) -> str:
+    return f"W4A8_M{p['M']}_N{p['N']}_K{p['K']}_{DTYPE_NAMES[p['dtype']]}"
 
 
 def shape_tag(p: dict) -> str:

@@ -87,3 +87,44 @@ def test_gemm_host_validation(L):
 def test_timeout_probe_rejects_bad_limits(L):
     assert L.w4a16_debug_timeout_probe(0, None) == w4.W4A16_ERR_INVALID_ARG
     assert L.w4a16_debug_timeout_probe(2_000_000, None) == w4.W4A16_ERR_INVALID_ARG
+
+
+# ---- W4A8 (include/w4a8.h) -------------------------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(32, 128), (4096, 4096), (28672, 8192), (40, 256), (8200, 384)])
+def test_w4a8_packed_bytes_formula(L, N, K):
+    Np = -(-N // 32) * 32
+    assert w4.w4a8_packed_bytes(N, K) == 128 + (Np // 32) * (K // 128) * 2112 + 4 * Np
+
+
+@pytest.mark.parametrize("N,K", [(0, 128), (32, 0), (32, 100), (32, 192), (32, 131072 + 128)])
+def test_w4a8_packed_bytes_unsupported(L, N, K):
+    assert w4.w4a8_packed_bytes(N, K) == 0
+
+
+def test_w4a8_host_validation(L):
+    fake = 1 << 20
+    # repack: nulls, capacity, alignment, shape
+    assert L.w4a8_repack(None, fake, fake, fake, 32, 128, fake, 1 << 20, None) \
+        == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a8_repack(fake, fake, fake, fake, 32, 128, fake, 100, None) \
+        == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a8_repack(fake + 4, fake, fake, fake, 32, 128, fake, 1 << 20, None) \
+        == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a8_repack(fake, fake, fake, fake, 32, 192, fake, 1 << 20, None) \
+        == w4.W4A16_ERR_UNSUPPORTED
+    # quantize: M == 0 is a no-op; dtype, K and alignment are checked first
+    assert L.w4a8_quantize_act(None, 0, 128, 0, None, None, None) == w4.W4A16_OK
+    assert L.w4a8_quantize_act(fake, 2, 128, 5, fake, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a8_quantize_act(fake, 2, 100, 0, fake, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a8_quantize_act(fake + 8, 2, 128, 0, fake, fake, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a8_quantize_act(fake, 2, 128, 0, fake, fake + 2, None) == w4.W4A16_ERR_INVALID_ARG
+    # gemm: M range, shape, pointers
+    assert L.w4a8_gemm(None, None, None, 0, 32, 128, 0, None, None) == w4.W4A16_OK
+    assert L.w4a8_gemm(fake, fake, fake, 17, 32, 128, 0, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a8_gemm(fake, fake, fake, -1, 32, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a8_gemm(fake, fake, fake, 4, 32, 100, 0, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a8_gemm(fake, fake, fake, 4, 32, 128, 3, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.w4a8_gemm(fake + 4, fake, fake, 4, 32, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a8_gemm(fake, fake, fake, 4, 32, 128, 0, fake + 1, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.w4a8_dequant_debug(None, 32, 128, fake, None) == w4.W4A16_ERR_INVALID_ARG

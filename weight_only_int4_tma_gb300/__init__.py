@@ -16,6 +16,7 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libw4a16.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "w4a16.h")
+HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "w4a8.h")]
 
 W4A16_OK = 0
 W4A16_ERR_INVALID_ARG = -1
@@ -91,15 +92,27 @@ def lib() -> ctypes.CDLL:
             L.w4a16_debug_timeout_probe.restype = I
             L.w4a16_debug_splitk_timeout_probe.argtypes = [P, P, I, I, I, I, I, P, U, P]
             L.w4a16_debug_splitk_timeout_probe.restype = I
+            L.w4a8_packed_bytes.argtypes = [I, I]
+            L.w4a8_packed_bytes.restype = Z
+            L.w4a8_repack.argtypes = [P, P, P, P, I, I, P, Z, P]
+            L.w4a8_repack.restype = I
+            L.w4a8_quantize_act.argtypes = [P, I, I, I, P, P, P]
+            L.w4a8_quantize_act.restype = I
+            L.w4a8_gemm.argtypes = [P, P, P, I, I, I, I, P, P]
+            L.w4a8_gemm.restype = I
+            L.w4a8_dequant_debug.argtypes = [P, I, I, P, P]
+            L.w4a8_dequant_debug.restype = I
             _lib = L
     return _lib
 
 
 def header_functions() -> list[str]:
-    """Names of the functions include/w4a16.h declares."""
-    src = open(HEADER).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(w4a16_[a-z_0-9]+)\s*\(", src)))
+    """Names of the functions the public headers (include/w4a16.h, include/w4a8.h) declare."""
+    names = set()
+    for h in HEADERS:
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names.update(re.findall(r"\b(w4a(?:16|8)_[a-z_0-9]+)\s*\(", src))
+    return sorted(names)
 
 
 def status_string(status: int) -> str:
@@ -206,6 +219,33 @@ def w4a16_debug_splitk_timeout_probe(A, packed, M: int, N: int, K: int, group: i
     _check(lib().w4a16_debug_splitk_timeout_probe(_ptr(A), _ptr(packed), M, N, K, group, dtype,
                                                   _ptr(Y), timeout_us, _stream(stream)),
            "w4a16_debug_splitk_timeout_probe")
+
+
+def w4a8_packed_bytes(N: int, K: int) -> int:
+    return int(lib().w4a8_packed_bytes(N, K))
+
+
+def w4a8_repack(qweight, s_u8, a, s_w, N: int, K: int, packed, packed_bytes: int | None = None,
+                stream=None) -> None:
+    if packed_bytes is None:
+        packed_bytes = packed.numel() * packed.element_size()
+    _check(lib().w4a8_repack(_ptr(qweight), _ptr(s_u8), _ptr(a), _ptr(s_w), N, K, _ptr(packed),
+                             packed_bytes, _stream(stream)), "w4a8_repack")
+
+
+def w4a8_quantize_act(A, M: int, K: int, dtype: int, A_i8, s_a, stream=None) -> None:
+    _check(lib().w4a8_quantize_act(_ptr(A), M, K, dtype, _ptr(A_i8), _ptr(s_a),
+                                   _stream(stream)), "w4a8_quantize_act")
+
+
+def w4a8_gemm(A_i8, s_a, packed, M: int, N: int, K: int, dtype: int, Y, stream=None) -> None:
+    _check(lib().w4a8_gemm(_ptr(A_i8), _ptr(s_a), _ptr(packed), M, N, K, dtype, _ptr(Y),
+                           _stream(stream)), "w4a8_gemm")
+
+
+def w4a8_dequant_debug(packed, N: int, K: int, W_out, stream=None) -> None:
+    _check(lib().w4a8_dequant_debug(_ptr(packed), N, K, _ptr(W_out), _stream(stream)),
+           "w4a8_dequant_debug")
 
 
 # ---- torch-friendly helpers (allocation + the calls above) ---------------------------

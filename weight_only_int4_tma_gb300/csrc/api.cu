@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "w4a16.h"
+#include "w4a8.h"
 #include "format.cuh"
 #include "launch.h"
 
@@ -411,6 +412,80 @@ int w4a16_debug_timeout_probe(unsigned int timeout_us, void* stream) {
     if (rc != W4A16_OK) return rc;
     return launch_timeout_probe(*ctx, static_cast<uint64_t>(timeout_us) * 1000ull,
                                 static_cast<cudaStream_t>(stream));
+}
+
+// ---- W4A8 (include/w4a8.h) ------------------------------------------------------------
+
+namespace {
+int w4a8_check_shape(int N, int K) {
+    if (N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
+    if (K % 128 != 0 || K > 131072) return W4A16_ERR_UNSUPPORTED;
+    if ((static_cast<long long>(N) + 31) / 32 * (K / 128) > 0x7FFFFFFFLL) return W4A16_ERR_UNSUPPORTED;
+    return W4A16_OK;
+}
+}  // namespace
+
+size_t w4a8_packed_bytes(int N, int K) {
+    if (w4a8_check_shape(N, K) != W4A16_OK) return 0;
+    return w4a8_blob_bytes(N, K);
+}
+
+int w4a8_repack(const uint32_t* qweight, const uint8_t* s_u8, const uint8_t* a,
+                const float* s_w, int N, int K, void* packed, size_t packed_bytes,
+                void* stream) {
+    if (!qweight || !s_u8 || !a || !s_w || !packed) return W4A16_ERR_INVALID_ARG;
+    int rc = w4a8_check_shape(N, K);
+    if (rc != W4A16_OK) return rc;
+    if (!aligned(qweight, 16) || !aligned(s_w, 4) || !aligned(packed, 16))
+        return W4A16_ERR_INVALID_ARG;
+    if (packed_bytes < w4a8_blob_bytes(N, K)) return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
+    return launch_w4a8_repack(*ctx, qweight, s_u8, a, s_w, N, K, packed,
+                              static_cast<cudaStream_t>(stream));
+}
+
+int w4a8_quantize_act(const void* A, int M, int K, int dtype, int8_t* A_i8, float* s_a,
+                      void* stream) {
+    if (M < 0 || K < 1) return W4A16_ERR_INVALID_ARG;
+    if (dtype != W4A16_FP16 && dtype != W4A16_BF16) return W4A16_ERR_UNSUPPORTED;
+    if (K % 128 != 0 || K > 131072) return W4A16_ERR_UNSUPPORTED;
+    if (M == 0) return W4A16_OK;
+    if (!A || !A_i8 || !s_a) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(A, 16) || !aligned(A_i8, 16) || !aligned(s_a, 4)) return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    int rc = get_ctx(&ctx);
+    if (rc != W4A16_OK) return rc;
+    return launch_w4a8_quantize(*ctx, A, M, K, dtype, A_i8, s_a,
+                                static_cast<cudaStream_t>(stream));
+}
+
+int w4a8_gemm(const int8_t* A_i8, const float* s_a, const void* packed, int M, int N, int K,
+              int dtype, void* Y, void* stream) {
+    if (M < 0) return W4A16_ERR_INVALID_ARG;
+    int rc = w4a8_check_shape(N, K);
+    if (rc != W4A16_OK) return rc;
+    if (dtype != W4A16_FP16 && dtype != W4A16_BF16) return W4A16_ERR_UNSUPPORTED;
+    if (M > 16) return W4A16_ERR_UNSUPPORTED;
+    if (M == 0) return W4A16_OK;
+    if (!A_i8 || !s_a || !packed || !Y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(A_i8, 16) || !aligned(s_a, 4) || !aligned(packed, 16) || !aligned(Y, 2))
+        return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
+    return launch_w4a8_gemm(*ctx, A_i8, s_a, packed, M, N, K, dtype, Y,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int w4a8_dequant_debug(const void* packed, int N, int K, int8_t* W_out, void* stream) {
+    if (!packed || !W_out) return W4A16_ERR_INVALID_ARG;
+    int rc = w4a8_check_shape(N, K);
+    if (rc != W4A16_OK) return rc;
+    if (!aligned(packed, 16) || !aligned(W_out, 16)) return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
+    return launch_w4a8_dequant_debug(*ctx, packed, N, K, W_out,
+                                     static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -56,6 +56,20 @@ int launch_tc_splitk_probe(const DeviceCtx& ctx, const void* A, const void* pack
                            int N, int K, int group, int dtype, void* Y, const GemmPlan& plan,
                            uint64_t timeout_ns, cudaStream_t stream);
 
+// W4A8 path (w4a8.cu): blob size, repack, int8 debug expansion, per-row activation
+// quantisation and the dp4a GEMM (M <= 16; returns -2 beyond).
+size_t w4a8_blob_bytes(int N, int K);
+int launch_w4a8_repack(const DeviceCtx& ctx, const uint32_t* qweight, const uint8_t* s_u8,
+                       const uint8_t* off, const float* s_w, int N, int K, void* packed,
+                       cudaStream_t stream);
+int launch_w4a8_dequant_debug(const DeviceCtx& ctx, const void* packed, int N, int K,
+                              void* W_out, cudaStream_t stream);
+int launch_w4a8_quantize(const DeviceCtx& ctx, const void* A, int M, int K, int dtype,
+                         int8_t* A_i8, float* s_a, cudaStream_t stream);
+int launch_w4a8_gemm(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
+                     const void* packed, int M, int N, int K, int dtype, void* Y,
+                     cudaStream_t stream);
+
 // Rows of A staged per 64-K chunk (8 or 16 for decode tiles, else the tile height).
 int tc_a_rows(int tile_m, int M);
 // 128-K weight blocks per ring stage (one bulk copy each stage).
