@@ -125,7 +125,7 @@ def test_dequant_debug_quantiser_output():
 
 
 @pytest.mark.parametrize("dtype", [si.FP16, si.BF16], ids=["fp16", "bf16"])
-@pytest.mark.parametrize("M,K", [(1, 128), (3, 4096), (16, 8192), (37, 28672)])
+@pytest.mark.parametrize("M,K", [(1, 128), (3, 4096), (16, 8192), (37, 28672), (2, 40960)])
 def test_quantize_act_bitexact(M, K, dtype):
     c = si.make_w4a8_case(M, 32, K, dtype=dtype, seed=7 * M + K,
                           zero_rows=(1,) if M > 1 else ())

@@ -205,28 +205,63 @@ __device__ __forceinline__ float dtype_bits_to_f32(uint32_t b) {
     else return __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(b)));
 }
 
-// One CTA per row m: amax = max |A[m, :]| (exact), s_a = amax / 127 (1 for an all-zero
-// row), A_i8 = rint(A / s_a) clipped to [-127, 127]; division and rounding in fp32,
-// round to nearest even, as the oracle states them.
+// One CTA of kQuantThreads threads per row m: amax = max |A[m, :]| (exact), s_a =
+// amax / 127 (1 for an all-zero row), A_i8 = rint(A / s_a) clipped to [-127, 127];
+// division and rounding in fp32, round to nearest even, as the oracle states them.
+// Rows of up to kQuantThreads * kQuantVec * 8 values are read once into registers (all
+// loads issued before the first is used); longer rows are read twice.
+constexpr int kQuantThreads = 512;
+constexpr int kQuantVec = 8;  // 16-byte pieces per thread held in registers
+
 template <int DT>
-__global__ void __launch_bounds__(kW4a8Threads) w4a8_quantize_kernel(
+__device__ __forceinline__ float amax_piece(uint4 v, float amax) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        amax = fmaxf(amax, fabsf(dtype_bits_to_f32<DT>(w[j] & 0xFFFFu)));
+        amax = fmaxf(amax, fabsf(dtype_bits_to_f32<DT>(w[j] >> 16)));
+    }
+    return amax;
+}
+
+template <int DT>
+__device__ __forceinline__ uint2 quantize_piece(uint4 v, float s) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[2] = {0, 0};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t bits = (w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
+        int q = __float2int_rn(__fdiv_rn(dtype_bits_to_f32<DT>(bits), s));
+        q = max(-127, min(127, q));
+        o[j >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (j & 3));
+    }
+    return make_uint2(o[0], o[1]);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kQuantThreads) w4a8_quantize_kernel(
     const uint16_t* __restrict__ A, int K, int8_t* __restrict__ A_i8, float* __restrict__ s_a) {
-    __shared__ float wmax[kW4a8Warps];
+    __shared__ float wmax[kQuantThreads / 32];
     __shared__ float s_row;
     grid_dep_wait();  // A belongs to the previous kernel until here
     const int m = static_cast<int>(blockIdx.x);
     const int tid = static_cast<int>(threadIdx.x);
     const uint4* row = reinterpret_cast<const uint4*>(A + static_cast<size_t>(m) * K);
+    uint2* out = reinterpret_cast<uint2*>(A_i8 + static_cast<size_t>(m) * K);
     const int nv = K / 8;
+    const bool in_regs = nv <= kQuantThreads * kQuantVec;
+    uint4 v[kQuantVec];
     float amax = 0.0f;
-    for (int i = tid; i < nv; i += kW4a8Threads) {
-        const uint4 v = __ldg(row + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (in_regs) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            amax = fmaxf(amax, fabsf(dtype_bits_to_f32<DT>(w[j] & 0xFFFFu)));
-            amax = fmaxf(amax, fabsf(dtype_bits_to_f32<DT>(w[j] >> 16)));
+        for (int j = 0; j < kQuantVec; ++j) {
+            const int i = tid + j * kQuantThreads;
+            v[j] = i < nv ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
         }
+#pragma unroll
+        for (int j = 0; j < kQuantVec; ++j) amax = amax_piece<DT>(v[j], amax);
+    } else {
+        for (int i = tid; i < nv; i += kQuantThreads) amax = amax_piece<DT>(__ldg(row + i), amax);
     }
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
@@ -234,7 +269,7 @@ __global__ void __launch_bounds__(kW4a8Threads) w4a8_quantize_kernel(
     __syncthreads();
     if (tid == 0) {
         float mx = wmax[0];
-        for (int w = 1; w < kW4a8Warps; ++w) mx = fmaxf(mx, wmax[w]);
+        for (int w = 1; w < kQuantThreads / 32; ++w) mx = fmaxf(mx, wmax[w]);
         const float s = mx > 0.0f ? __fdiv_rn(mx, 127.0f) : 1.0f;
         s_row = s;
         s_a[m] = s;
@@ -242,31 +277,42 @@ __global__ void __launch_bounds__(kW4a8Threads) w4a8_quantize_kernel(
     __syncthreads();
     grid_dep_launch();
     const float s = s_row;
-    uint2* out = reinterpret_cast<uint2*>(A_i8 + static_cast<size_t>(m) * K);
-    for (int i = tid; i < nv; i += kW4a8Threads) {
-        const uint4 v = __ldg(row + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t o[2] = {0, 0};
+    if (in_regs) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t bits = (w[j >> 1] >> (16 * (j & 1))) & 0xFFFFu;
-            int q = __float2int_rn(__fdiv_rn(dtype_bits_to_f32<DT>(bits), s));
-            q = max(-127, min(127, q));
-            o[j >> 2] |= (static_cast<uint32_t>(q) & 0xFFu) << (8 * (j & 3));
+        for (int j = 0; j < kQuantVec; ++j) {
+            const int i = tid + j * kQuantThreads;
+            if (i < nv) out[i] = quantize_piece<DT>(v[j], s);
         }
-        out[i] = make_uint2(o[0], o[1]);
+    } else {
+        for (int i = tid; i < nv; i += kQuantThreads) out[i] = quantize_piece<DT>(__ldg(row + i), s);
     }
 }
 
 // ---- the GEMM ----------------------------------------------------------------------
 
-// acc[m][*] += the int8 products of one 128-K block of this thread's channel with
-// activation rows m < M.  w: the block's four 16-byte pieces; meta: step in bits 0..7,
-// offset in bits 8..15; a_blk: row 0 of the int8 activations at the block's first K value.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Accumulator chains per activation row: two independent dp4a chains where there are
+// only one or two rows, one where the rows already give enough independent chains.
 template <int MT>
+constexpr int w4a8_chains() { return MT <= 2 ? 2 : 1; }
+
+// acc[m][*] += the int8 products of one 128-K block of this thread's channel with the
+// MT activation rows staged in shared memory (rows past M hold zeros).  w: the block's
+// four 16-byte pieces; meta: step in bits 0..7, offset in bits 8..15; a_s: row 0 of the
+// block's int8 activations, row m at + m * kRow bytes.
+template <int MT, uint32_t kRow>
 __device__ __forceinline__ void w4a8_block(const uint4 (&w)[4], uint32_t meta,
-                                           const int8_t* __restrict__ a_blk, int K, int M,
-                                           int (&acc)[MT][2]) {
+                                           const uint8_t* a_s,
+                                           int (&acc)[MT][w4a8_chains<MT>()]) {
+    constexpr int C = w4a8_chains<MT>();
     const uint32_t s = meta & 0xFFu;
     const uint32_t add = ((meta >> 8) & 0xFFu) * 0x01010101u;
 #pragma unroll
@@ -280,22 +326,12 @@ __device__ __forceinline__ void w4a8_block(const uint4 (&w)[4], uint32_t meta,
         }
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            if (m < M) {
-                const uint4* ap =
-                    reinterpret_cast<const uint4*>(a_blk + static_cast<size_t>(m) * K + 32 * p);
-                const uint4 a0 = __ldg(ap), a1 = __ldg(ap + 1);
-                int t0 = acc[m][0], t1 = acc[m][1];
-                t0 = __dp4a(wq[0], static_cast<int>(a0.x), t0);
-                t1 = __dp4a(wq[1], static_cast<int>(a0.y), t1);
-                t0 = __dp4a(wq[2], static_cast<int>(a0.z), t0);
-                t1 = __dp4a(wq[3], static_cast<int>(a0.w), t1);
-                t0 = __dp4a(wq[4], static_cast<int>(a1.x), t0);
-                t1 = __dp4a(wq[5], static_cast<int>(a1.y), t1);
-                t0 = __dp4a(wq[6], static_cast<int>(a1.z), t0);
-                t1 = __dp4a(wq[7], static_cast<int>(a1.w), t1);
-                acc[m][0] = t0;
-                acc[m][1] = t1;
-            }
+            const uint4* ap = reinterpret_cast<const uint4*>(a_s + m * kRow + 32 * p);
+            const uint4 a0 = ap[0], a1 = ap[1];
+            const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                acc[m][i % C] = __dp4a(wq[i], static_cast<int>(av[i]), acc[m][i % C]);
         }
     }
 }
@@ -306,22 +342,34 @@ __device__ __forceinline__ uint16_t w4a8_f32_to_dtype(float v) {
     else return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
+// Dynamic shared memory of one GEMM CTA: two buffers of int8 activations, each MT rows
+// x (K slots x 128) values (the activations of one round of blocks).
+__host__ __device__ constexpr uint32_t w4a8_smem_bytes(int MT, int ROWS) {
+    return 2u * MT * (kW4a8Warps * (32 / ROWS)) * kW4a8Group;
+}
+
 // Work split.  A CTA owns ROWS (16 or 32) consecutive output channels over the whole K
 // range: thread lane % ROWS is the channel, and the 256 / ROWS K slots (ROWS lanes each)
-// take the 128-K blocks slot, slot + slots, ...  Each thread keeps two blocks of its
-// channel in flight in registers (loads of the next but one block are issued before the
-// current one is multiplied).  The slots' int32 partials are summed in shared memory;
-// the sum is exact, so the slot order does not matter.  Epilogue per output element:
+// take the 128-K blocks slot, slot + slots, ...: round r of the CTA is blocks
+// r * slots .. r * slots + slots - 1, one per slot.  Each thread keeps the weights of
+// two rounds in flight in registers (the loads of round r + 2 are issued as soon as
+// round r is multiplied); the int8 activations of a round are staged in shared memory
+// by the whole CTA with cp.async, one round ahead, so that the dp4a chains read them at
+// shared-memory latency.  The slots' int32 partials are summed in shared memory; the
+// sum is exact, so the slot order does not matter.  Epilogue per output element:
 // fp32(acc) * s_a[m] * s_w[n], two fp32 multiplies rounded to nearest even, then one
 // rounding to the output dtype.
 template <int MT, int DT, int ROWS>
-__global__ void __launch_bounds__(kW4a8Threads) w4a8_gemm_kernel(
+__global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : (MT == 2 ? 3 : 2)) w4a8_gemm_kernel(
     const int8_t* __restrict__ A_i8, const float* __restrict__ s_a,
     const uint8_t* __restrict__ packed, uint16_t* __restrict__ Y, int* status, int M, int N,
     int K) {
     constexpr int kSub = 32 / ROWS;
     constexpr int kSlots = kW4a8Warps * kSub;
-    __shared__ int red[kSlots][MT][ROWS];
+    constexpr int C = w4a8_chains<MT>();
+    constexpr uint32_t kRow = kSlots * kW4a8Group;  // bytes of one activation row per round
+    constexpr uint32_t kBuf = MT * kRow;
+    extern __shared__ __align__(16) uint8_t a_smem[];
     __shared__ int s_ok;
     const int tid = static_cast<int>(threadIdx.x);
     const int lane = tid & 31;
@@ -340,6 +388,7 @@ __global__ void __launch_bounds__(kW4a8Threads) w4a8_gemm_kernel(
     if (tid == 0) grid_dep_launch();
 
     const int kblocks = K / kW4a8Group;
+    const int rounds = (kblocks + kSlots - 1) / kSlots;
     const uint8_t* tile = packed + 128 +
                           static_cast<size_t>(n0 / kW4a8TileN) * kblocks * kW4a8BlockBytes;
     auto load = [&](int kb, uint4 (&w)[4], uint32_t& meta) {
@@ -348,27 +397,70 @@ __global__ void __launch_bounds__(kW4a8Threads) w4a8_gemm_kernel(
         for (int p = 0; p < 4; ++p) w[p] = ld_stream_v4(blk + p * 512 + r * 16);
         meta = ld_stream_u32(blk + kW4a8CodeBytes + (r & ~1) * 2) >> ((r & 1) * 16);
     };
+    const uint32_t smem = smem_addr(a_smem);
+    // The activations of round rr into buffer rr & 1: rows m < M, 16 bytes per copy
+    // (pieces past K, in the last round only, are skipped: no block reads them).
+    auto stage = [&](int rr) {
+        constexpr int kPieces = static_cast<int>(kRow / 16);
+        const int k0 = rr * static_cast<int>(kRow);
+        const uint32_t buf = smem + (rr & 1) * kBuf;
+        for (int e = tid; e < M * kPieces; e += kW4a8Threads) {
+            const int m = e / kPieces, c = e % kPieces;
+            if (k0 + c * 16 < K)
+                cp_async16(buf + m * kRow + c * 16, A_i8 + static_cast<size_t>(m) * K + k0 + c * 16);
+        }
+    };
+    // Rows M..MT-1 of both buffers are zero for the whole kernel (every block multiplies
+    // all MT rows; those products are 0 and their sums are never stored).
+    for (int e = tid; e < (MT - M) * static_cast<int>(kRow / 16) * 2; e += kW4a8Threads) {
+        const int per_buf = (MT - M) * static_cast<int>(kRow / 16);
+        const int bsel = e / per_buf, rem = e % per_buf;
+        const int m = M + rem / static_cast<int>(kRow / 16), c = rem % static_cast<int>(kRow / 16);
+        *reinterpret_cast<uint4*>(a_smem + bsel * kBuf + m * kRow + c * 16) = make_uint4(0, 0, 0, 0);
+    }
 
-    int acc[MT][2];
+    int acc[MT][C];
 #pragma unroll
-    for (int m = 0; m < MT; ++m) acc[m][0] = acc[m][1] = 0;
+    for (int m = 0; m < MT; ++m)
+#pragma unroll
+        for (int c = 0; c < C; ++c) acc[m][c] = 0;
     uint4 wa[4], wb[4];
     uint32_t ma = 0, mb = 0;
-    // The packed weights do not depend on the previous kernel: the first two blocks are
+    // The packed weights do not depend on the previous kernel: the first two rounds are
     // requested before the dependency wait.
     if (slot < kblocks) load(slot, wa, ma);
     if (slot + kSlots < kblocks) load(slot + kSlots, wb, mb);
     grid_dep_wait();  // A_i8 and s_a (and Y) belong to the previous kernel until here
-    for (int kb = slot; kb < kblocks; kb += 2 * kSlots) {
-        w4a8_block<MT>(wa, ma, A_i8 + kb * kW4a8Group, K, M, acc);
-        if (kb + 2 * kSlots < kblocks) load(kb + 2 * kSlots, wa, ma);
-        if (kb + kSlots < kblocks) {
-            w4a8_block<MT>(wb, mb, A_i8 + (kb + kSlots) * kW4a8Group, K, M, acc);
-            if (kb + 3 * kSlots < kblocks) load(kb + 3 * kSlots, wb, mb);
+    stage(0);
+    cp_async_commit();
+    for (int rr = 0; rr < rounds; ++rr) {
+        if (rr + 1 < rounds) stage(rr + 1);
+        cp_async_commit();      // (an empty group in the last round)
+        cp_async_wait<1>();     // this thread's copies of round rr have landed ...
+        __syncthreads();        // ... and every other thread's
+        const int kb = rr * kSlots + slot;
+        if (kb < kblocks) {
+            const uint8_t* a_s = a_smem + (rr & 1) * kBuf + slot * kW4a8Group;
+            if (rr & 1) {
+                w4a8_block<MT, kRow>(wb, mb, a_s, acc);
+                if (kb + 2 * kSlots < kblocks) load(kb + 2 * kSlots, wb, mb);
+            } else {
+                w4a8_block<MT, kRow>(wa, ma, a_s, acc);
+                if (kb + 2 * kSlots < kblocks) load(kb + 2 * kSlots, wa, ma);
+            }
         }
+        __syncthreads();        // buffer rr & 1 is free for round rr + 2
     }
+    cp_async_wait<0>();
+    // The activation buffers are reused for the slots' partials: red[slot][m][channel].
+    int* red = reinterpret_cast<int*>(a_smem);
 #pragma unroll
-    for (int m = 0; m < MT; ++m) red[slot][m][rl] = acc[m][0] + acc[m][1];
+    for (int m = 0; m < MT; ++m) {
+        int t = acc[m][0];
+#pragma unroll
+        for (int c = 1; c < C; ++c) t += acc[m][c];
+        red[(slot * MT + m) * ROWS + rl] = t;
+    }
     __syncthreads();
     const float* sw = reinterpret_cast<const float*>(packed + w4a8_sw_offset(N, K));
     for (int e = tid; e < MT * ROWS; e += kW4a8Threads) {
@@ -377,7 +469,7 @@ __global__ void __launch_bounds__(kW4a8Threads) w4a8_gemm_kernel(
         if (m < M && n < N) {
             int sum = 0;
 #pragma unroll
-            for (int q = 0; q < kSlots; ++q) sum += red[q][m][jr];
+            for (int q = 0; q < kSlots; ++q) sum += red[(q * MT + m) * ROWS + jr];
             float y = __int2float_rn(sum);
             y = __fmul_rn(y, s_a[m]);
             y = __fmul_rn(y, sw[n]);
@@ -389,35 +481,82 @@ __global__ void __launch_bounds__(kW4a8Threads) w4a8_gemm_kernel(
 template <int MT, int DT, int ROWS>
 int launch_w4a8_instance(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
                          const void* packed, int M, int N, int K, void* Y, cudaStream_t stream) {
+    auto kern = w4a8_gemm_kernel<MT, DT, ROWS>;
+    constexpr uint32_t smem = w4a8_smem_bytes(MT, ROWS);
+    static int configured_device = -1;  // attribute set once per device and instance
+    if (configured_device != ctx.device) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess)
+            return -3;
+        configured_device = ctx.device;
+    }
     const int np = w4a8_tiles(N) * kW4a8TileN;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(np / ROWS), 1, 1);
     cfg.blockDim = dim3(kW4a8Threads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, w4a8_gemm_kernel<MT, DT, ROWS>, A_i8, s_a,
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, A_i8, s_a,
                                              static_cast<const uint8_t*>(packed),
                                              static_cast<uint16_t*>(Y), ctx.status, M, N, K);
     return e == cudaSuccess ? 0 : -3;
+}
+
+// CTAs of one instance resident per SM (queried once per device).
+template <int MT, int DT, int ROWS>
+int w4a8_occupancy(const DeviceCtx& ctx) {
+    static int device = -1, occ = 0;
+    if (device != ctx.device) {
+        auto kern = w4a8_gemm_kernel<MT, DT, ROWS>;
+        constexpr uint32_t smem = w4a8_smem_bytes(MT, ROWS);
+        int o = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem)) != cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kW4a8Threads, smem) !=
+                cudaSuccess)
+            return 0;
+        occ = o;
+        device = ctx.device;
+    }
+    return occ;
+}
+
+// Fraction of the CTA slots of the GPU that the launch's waves keep busy.
+inline double w4a8_wave_fill(int units, int per_sm, int sms) {
+    if (per_sm < 1) return 0.0;
+    const long long slots = static_cast<long long>(per_sm) * sms;
+    const long long waves = (units + slots - 1) / slots;
+    return static_cast<double>(units) / static_cast<double>(waves * slots);
+}
+
+template <int MT, int DT>
+int launch_w4a8_dt(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
+                   const void* packed, int M, int N, int K, void* Y, cudaStream_t stream) {
+    // 16-channel CTAs (twice as many, each with twice the K slots) unless 32-channel
+    // CTAs already fill every CTA slot of the GPU at least once; then whichever fills
+    // the last wave better (32 on a tie: fewer K slots to reduce).
+    const int units32 = w4a8_tiles(N), units16 = 2 * w4a8_tiles(N);
+    const int occ32 = w4a8_occupancy<MT, DT, 32>(ctx), occ16 = w4a8_occupancy<MT, DT, 16>(ctx);
+    if (occ32 < 1 || occ16 < 1) return -3;
+    const double f32 = units32 >= occ32 * ctx.num_sms
+                           ? w4a8_wave_fill(units32, occ32, ctx.num_sms) : 0.0;
+    const double f16 = w4a8_wave_fill(units16, occ16, ctx.num_sms);
+    if (f32 >= f16)
+        return launch_w4a8_instance<MT, DT, 32>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
+    return launch_w4a8_instance<MT, DT, 16>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
 }
 
 template <int MT>
 int launch_w4a8_mt(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
                    const void* packed, int M, int N, int K, int dtype, void* Y,
                    cudaStream_t stream) {
-    // 32-channel CTAs where they give at least two per SM, else 16-channel CTAs (twice as
-    // many, each with twice as many K slots).
-    const bool wide = w4a8_tiles(N) >= 2 * ctx.num_sms;
-    if (wide)
-        return dtype == 0 ? launch_w4a8_instance<MT, 0, 32>(ctx, A_i8, s_a, packed, M, N, K, Y, stream)
-                          : launch_w4a8_instance<MT, 1, 32>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
-    return dtype == 0 ? launch_w4a8_instance<MT, 0, 16>(ctx, A_i8, s_a, packed, M, N, K, Y, stream)
-                      : launch_w4a8_instance<MT, 1, 16>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
+    return dtype == 0 ? launch_w4a8_dt<MT, 0>(ctx, A_i8, s_a, packed, M, N, K, Y, stream)
+                      : launch_w4a8_dt<MT, 1>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
 }
 
 }  // namespace
@@ -450,7 +589,7 @@ int launch_w4a8_quantize(const DeviceCtx& ctx, const void* A, int M, int K, int 
     (void)ctx;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(M), 1, 1);
-    cfg.blockDim = dim3(kW4a8Threads, 1, 1);
+    cfg.blockDim = dim3(kQuantThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
