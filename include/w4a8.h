@@ -14,8 +14,10 @@
  * exactly in int32 and scaled in fp32 (two multiplies, in the order above), then
  * rounded once to the output dtype.
  *
- * On sm_103a there is no int8 tensor-core MMA (tcgen05.mma.kind::i8 is rejected for
- * this target), so the int8 dot products run on the CUDA cores (dp4a); see w4a8_gemm.
+ * On sm_103a the tcgen05 family has no int8 MMA (kind::i8 is rejected for this target)
+ * and the int8 mma.sync runs at the rate of dp4a on the CUDA cores, so the int8 products
+ * are computed exactly through the f16 mma.sync (int8 values are exact in fp16, and each
+ * 128-K block's sum stays below 2^24) or by dp4a; see w4a8_gemm.
  *
  * Conventions are those of w4a16.h: device pointers on the current device, caller-owned
  * buffers, `stream` a cudaStream_t passed as void*, asynchronous calls, w4a16_status
@@ -39,10 +41,10 @@ extern "C" {
  * unsupported (N < 1, K < 128, K % 128 != 0, K > 131072).  Host-only.  Source: the
  * two-level format of "W4A8量化计算优化" §2.1 (4-bit codes, one step and one offset byte
  * per group, one fp32 channel scale), repacked into the kernel's order.  With Np = N
- * rounded up to a multiple of 32 the blob is
+ * rounded up to a multiple of 16 the blob is
  *     128-byte header
- *   + (Np/32)*(K/128) blocks of 2112 bytes (2048 bytes of codes for 32 channels x 128 K,
- *     then each channel's step and offset)
+ *   + (Np/16)*(K/128) blocks of 1056 bytes (1024 bytes of codes for 16 channels x 128 K
+ *     in the MMA fragment order, then the channels' steps and offsets)
  *   + 4*Np bytes of fp32 channel scales.
  * The layout is private to this library and versioned by the header.
  */
@@ -88,10 +90,12 @@ int w4a8_quantize_act(const void* A, int M, int K, int dtype, int8_t* A_i8, floa
 
 /*
  * The W4A8 GEMM: Y = the formula at the top of this header, with the int8 weights
- * dequantised in registers from `packed` by one IMAD and one XOR per four codes and
- * never written back ("W4A8量化计算优化" §3.1-3.2).  The int8 dot products run on the CUDA
- * cores (dp4a, exact int32 sums) because sm_103a has no int8 tensor-core MMA; this is a
- * decode path: 1 <= M <= 16 (larger M returns UNSUPPORTED).
+ * dequantised in registers from `packed` by one IMAD per four codes and never written
+ * back ("W4A8量化计算优化" §3.1-3.2).  For 3..16 rows the int8 products go through the f16
+ * tensor-core mma.sync (int8 values carried exactly as fp16, each 128-K block summed
+ * exactly in fp32, the blocks added in int32); for 1 or 2 rows through dp4a on the CUDA
+ * cores.  The sum is exact either way.  This is a decode path: 1 <= M <= 16 (larger M
+ * returns UNSUPPORTED).
  *   A_i8, s_a  device, as written by w4a8_quantize_act (A_i8 16-byte aligned).
  *   packed     device, blob written by w4a8_repack with the same N and K.
  *   M, N, K    M == 0 is a no-op; N, K as for w4a8_repack.
@@ -110,7 +114,7 @@ int w4a8_gemm(const int8_t* A_i8, const float* s_a, const void* packed, int M, i
 /*
  * Debug / parity only: the int8 weights Q_i8[N][K] (row-major, device, 16-byte aligned,
  * caller-owned) the GEMM multiplies, expanded from the blob with the GEMM's own
- * IMAD + XOR arithmetic (the congruence of "W4A8量化计算优化" §2.1).  Header checked as in
+ * IMAD arithmetic and the XOR (the congruence of "W4A8量化计算优化" §2.1).  Header checked as in
  * w4a8_gemm.  Errors: INVALID_ARG, UNSUPPORTED, CUDA.
  */
 int w4a8_dequant_debug(const void* packed, int N, int K, int8_t* W_out, void* stream);

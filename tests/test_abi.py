@@ -93,8 +93,8 @@ def test_timeout_probe_rejects_bad_limits(L):
 
 @pytest.mark.parametrize("N,K", [(32, 128), (4096, 4096), (28672, 8192), (40, 256), (8200, 384)])
 def test_w4a8_packed_bytes_formula(L, N, K):
-    Np = -(-N // 32) * 32
-    assert w4.w4a8_packed_bytes(N, K) == 128 + (Np // 32) * (K // 128) * 2112 + 4 * Np
+    Np = -(-N // 16) * 16
+    assert w4.w4a8_packed_bytes(N, K) == 128 + (Np // 16) * (K // 128) * 1056 + 4 * Np
 
 
 @pytest.mark.parametrize("N,K", [(0, 128), (32, 0), (32, 100), (32, 192), (32, 131072 + 128)])

@@ -179,11 +179,13 @@ def test_gemm_every_element_bitexact(M, N, K, dtype):
     _assert_bits(Y, _oracle_y(c, qa, sa), "Y")
 
 
-def test_gemm_extreme_codes():
+@pytest.mark.parametrize("M", [2, 16], ids=["dp4a_m2", "mma_m16"])
+def test_gemm_extreme_codes(M):
     """Every group at its extremes: steps 16 with codes 15 (int8 127) and steps 1 with
     code 0 and offset 0 (int8 -128), against activations of +-127: the largest products
-    the format allows, summed over K = 28672 (|sum| close to 2^29)."""
-    M, N, K = 2, 64, 28672
+    the format allows, summed over K = 28672 (|sum| close to 2^29; on the tensor-core path
+    each 128-K block's fp32 partial reaches 128 * 127 * 128, its largest exact case)."""
+    N, K = 64, 28672
     G = K // 128
     qweight = np.full((N, K // 8), 0xFFFFFFFF, dtype=np.uint32)
     qweight[N // 2:] = 0
@@ -192,7 +194,7 @@ def test_gemm_extreme_codes():
     a = np.full((N, G), 15, np.uint8)   # 15 * 16 + 15 = 255 -> int8 127
     a[N // 2:] = 0                      # 0 * 1 + 0 = 0 -> int8 -128
     A = np.ones((M, K))
-    A[1, ::2] = -1.0
+    A[1::2, ::2] = -1.0
     c = si.W4A8Case(M, N, K, si.FP16, si.to_dtype_bits(A, si.FP16), qweight, s_u8, a,
                     np.full(N, 1e-5, np.float32))
     packed = _repack(c)

@@ -1,32 +1,41 @@
 // W4A8 path (LiquidQuant): 4-bit weight codes turned back into int8 inside the kernel,
-// multiplied with per-row int8 activations, accumulated exactly in int32 and scaled in
-// fp32.  Source: "W4A8量化计算优化：提升LLM推理效率的关键技术" §2.1 (the congruence
+// multiplied with per-row int8 activations, summed exactly and scaled in fp32.  Source:
+// "W4A8量化计算优化：提升LLM推理效率的关键技术" §2.1 (the congruence
 // Q_i8 = (Q_u4 * s_u8 + a) XOR 0x80 with an integer step s_u8 <= 16, so that one IMAD
-// and one XOR dequantise four weights packed one per byte), §3.1-3.2 (dequantise in
-// registers, feed the multiply directly, never write the int8 weights back).
+// dequantises four codes packed one per byte), §3.1-3.2 (dequantise in registers and
+// feed the multiply directly; the int8 weights are never written back).
 //
-// The int8 tensor-core MMA the page feeds (tcgen05.mma.kind::i8) is not available on
-// sm_103a (ptxas rejects the kind for this target), so the int8 dot products run on the
-// CUDA cores as dp4a: four int8 x int8 products and their sum added to an int32 in one
-// instruction.  Integer accumulation is exact, so the result does not depend on the
-// order of the K sum and equals the plain definition bit for bit.
+// The page feeds an int8 x int8 -> int32 tensor-core MMA.  On sm_103a the int8 MMA of
+// the tcgen05 family does not exist (ptxas rejects kind::i8 for this target), and the
+// int8 mma.sync runs at about the rate of dp4a on the CUDA cores (measured 75 and 72
+// T MAC/s), while the f16 mma.sync runs at 297 T MAC/s.  Every int8 value is exact in
+// fp16, and one 128-K block's partial sum of int8 products stays below 2^24 in
+// magnitude (128 * 127 * 128), so an f16 MMA with fp32 accumulation computes each
+// block's integer sum exactly; the blocks' sums are then added in int32.  The GEMM
+// therefore takes the f16 mma.sync for 3..16 activation rows and dp4a for one or two
+// rows (where the MMA's fixed 8-row width would waste most of its work).  Either way
+// the result is the exact integer sum, the same bits as the plain definition.
 //
 // Packed blob (private to this file, versioned by its header):
-//   [0, 128)              header (W4A8Header)
-//   blocks                one per (32-channel tile t, 128-K block kb), tiles in order,
-//                         blocks of one tile contiguous along K; kW4a8BlockBytes each:
-//     [0, 2048)           codes: piece p (32 K values) x channel r (32) x 16 bytes.  The
-//                         16 bytes of (p, r) are four words; word i holds K values
-//                         32p + 8i + (0..7) with K value j in byte j & 3, low nibble for
-//                         j < 4, high nibble for j >= 4.  So (x & 0x0F0F0F0F) and
-//                         ((x >> 4) & 0x0F0F0F0F) are four consecutive codes each, one
-//                         per byte, in K order -- the byte order of an int8 activation
-//                         word -- and a warp whose lanes are 32 channels reads piece p of
-//                         a block as 512 contiguous bytes.
-//     [2048, 2112)        channel r's step s_u8 (byte 2r) and offset a (byte 2r + 1).
-//   s_w                   fp32 [Np], the per-channel scale (0 past N).
-// N is padded to Np = a multiple of 32 (padded channels: codes 0, step 1, offset 128, so
+//   [0, 128)            header (W4A8Header)
+//   blocks              one per (16-channel tile t, 128-K block kb), tiles in order,
+//                       blocks of one tile contiguous along K; kW4a8BlockBytes each:
+//     [0, 1024)         codes in the mma.sync fragment order: lane l = 4g + i (g = l / 4,
+//                       i = l % 4) owns 32 bytes at 32 l, one word per 16-K step j; byte
+//                       b of word j holds the codes of K value 16 j + 4 i + b of channel
+//                       g (low nibble) and of channel g + 8 (high nibble).  So
+//                       (x & 0x0F0F0F0F) and ((x >> 4) & 0x0F0F0F0F) are four codes of
+//                       one channel in K order, and a warp reads a block as 1 KB of
+//                       contiguous 32-byte pieces.
+//     [1024, 1056)      word g: step and offset of channel g (bytes 0, 1) and of
+//                       channel g + 8 (bytes 2, 3).
+//   s_w                 fp32 [Np], the per-channel scale (0 past N).
+// N is padded to Np = a multiple of 16 (padded channels: codes 0, step 1, offset 128, so
 // their int8 weights are exactly 0); K must be a multiple of 128 (one group per block).
+//
+// Within a 16-K step the MMA's K index k' = 2i + e (e = 0, 1) stands for K value 4i + e
+// and k' = 8 + 2i + e for 4i + 2 + e, for the weights and the activations alike; a sum
+// over K does not depend on the order of its terms, and these sums are exact.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -38,14 +47,14 @@ namespace w4g {
 namespace {
 
 constexpr uint32_t kW4a8Magic = 0x38413457u;  // "W4A8"
-constexpr uint32_t kW4a8Version = 1;
+constexpr uint32_t kW4a8Version = 2;
 constexpr int kW4a8Group = 128;
-constexpr int kW4a8TileN = 32;
-constexpr uint32_t kW4a8CodeBytes = kW4a8TileN * kW4a8Group / 2;             // 2048
-constexpr uint32_t kW4a8BlockBytes = kW4a8CodeBytes + 2 * kW4a8TileN;        // 2112
+constexpr int kW4a8TileN = 16;
+constexpr uint32_t kW4a8CodeBytes = kW4a8TileN * kW4a8Group / 2;             // 1024
+constexpr uint32_t kW4a8BlockBytes = kW4a8CodeBytes + 2 * kW4a8TileN;        // 1056
 constexpr int kW4a8Threads = 256;
-constexpr int kW4a8Warps = kW4a8Threads / 32;
-constexpr int kStatusInvalidArg = -1;  // w4a16_status W4A16_ERR_INVALID_ARG
+constexpr int kW4a8Warps = kW4a8Threads / 32;  // K slots of a GEMM CTA
+constexpr int kStatusInvalidArg = -1;          // w4a16_status W4A16_ERR_INVALID_ARG
 
 struct W4A8Header {
     uint32_t magic;
@@ -67,11 +76,12 @@ __host__ __device__ inline uint64_t w4a8_sw_offset(int N, int K) {
     return 128ull + static_cast<uint64_t>(w4a8_tiles(N)) * (K / kW4a8Group) * kW4a8BlockBytes;
 }
 
-// Four codes (one per byte, each 0..15) -> four int8 weights by the congruence: the
-// products code * s stay below 256 and, with the offset added, every byte stays at most
-// 255 (the format's precondition), so no carry crosses a byte.
-__device__ __forceinline__ int congruence_i8x4(uint32_t codes, uint32_t s, uint32_t add) {
-    return static_cast<int>((codes * s + add) ^ 0x80808080u);
+// Four codes (one per byte, each 0..15) -> code * s + a per byte, i.e. the int8 weights
+// plus 128 (the congruence before its XOR): the products code * s stay below 256 and,
+// with the offset added, every byte stays at most 255 (the format's precondition), so
+// no carry crosses a byte.
+__device__ __forceinline__ uint32_t biased_i8x4(uint32_t codes, uint32_t s, uint32_t add) {
+    return codes * s + add;
 }
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
@@ -90,52 +100,57 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
 
 // ---- repack ------------------------------------------------------------------------
 
-// One CTA per (tile, block); thread (p, r) = (tid / 32, tid % 32) writes the 16 code
-// bytes of piece p of channel r; warp 0 also writes the channel's step and offset.
-// Codes whose byte value code * s + a would pass 255, and steps outside 1..16, are
-// recorded as W4A16_ERR_INVALID_ARG in the status word (the blob is written anyway).
-__global__ void __launch_bounds__(128) w4a8_repack_kernel(
+// One CTA per (tile, block); thread (j, l) = (tid / 32, tid % 32) writes word j of lane
+// l: the codes of K values 16 j + 4 i + (0..3) of channels g and g + 8 (g = l / 4,
+// i = l % 4).  Lanes 4g of step 0 also write the step and offset word g, and in block 0
+// of the tile the two channels' s_w.  Codes whose byte value code * s + a would pass
+// 255, and steps outside 1..16, are recorded as W4A16_ERR_INVALID_ARG in the status word
+// (the blob is written anyway).
+__global__ void __launch_bounds__(256) w4a8_repack_kernel(
     const uint32_t* __restrict__ qweight, const uint8_t* __restrict__ s_u8,
     const uint8_t* __restrict__ off, const float* __restrict__ s_w, int N, int K,
     uint8_t* __restrict__ packed, int* status) {
     const int kblocks = K / kW4a8Group;
     const int t = static_cast<int>(blockIdx.x) / kblocks;
     const int kb = static_cast<int>(blockIdx.x) - t * kblocks;
-    const int p = static_cast<int>(threadIdx.x) >> 5;
-    const int r = static_cast<int>(threadIdx.x) & 31;
-    const int n = t * kW4a8TileN + r;
+    const int j = static_cast<int>(threadIdx.x) >> 5;
+    const int l = static_cast<int>(threadIdx.x) & 31;
+    const int g = l >> 2, i = l & 3;
     uint8_t* blk = packed + 128 + static_cast<size_t>(blockIdx.x) * kW4a8BlockBytes;
-
-    uint32_t s = 1, a = 128;
-    uint4 in = make_uint4(0, 0, 0, 0);
-    if (n < N) {
-        s = s_u8[static_cast<size_t>(n) * kblocks + kb];
-        a = off[static_cast<size_t>(n) * kblocks + kb];
-        in = *reinterpret_cast<const uint4*>(qweight + static_cast<size_t>(n) * (K / 8) +
-                                              kb * 16 + p * 4);
-    }
-    const uint32_t words[4] = {in.x, in.y, in.z, in.w};
-    uint32_t out[4];
-    bool bad = s < 1 || s > 16;
+    const int k0 = kb * kW4a8Group + 16 * j + 4 * i;  // first of the four K values
+    uint32_t codes[2], sv[2], av[2];
+    bool bad = false;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t o = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t q = (words[i] >> (4 * j)) & 0xFu;
-            bad |= q * s + a > 255u;
-            o |= q << (8 * (j & 3) + 4 * (j >> 2));
+    for (int h = 0; h < 2; ++h) {  // channel g (h = 0) and g + 8 (h = 1)
+        const int n = t * kW4a8TileN + g + 8 * h;
+        uint32_t s = 1, a = 128, c = 0;
+        if (n < N) {
+            s = s_u8[static_cast<size_t>(n) * kblocks + kb];
+            a = off[static_cast<size_t>(n) * kblocks + kb];
+            const uint32_t w = qweight[static_cast<size_t>(n) * (K / 8) + k0 / 8];
+            c = (w >> (4 * (k0 & 7))) & 0xFFFFu;  // four nibbles, K order
         }
-        out[i] = o;
+        bad |= s < 1 || s > 16;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) bad |= ((c >> (4 * b)) & 0xFu) * s + a > 255u;
+        codes[h] = c;
+        sv[h] = s;
+        av[h] = a;
     }
     if (bad) record_status(status, kStatusInvalidArg);
-    *reinterpret_cast<uint4*>(blk + p * 512 + r * 16) = make_uint4(out[0], out[1], out[2], out[3]);
-    if (p == 0) {
-        blk[kW4a8CodeBytes + 2 * r] = static_cast<uint8_t>(s);
-        blk[kW4a8CodeBytes + 2 * r + 1] = static_cast<uint8_t>(a);
+    uint32_t word = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+        word |= (((codes[0] >> (4 * b)) & 0xFu) | (((codes[1] >> (4 * b)) & 0xFu) << 4)) << (8 * b);
+    *reinterpret_cast<uint32_t*>(blk + 32 * l + 4 * j) = word;
+    if (j == 0 && i == 0) {
+        *reinterpret_cast<uint32_t*>(blk + kW4a8CodeBytes + 4 * g) =
+            sv[0] | (av[0] << 8) | (sv[1] << 16) | (av[1] << 24);
         if (kb == 0) {
             float* sw = reinterpret_cast<float*>(packed + w4a8_sw_offset(N, K));
-            sw[n] = n < N ? s_w[n] : 0.0f;
+            const int n0 = t * kW4a8TileN + g;
+            sw[n0] = n0 < N ? s_w[n0] : 0.0f;
+            sw[n0 + 8] = n0 + 8 < N ? s_w[n0 + 8] : 0.0f;
         }
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -165,7 +180,10 @@ __device__ __forceinline__ bool w4a8_header_ok(const uint8_t* packed, int N, int
 
 // ---- debug dequant: the int8 weights W_i8[N][K] the GEMM multiplies -------------------
 
-__global__ void __launch_bounds__(128) w4a8_dequant_debug_kernel(
+// Thread (j, l) of a block's CTA expands word j of lane l with the GEMM's arithmetic
+// (one IMAD per four codes, then the XOR) into the four int8 weights of channels g and
+// g + 8.
+__global__ void __launch_bounds__(256) w4a8_dequant_debug_kernel(
     const uint8_t* __restrict__ packed, int N, int K, int8_t* __restrict__ W, int* status) {
     __shared__ int ok;
     if (threadIdx.x == 0) {
@@ -177,24 +195,20 @@ __global__ void __launch_bounds__(128) w4a8_dequant_debug_kernel(
     const int kblocks = K / kW4a8Group;
     const int t = static_cast<int>(blockIdx.x) / kblocks;
     const int kb = static_cast<int>(blockIdx.x) - t * kblocks;
-    const int p = static_cast<int>(threadIdx.x) >> 5;
-    const int r = static_cast<int>(threadIdx.x) & 31;
-    const int n = t * kW4a8TileN + r;
-    if (n >= N) return;
+    const int j = static_cast<int>(threadIdx.x) >> 5;
+    const int l = static_cast<int>(threadIdx.x) & 31;
+    const int g = l >> 2, i = l & 3;
     const uint8_t* blk = packed + 128 + static_cast<size_t>(blockIdx.x) * kW4a8BlockBytes;
-    const uint4 v = *reinterpret_cast<const uint4*>(blk + p * 512 + r * 16);
-    const uint32_t s = blk[kW4a8CodeBytes + 2 * r];
-    const uint32_t add = blk[kW4a8CodeBytes + 2 * r + 1] * 0x01010101u;
-    const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-    int o[8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        o[2 * i] = congruence_i8x4(x[i] & 0x0F0F0F0Fu, s, add);
-        o[2 * i + 1] = congruence_i8x4((x[i] >> 4) & 0x0F0F0F0Fu, s, add);
-    }
-    int4* dst = reinterpret_cast<int4*>(W + static_cast<size_t>(n) * K + kb * kW4a8Group + p * 32);
-    dst[0] = make_int4(o[0], o[1], o[2], o[3]);
-    dst[1] = make_int4(o[4], o[5], o[6], o[7]);
+    const uint32_t x = *reinterpret_cast<const uint32_t*>(blk + 32 * l + 4 * j);
+    const uint32_t meta = *reinterpret_cast<const uint32_t*>(blk + kW4a8CodeBytes + 4 * g);
+    const uint32_t w0 = biased_i8x4(x & 0x0F0F0F0Fu, meta & 0xFFu,
+                                    ((meta >> 8) & 0xFFu) * 0x01010101u) ^ 0x80808080u;
+    const uint32_t w1 = biased_i8x4((x >> 4) & 0x0F0F0F0Fu, (meta >> 16) & 0xFFu,
+                                    (meta >> 24) * 0x01010101u) ^ 0x80808080u;
+    const int k0 = kb * kW4a8Group + 16 * j + 4 * i;
+    const int n0 = t * kW4a8TileN + g;
+    if (n0 < N) *reinterpret_cast<uint32_t*>(W + static_cast<size_t>(n0) * K + k0) = w0;
+    if (n0 + 8 < N) *reinterpret_cast<uint32_t*>(W + static_cast<size_t>(n0 + 8) * K + k0) = w1;
 }
 
 // ---- per-row int8 activations ------------------------------------------------------
@@ -299,41 +313,89 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-// Accumulator chains per activation row: two independent dp4a chains where there are
-// only one or two rows, one where the rows already give enough independent chains.
-template <int MT>
-constexpr int w4a8_chains() { return MT <= 2 ? 2 : 1; }
+// One round of staged int8 activations per row: the K values of one block per K slot,
+// padded by 16 bytes so that the eight rows an MMA fragment reads fall in distinct banks.
+constexpr uint32_t kW4a8ARow = kW4a8Warps * kW4a8Group + 16;  // 1040
 
-// acc[m][*] += the int8 products of one 128-K block of this thread's channel with the
-// MT activation rows staged in shared memory (rows past M hold zeros).  w: the block's
-// four 16-byte pieces; meta: step in bits 0..7, offset in bits 8..15; a_s: row 0 of the
-// block's int8 activations, row m at + m * kRow bytes.
-template <int MT, uint32_t kRow>
-__device__ __forceinline__ void w4a8_block(const uint4 (&w)[4], uint32_t meta,
-                                           const uint8_t* a_s,
-                                           int (&acc)[MT][w4a8_chains<MT>()]) {
-    constexpr int C = w4a8_chains<MT>();
-    const uint32_t s = meta & 0xFFu;
-    const uint32_t add = ((meta >> 8) & 0xFFu) * 0x01010101u;
+__host__ __device__ constexpr uint32_t w4a8_smem_bytes(int MT) { return 2u * MT * kW4a8ARow; }
+
+// Two biased int8 values (bytes sel picks, each v + 128) -> their values as an fp16 pair:
+// 0x6400 | byte is 1024 + byte exactly, and subtracting 1152 leaves v exactly.
+__device__ __forceinline__ uint32_t biased_u8x2_to_f16x2(uint32_t u, uint32_t sel) {
+    uint32_t d = __byte_perm(u, 0x64646464u, sel);
+    asm("sub.rn.f16x2 %0, %0, %1;" : "+r"(d) : "r"(0x64806480u));
+    return d;
+}
+
+__device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint32_t a1,
+                                                uint32_t a2, uint32_t a3, uint32_t b0,
+                                                uint32_t b1) {
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, "
+        "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// One 128-K block of this lane's two channels (g and g + 8) with MT <= 2 activation rows,
+// by dp4a: acc[h][m] += the int8 products of channel g + 8h with row m over the lane's
+// four K values of each 16-K step.  a_s: the block's staged activations at this lane's
+// K offset 4i (row m at + m * kW4a8ARow).
+template <int MT>
+__device__ __forceinline__ void w4a8_block_dp4a(const uint4 (&w)[2], uint32_t meta,
+                                                const uint8_t* a_s, int (&acc)[2][MT]) {
+    const uint32_t s0 = meta & 0xFFu, add0 = ((meta >> 8) & 0xFFu) * 0x01010101u;
+    const uint32_t s1 = (meta >> 16) & 0xFFu, add1 = (meta >> 24) * 0x01010101u;
+    const uint32_t x[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const uint32_t x[4] = {w[p].x, w[p].y, w[p].z, w[p].w};
-        int wq[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            wq[2 * i] = congruence_i8x4(x[i] & 0x0F0F0F0Fu, s, add);
-            wq[2 * i + 1] = congruence_i8x4((x[i] >> 4) & 0x0F0F0F0Fu, s, add);
-        }
+    for (int j = 0; j < 8; ++j) {
+        const int w0 = static_cast<int>(biased_i8x4(x[j] & 0x0F0F0F0Fu, s0, add0) ^ 0x80808080u);
+        const int w1 = static_cast<int>(biased_i8x4((x[j] >> 4) & 0x0F0F0F0Fu, s1, add1) ^ 0x80808080u);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const uint4* ap = reinterpret_cast<const uint4*>(a_s + m * kRow + 32 * p);
-            const uint4 a0 = ap[0], a1 = ap[1];
-            const uint32_t av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                acc[m][i % C] = __dp4a(wq[i], static_cast<int>(av[i]), acc[m][i % C]);
+            const int a = *reinterpret_cast<const int*>(a_s + m * kW4a8ARow + 16 * j);
+            acc[0][m] = __dp4a(w0, a, acc[0][m]);
+            acc[1][m] = __dp4a(w1, a, acc[1][m]);
         }
     }
+}
+
+// One 128-K block of the warp's 16 channels with NT groups of 8 activation rows, by f16
+// mma.sync (m16n8k16): the weights, as int8 values in fp16, are the A fragments (rows g
+// and g + 8 of the tile), the activations the B fragments (row 8t + g of group t).  The
+// block's sums are accumulated in fp32 from zero (exact: every partial sum is an integer
+// below 2^24) and then added to iacc in int32.  a_s: the block's staged activations at
+// this lane's K offset 4i and row g (group t at + 8t rows).
+template <int NT>
+__device__ __forceinline__ void w4a8_block_mma(const uint4 (&w)[2], uint32_t meta,
+                                               const uint8_t* a_s, int (&iacc)[NT][4]) {
+    const uint32_t s0 = meta & 0xFFu, add0 = ((meta >> 8) & 0xFFu) * 0x01010101u;
+    const uint32_t s1 = (meta >> 16) & 0xFFu, add1 = (meta >> 24) * 0x01010101u;
+    const uint32_t x[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
+    float f[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) f[t][e] = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t u0 = biased_i8x4(x[j] & 0x0F0F0F0Fu, s0, add0);
+        const uint32_t u1 = biased_i8x4((x[j] >> 4) & 0x0F0F0F0Fu, s1, add1);
+        const uint32_t a0 = biased_u8x2_to_f16x2(u0, 0x4140u);  // channel g, K 4i, 4i+1
+        const uint32_t a2 = biased_u8x2_to_f16x2(u0, 0x4342u);  // channel g, K 4i+2, 4i+3
+        const uint32_t a1 = biased_u8x2_to_f16x2(u1, 0x4140u);  // channel g + 8
+        const uint32_t a3 = biased_u8x2_to_f16x2(u1, 0x4342u);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const uint32_t av =
+                *reinterpret_cast<const uint32_t*>(a_s + 8 * t * kW4a8ARow + 16 * j) ^ 0x80808080u;
+            mma_f16_16x8x16(f[t], a0, a1, a2, a3, biased_u8x2_to_f16x2(av, 0x4140u),
+                            biased_u8x2_to_f16x2(av, 0x4342u));
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) iacc[t][e] += __float2int_rn(f[t][e]);
 }
 
 template <int DT>
@@ -342,41 +404,30 @@ __device__ __forceinline__ uint16_t w4a8_f32_to_dtype(float v) {
     else return __bfloat16_as_ushort(__float2bfloat16_rn(v));
 }
 
-// Dynamic shared memory of one GEMM CTA: two buffers of int8 activations, each MT rows
-// x (K slots x 128) values (the activations of one round of blocks).
-__host__ __device__ constexpr uint32_t w4a8_smem_bytes(int MT, int ROWS) {
-    return 2u * MT * (kW4a8Warps * (32 / ROWS)) * kW4a8Group;
-}
-
-// Work split.  A CTA owns ROWS (16 or 32) consecutive output channels over the whole K
-// range: thread lane % ROWS is the channel, and the 256 / ROWS K slots (ROWS lanes each)
-// take the 128-K blocks slot, slot + slots, ...: round r of the CTA is blocks
-// r * slots .. r * slots + slots - 1, one per slot.  Each thread keeps the weights of
-// two rounds in flight in registers (the loads of round r + 2 are issued as soon as
-// round r is multiplied); the int8 activations of a round are staged in shared memory
-// by the whole CTA with cp.async, one round ahead, so that the dp4a chains read them at
-// shared-memory latency.  The slots' int32 partials are summed in shared memory; the
-// sum is exact, so the slot order does not matter.  Epilogue per output element:
-// fp32(acc) * s_a[m] * s_w[n], two fp32 multiplies rounded to nearest even, then one
-// rounding to the output dtype.
-template <int MT, int DT, int ROWS>
-__global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : (MT == 2 ? 3 : 2)) w4a8_gemm_kernel(
+// Work split.  A CTA owns one 16-channel tile over the whole K range; its 8 warps are K
+// slots taking the 128-K blocks in rounds (round r: block 8r + warp).  Each lane keeps
+// its 32 bytes of codes of two rounds in flight in registers (the loads of round r + 2
+// are issued as soon as round r is multiplied); the CTA stages each round's int8
+// activations in shared memory with cp.async, one round ahead, rows M..MT-1 zero.  MT
+// is 1 or 2 (dp4a) or 8 or 16 (f16 mma.sync, one or two groups of 8 rows).  The warps'
+// int32 partials are summed in shared memory (exact, so the order does not matter).
+// Epilogue per output element: fp32(acc) * s_a[m] * s_w[n], two fp32 multiplies rounded
+// to nearest even, then one rounding to the output dtype.
+template <int MT, int DT>
+__global__ void __launch_bounds__(kW4a8Threads, MT <= 2 ? 4 : 3) w4a8_gemm_kernel(
     const int8_t* __restrict__ A_i8, const float* __restrict__ s_a,
     const uint8_t* __restrict__ packed, uint16_t* __restrict__ Y, int* status, int M, int N,
     int K) {
-    constexpr int kSub = 32 / ROWS;
-    constexpr int kSlots = kW4a8Warps * kSub;
-    constexpr int C = w4a8_chains<MT>();
-    constexpr uint32_t kRow = kSlots * kW4a8Group;  // bytes of one activation row per round
-    constexpr uint32_t kBuf = MT * kRow;
+    constexpr bool kMma = MT >= 8;
+    constexpr int NT = kMma ? MT / 8 : 1;
+    constexpr uint32_t kBuf = MT * kW4a8ARow;
+    constexpr int kPieces = static_cast<int>(kW4a8Warps * kW4a8Group / 16);  // per row and round
     extern __shared__ __align__(16) uint8_t a_smem[];
     __shared__ int s_ok;
     const int tid = static_cast<int>(threadIdx.x);
-    const int lane = tid & 31;
-    const int rl = lane % ROWS;
-    const int slot = (tid >> 5) * kSub + lane / ROWS;
-    const int n0 = static_cast<int>(blockIdx.x) * ROWS;
-    const int r = n0 % kW4a8TileN + rl;  // channel within its 32-channel tile
+    const int slot = tid >> 5, l = tid & 31;
+    const int g = l >> 2, i = l & 3;
+    const int tile = static_cast<int>(blockIdx.x);
 
     if (tid == 0) {
         const int ok = w4a8_header_ok(packed, N, K);
@@ -388,48 +439,52 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : (MT == 2 ? 3 : 2))
     if (tid == 0) grid_dep_launch();
 
     const int kblocks = K / kW4a8Group;
-    const int rounds = (kblocks + kSlots - 1) / kSlots;
-    const uint8_t* tile = packed + 128 +
-                          static_cast<size_t>(n0 / kW4a8TileN) * kblocks * kW4a8BlockBytes;
-    auto load = [&](int kb, uint4 (&w)[4], uint32_t& meta) {
-        const uint8_t* blk = tile + static_cast<size_t>(kb) * kW4a8BlockBytes;
-#pragma unroll
-        for (int p = 0; p < 4; ++p) w[p] = ld_stream_v4(blk + p * 512 + r * 16);
-        meta = ld_stream_u32(blk + kW4a8CodeBytes + (r & ~1) * 2) >> ((r & 1) * 16);
+    const int rounds = (kblocks + kW4a8Warps - 1) / kW4a8Warps;
+    const uint8_t* tile_p = packed + 128 + static_cast<size_t>(tile) * kblocks * kW4a8BlockBytes;
+    auto load = [&](int kb, uint4 (&w)[2], uint32_t& meta) {
+        const uint8_t* blk = tile_p + static_cast<size_t>(kb) * kW4a8BlockBytes;
+        w[0] = ld_stream_v4(blk + 32 * l);
+        w[1] = ld_stream_v4(blk + 32 * l + 16);
+        meta = ld_stream_u32(blk + kW4a8CodeBytes + 4 * g);
     };
     const uint32_t smem = smem_addr(a_smem);
-    // The activations of round rr into buffer rr & 1: rows m < M, 16 bytes per copy
-    // (pieces past K, in the last round only, are skipped: no block reads them).
+    // The activations of round rr into buffer rr & 1 (rows m < M; pieces past K, in the
+    // last round only, are skipped: no block reads them).
     auto stage = [&](int rr) {
-        constexpr int kPieces = static_cast<int>(kRow / 16);
-        const int k0 = rr * static_cast<int>(kRow);
+        const int k0 = rr * kW4a8Warps * kW4a8Group;
         const uint32_t buf = smem + (rr & 1) * kBuf;
         for (int e = tid; e < M * kPieces; e += kW4a8Threads) {
             const int m = e / kPieces, c = e % kPieces;
             if (k0 + c * 16 < K)
-                cp_async16(buf + m * kRow + c * 16, A_i8 + static_cast<size_t>(m) * K + k0 + c * 16);
+                cp_async16(buf + m * kW4a8ARow + c * 16,
+                           A_i8 + static_cast<size_t>(m) * K + k0 + c * 16);
         }
     };
-    // Rows M..MT-1 of both buffers are zero for the whole kernel (every block multiplies
-    // all MT rows; those products are 0 and their sums are never stored).
-    for (int e = tid; e < (MT - M) * static_cast<int>(kRow / 16) * 2; e += kW4a8Threads) {
-        const int per_buf = (MT - M) * static_cast<int>(kRow / 16);
+    // Rows M..MT-1 of both buffers stay zero for the whole kernel.
+    for (int e = tid; e < (MT - M) * kPieces * 2; e += kW4a8Threads) {
+        const int per_buf = (MT - M) * kPieces;
         const int bsel = e / per_buf, rem = e % per_buf;
-        const int m = M + rem / static_cast<int>(kRow / 16), c = rem % static_cast<int>(kRow / 16);
-        *reinterpret_cast<uint4*>(a_smem + bsel * kBuf + m * kRow + c * 16) = make_uint4(0, 0, 0, 0);
+        const int m = M + rem / kPieces, c = rem % kPieces;
+        *reinterpret_cast<uint4*>(a_smem + bsel * kBuf + m * kW4a8ARow + c * 16) =
+            make_uint4(0, 0, 0, 0);
     }
 
-    int acc[MT][C];
+    int acc[2][kMma ? 1 : MT];   // dp4a: channel g + 8h, row m
+    int iacc[NT][4];             // mma: D fragment of group t
 #pragma unroll
-    for (int m = 0; m < MT; ++m)
+    for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int c = 0; c < C; ++c) acc[m][c] = 0;
-    uint4 wa[4], wb[4];
+        for (int m = 0; m < (kMma ? 1 : MT); ++m) acc[h][m] = 0;
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) iacc[t][e] = 0;
+    uint4 wa[2], wb[2];
     uint32_t ma = 0, mb = 0;
     // The packed weights do not depend on the previous kernel: the first two rounds are
     // requested before the dependency wait.
     if (slot < kblocks) load(slot, wa, ma);
-    if (slot + kSlots < kblocks) load(slot + kSlots, wb, mb);
+    if (slot + kW4a8Warps < kblocks) load(slot + kW4a8Warps, wb, mb);
     grid_dep_wait();  // A_i8 and s_a (and Y) belong to the previous kernel until here
     stage(0);
     cp_async_commit();
@@ -438,38 +493,50 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : (MT == 2 ? 3 : 2))
         cp_async_commit();      // (an empty group in the last round)
         cp_async_wait<1>();     // this thread's copies of round rr have landed ...
         __syncthreads();        // ... and every other thread's
-        const int kb = rr * kSlots + slot;
+        const int kb = rr * kW4a8Warps + slot;
         if (kb < kblocks) {
-            const uint8_t* a_s = a_smem + (rr & 1) * kBuf + slot * kW4a8Group;
+            const uint8_t* a_s = a_smem + (rr & 1) * kBuf + slot * kW4a8Group + 4 * i;
             if (rr & 1) {
-                w4a8_block<MT, kRow>(wb, mb, a_s, acc);
-                if (kb + 2 * kSlots < kblocks) load(kb + 2 * kSlots, wb, mb);
+                if constexpr (kMma) w4a8_block_mma<NT>(wb, mb, a_s + g * kW4a8ARow, iacc);
+                else w4a8_block_dp4a<MT>(wb, mb, a_s, acc);
+                if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wb, mb);
             } else {
-                w4a8_block<MT, kRow>(wa, ma, a_s, acc);
-                if (kb + 2 * kSlots < kblocks) load(kb + 2 * kSlots, wa, ma);
+                if constexpr (kMma) w4a8_block_mma<NT>(wa, ma, a_s + g * kW4a8ARow, iacc);
+                else w4a8_block_dp4a<MT>(wa, ma, a_s, acc);
+                if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wa, ma);
             }
         }
         __syncthreads();        // buffer rr & 1 is free for round rr + 2
     }
     cp_async_wait<0>();
-    // The activation buffers are reused for the slots' partials: red[slot][m][channel].
+    // The activation buffers are reused for the warps' partials: red[slot][channel][row].
     int* red = reinterpret_cast<int*>(a_smem);
+    if constexpr (kMma) {
 #pragma unroll
-    for (int m = 0; m < MT; ++m) {
-        int t = acc[m][0];
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-        for (int c = 1; c < C; ++c) t += acc[m][c];
-        red[(slot * MT + m) * ROWS + rl] = t;
+            for (int e = 0; e < 4; ++e)
+                red[(slot * kW4a8TileN + g + 8 * (e >> 1)) * MT + 8 * t + 2 * i + (e & 1)] = iacc[t][e];
+    } else {
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int m = 0; m < MT; ++m) {
+                int v = acc[h][m];  // the four lanes of a channel pair hold K quarters
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+                v += __shfl_xor_sync(0xFFFFFFFFu, v, 2);
+                if (i == 0) red[(slot * kW4a8TileN + g + 8 * h) * MT + m] = v;
+            }
     }
     __syncthreads();
     const float* sw = reinterpret_cast<const float*>(packed + w4a8_sw_offset(N, K));
-    for (int e = tid; e < MT * ROWS; e += kW4a8Threads) {
-        const int m = e / ROWS, jr = e - (e / ROWS) * ROWS;
-        const int n = n0 + jr;
-        if (m < M && n < N) {
+    for (int e = tid; e < kW4a8TileN * M; e += kW4a8Threads) {
+        const int m = e / kW4a8TileN, row = e % kW4a8TileN;
+        const int n = tile * kW4a8TileN + row;
+        if (n < N) {
             int sum = 0;
 #pragma unroll
-            for (int q = 0; q < kSlots; ++q) sum += red[(q * MT + m) * ROWS + jr];
+            for (int q = 0; q < kW4a8Warps; ++q) sum += red[(q * kW4a8TileN + row) * MT + m];
             float y = __int2float_rn(sum);
             y = __fmul_rn(y, s_a[m]);
             y = __fmul_rn(y, sw[n]);
@@ -478,21 +545,13 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : (MT == 2 ? 3 : 2))
     }
 }
 
-template <int MT, int DT, int ROWS>
+template <int MT, int DT>
 int launch_w4a8_instance(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
                          const void* packed, int M, int N, int K, void* Y, cudaStream_t stream) {
-    auto kern = w4a8_gemm_kernel<MT, DT, ROWS>;
-    constexpr uint32_t smem = w4a8_smem_bytes(MT, ROWS);
-    static int configured_device = -1;  // attribute set once per device and instance
-    if (configured_device != ctx.device) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess)
-            return -3;
-        configured_device = ctx.device;
-    }
-    const int np = w4a8_tiles(N) * kW4a8TileN;
+    auto kern = w4a8_gemm_kernel<MT, DT>;
+    constexpr uint32_t smem = w4a8_smem_bytes(MT);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(np / ROWS), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(w4a8_tiles(N)), 1, 1);
     cfg.blockDim = dim3(kW4a8Threads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
@@ -507,56 +566,12 @@ int launch_w4a8_instance(const DeviceCtx& ctx, const int8_t* A_i8, const float* 
     return e == cudaSuccess ? 0 : -3;
 }
 
-// CTAs of one instance resident per SM (queried once per device).
-template <int MT, int DT, int ROWS>
-int w4a8_occupancy(const DeviceCtx& ctx) {
-    static int device = -1, occ = 0;
-    if (device != ctx.device) {
-        auto kern = w4a8_gemm_kernel<MT, DT, ROWS>;
-        constexpr uint32_t smem = w4a8_smem_bytes(MT, ROWS);
-        int o = 0;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem)) != cudaSuccess ||
-            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kW4a8Threads, smem) !=
-                cudaSuccess)
-            return 0;
-        occ = o;
-        device = ctx.device;
-    }
-    return occ;
-}
-
-// Fraction of the CTA slots of the GPU that the launch's waves keep busy.
-inline double w4a8_wave_fill(int units, int per_sm, int sms) {
-    if (per_sm < 1) return 0.0;
-    const long long slots = static_cast<long long>(per_sm) * sms;
-    const long long waves = (units + slots - 1) / slots;
-    return static_cast<double>(units) / static_cast<double>(waves * slots);
-}
-
-template <int MT, int DT>
-int launch_w4a8_dt(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
-                   const void* packed, int M, int N, int K, void* Y, cudaStream_t stream) {
-    // 16-channel CTAs (twice as many, each with twice the K slots) unless 32-channel
-    // CTAs already fill every CTA slot of the GPU at least once; then whichever fills
-    // the last wave better (32 on a tie: fewer K slots to reduce).
-    const int units32 = w4a8_tiles(N), units16 = 2 * w4a8_tiles(N);
-    const int occ32 = w4a8_occupancy<MT, DT, 32>(ctx), occ16 = w4a8_occupancy<MT, DT, 16>(ctx);
-    if (occ32 < 1 || occ16 < 1) return -3;
-    const double f32 = units32 >= occ32 * ctx.num_sms
-                           ? w4a8_wave_fill(units32, occ32, ctx.num_sms) : 0.0;
-    const double f16 = w4a8_wave_fill(units16, occ16, ctx.num_sms);
-    if (f32 >= f16)
-        return launch_w4a8_instance<MT, DT, 32>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
-    return launch_w4a8_instance<MT, DT, 16>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
-}
-
 template <int MT>
 int launch_w4a8_mt(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
                    const void* packed, int M, int N, int K, int dtype, void* Y,
                    cudaStream_t stream) {
-    return dtype == 0 ? launch_w4a8_dt<MT, 0>(ctx, A_i8, s_a, packed, M, N, K, Y, stream)
-                      : launch_w4a8_dt<MT, 1>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
+    return dtype == 0 ? launch_w4a8_instance<MT, 0>(ctx, A_i8, s_a, packed, M, N, K, Y, stream)
+                      : launch_w4a8_instance<MT, 1>(ctx, A_i8, s_a, packed, M, N, K, Y, stream);
 }
 
 }  // namespace
@@ -569,7 +584,7 @@ int launch_w4a8_repack(const DeviceCtx& ctx, const uint32_t* qweight, const uint
                        const uint8_t* off, const float* s_w, int N, int K, void* packed,
                        cudaStream_t stream) {
     const unsigned blocks = static_cast<unsigned>(w4a8_tiles(N) * (K / kW4a8Group));
-    w4a8_repack_kernel<<<blocks, 128, 0, stream>>>(qweight, s_u8, off, s_w, N, K,
+    w4a8_repack_kernel<<<blocks, 256, 0, stream>>>(qweight, s_u8, off, s_w, N, K,
                                                     static_cast<uint8_t*>(packed), ctx.status);
     if (cudaGetLastError() != cudaSuccess) return -3;
     w4a8_fence_kernel<<<1, 32, 0, stream>>>();
@@ -579,7 +594,7 @@ int launch_w4a8_repack(const DeviceCtx& ctx, const uint32_t* qweight, const uint
 int launch_w4a8_dequant_debug(const DeviceCtx& ctx, const void* packed, int N, int K,
                               void* W_out, cudaStream_t stream) {
     const unsigned blocks = static_cast<unsigned>(w4a8_tiles(N) * (K / kW4a8Group));
-    w4a8_dequant_debug_kernel<<<blocks, 128, 0, stream>>>(
+    w4a8_dequant_debug_kernel<<<blocks, 256, 0, stream>>>(
         static_cast<const uint8_t*>(packed), N, K, static_cast<int8_t*>(W_out), ctx.status);
     return cudaGetLastError() == cudaSuccess ? 0 : -3;
 }
@@ -606,9 +621,9 @@ int launch_w4a8_quantize(const DeviceCtx& ctx, const void* A, int M, int K, int 
 int launch_w4a8_gemm(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
                      const void* packed, int M, int N, int K, int dtype, void* Y,
                      cudaStream_t stream) {
+    // dp4a for one or two rows, the f16 MMA (groups of 8 rows) above
     if (M <= 1) return launch_w4a8_mt<1>(ctx, A_i8, s_a, packed, M, N, K, dtype, Y, stream);
     if (M <= 2) return launch_w4a8_mt<2>(ctx, A_i8, s_a, packed, M, N, K, dtype, Y, stream);
-    if (M <= 4) return launch_w4a8_mt<4>(ctx, A_i8, s_a, packed, M, N, K, dtype, Y, stream);
     if (M <= 8) return launch_w4a8_mt<8>(ctx, A_i8, s_a, packed, M, N, K, dtype, Y, stream);
     if (M <= 16) return launch_w4a8_mt<16>(ctx, A_i8, s_a, packed, M, N, K, dtype, Y, stream);
     return -2;
