@@ -317,7 +317,11 @@ __device__ __forceinline__ void cp_async_wait() {
 // padded by 16 bytes so that the eight rows an MMA fragment reads fall in distinct banks.
 constexpr uint32_t kW4a8ARow = kW4a8Warps * kW4a8Group + 16;  // 1040
 
-__host__ __device__ constexpr uint32_t w4a8_smem_bytes(int MT) { return 2u * MT * kW4a8ARow; }
+// Dynamic shared memory of a GEMM CTA: the two activation buffers of the MMA path, or
+// only the warps' partials (8 slots x 16 channels x MT rows of int32) of the dp4a path.
+__host__ __device__ constexpr uint32_t w4a8_smem_bytes(int MT) {
+    return MT >= 8 ? 2u * MT * kW4a8ARow : 512u * MT;
+}
 
 // Two biased int8 values (bytes sel picks, each v + 128) -> their values as an fp16 pair:
 // 0x6400 | byte is 1024 + byte exactly, and subtracting 1152 leaves v exactly.
@@ -338,11 +342,10 @@ __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint
 
 // One 128-K block of this lane's two channels (g and g + 8) with MT <= 2 activation rows,
 // by dp4a: acc[h][m] += the int8 products of channel g + 8h with row m over the lane's
-// four K values of each 16-K step.  a_s: the block's staged activations at this lane's
-// K offset 4i (row m at + m * kW4a8ARow).
+// four K values of each 16-K step j; xa[m][j]: those four activations of row m.
 template <int MT>
 __device__ __forceinline__ void w4a8_block_dp4a(const uint4 (&w)[2], uint32_t meta,
-                                                const uint8_t* a_s, int (&acc)[2][MT]) {
+                                                const uint32_t (&xa)[MT][8], int (&acc)[2][MT]) {
     const uint32_t s0 = meta & 0xFFu, add0 = ((meta >> 8) & 0xFFu) * 0x01010101u;
     const uint32_t s1 = (meta >> 16) & 0xFFu, add1 = (meta >> 24) * 0x01010101u;
     const uint32_t x[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
@@ -352,9 +355,8 @@ __device__ __forceinline__ void w4a8_block_dp4a(const uint4 (&w)[2], uint32_t me
         const int w1 = static_cast<int>(biased_i8x4((x[j] >> 4) & 0x0F0F0F0Fu, s1, add1) ^ 0x80808080u);
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-            const int a = *reinterpret_cast<const int*>(a_s + m * kW4a8ARow + 16 * j);
-            acc[0][m] = __dp4a(w0, a, acc[0][m]);
-            acc[1][m] = __dp4a(w1, a, acc[1][m]);
+            acc[0][m] = __dp4a(w0, static_cast<int>(xa[m][j]), acc[0][m]);
+            acc[1][m] = __dp4a(w1, static_cast<int>(xa[m][j]), acc[1][m]);
         }
     }
 }
@@ -414,7 +416,7 @@ __device__ __forceinline__ uint16_t w4a8_f32_to_dtype(float v) {
 // Epilogue per output element: fp32(acc) * s_a[m] * s_w[n], two fp32 multiplies rounded
 // to nearest even, then one rounding to the output dtype.
 template <int MT, int DT>
-__global__ void __launch_bounds__(kW4a8Threads, MT <= 2 ? 4 : 3) w4a8_gemm_kernel(
+__global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kernel(
     const int8_t* __restrict__ A_i8, const float* __restrict__ s_a,
     const uint8_t* __restrict__ packed, uint16_t* __restrict__ Y, int* status, int M, int N,
     int K) {
@@ -460,8 +462,8 @@ __global__ void __launch_bounds__(kW4a8Threads, MT <= 2 ? 4 : 3) w4a8_gemm_kerne
                            A_i8 + static_cast<size_t>(m) * K + k0 + c * 16);
         }
     };
-    // Rows M..MT-1 of both buffers stay zero for the whole kernel.
-    for (int e = tid; e < (MT - M) * kPieces * 2; e += kW4a8Threads) {
+    // Rows M..MT-1 of both buffers stay zero for the whole kernel (MMA path).
+    for (int e = tid; kMma && e < (MT - M) * kPieces * 2; e += kW4a8Threads) {
         const int per_buf = (MT - M) * kPieces;
         const int bsel = e / per_buf, rem = e % per_buf;
         const int m = M + rem / kPieces, c = rem % kPieces;
@@ -486,29 +488,62 @@ __global__ void __launch_bounds__(kW4a8Threads, MT <= 2 ? 4 : 3) w4a8_gemm_kerne
     if (slot < kblocks) load(slot, wa, ma);
     if (slot + kW4a8Warps < kblocks) load(slot + kW4a8Warps, wb, mb);
     grid_dep_wait();  // A_i8 and s_a (and Y) belong to the previous kernel until here
-    stage(0);
-    cp_async_commit();
-    for (int rr = 0; rr < rounds; ++rr) {
-        if (rr + 1 < rounds) stage(rr + 1);
-        cp_async_commit();      // (an empty group in the last round)
-        cp_async_wait<1>();     // this thread's copies of round rr have landed ...
-        __syncthreads();        // ... and every other thread's
-        const int kb = rr * kW4a8Warps + slot;
-        if (kb < kblocks) {
-            const uint8_t* a_s = a_smem + (rr & 1) * kBuf + slot * kW4a8Group + 4 * i;
-            if (rr & 1) {
-                if constexpr (kMma) w4a8_block_mma<NT>(wb, mb, a_s + g * kW4a8ARow, iacc);
-                else w4a8_block_dp4a<MT>(wb, mb, a_s, acc);
-                if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wb, mb);
-            } else {
-                if constexpr (kMma) w4a8_block_mma<NT>(wa, ma, a_s + g * kW4a8ARow, iacc);
-                else w4a8_block_dp4a<MT>(wa, ma, a_s, acc);
-                if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wa, ma);
+    if constexpr (kMma) {
+        stage(0);
+        cp_async_commit();
+        for (int rr = 0; rr < rounds; ++rr) {
+            if (rr + 1 < rounds) stage(rr + 1);
+            cp_async_commit();      // (an empty group in the last round)
+            cp_async_wait<1>();     // this thread's copies of round rr have landed ...
+            __syncthreads();        // ... and every other thread's
+            const int kb = rr * kW4a8Warps + slot;
+            if (kb < kblocks) {
+                const uint8_t* a_s =
+                    a_smem + (rr & 1) * kBuf + slot * kW4a8Group + 4 * i + g * kW4a8ARow;
+                if (rr & 1) {
+                    w4a8_block_mma<NT>(wb, mb, a_s, iacc);
+                    if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wb, mb);
+                } else {
+                    w4a8_block_mma<NT>(wa, ma, a_s, iacc);
+                    if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wa, ma);
+                }
+            }
+            __syncthreads();        // buffer rr & 1 is free for round rr + 2
+        }
+        cp_async_wait<0>();
+    } else {
+        // One or two rows: no shared staging and no barrier in the loop.  Each lane loads
+        // the activation words its blocks need (K values 16j + 4i .. +3 of every row)
+        // from global memory, L1-cached (every CTA reads the same rows), together with the
+        // block's codes and one block ahead; the warps of a CTA run independently.
+        uint32_t xa[MT][8], xb[MT][8];
+        auto load_a = [&](int kb, uint32_t (&xr)[MT][8]) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    xr[m][j] = m < M ? __ldg(reinterpret_cast<const unsigned int*>(
+                                           A_i8 + static_cast<size_t>(m) * K + kb * kW4a8Group +
+                                           16 * j + 4 * i))
+                                     : 0u;
+        };
+        if (slot < kblocks) load_a(slot, xa);
+        if (slot + kW4a8Warps < kblocks) load_a(slot + kW4a8Warps, xb);
+        for (int kb = slot; kb < kblocks; kb += 2 * kW4a8Warps) {
+            w4a8_block_dp4a<MT>(wa, ma, xa, acc);
+            if (kb + 2 * kW4a8Warps < kblocks) {
+                load(kb + 2 * kW4a8Warps, wa, ma);
+                load_a(kb + 2 * kW4a8Warps, xa);
+            }
+            if (kb + kW4a8Warps < kblocks) {
+                w4a8_block_dp4a<MT>(wb, mb, xb, acc);
+                if (kb + 3 * kW4a8Warps < kblocks) {
+                    load(kb + 3 * kW4a8Warps, wb, mb);
+                    load_a(kb + 3 * kW4a8Warps, xb);
+                }
             }
         }
-        __syncthreads();        // buffer rr & 1 is free for round rr + 2
     }
-    cp_async_wait<0>();
     // The activation buffers are reused for the warps' partials: red[slot][channel][row].
     int* red = reinterpret_cast<int*>(a_smem);
     if constexpr (kMma) {
