@@ -313,14 +313,21 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// 16 activation rows (two MMA groups) are staged in shared memory instead of being held in
+// registers (their register copies would cost the CTA its third slot on an SM).
+template <int MT>
+constexpr bool w4a8_staged() { return MT == 16; }
+
 // One round of staged int8 activations per row: the K values of one block per K slot,
 // padded by 16 bytes so that the eight rows an MMA fragment reads fall in distinct banks.
 constexpr uint32_t kW4a8ARow = kW4a8Warps * kW4a8Group + 16;  // 1040
 
-// Dynamic shared memory of a GEMM CTA: the two activation buffers of the MMA path, or
-// only the warps' partials (8 slots x 16 channels x MT rows of int32) of the dp4a path.
-__host__ __device__ constexpr uint32_t w4a8_smem_bytes(int MT) {
-    return MT >= 8 ? 2u * MT * kW4a8ARow : 512u * MT;
+// Dynamic shared memory of a GEMM CTA: two rounds of staged activations (16 rows), else
+// only the warps' partials (8 slots x 16 channels x MT rows of int32), which reuse the
+// staging buffers where there are any.
+template <int MT>
+constexpr uint32_t w4a8_smem_bytes() {
+    return w4a8_staged<MT>() ? 2u * MT * kW4a8ARow : 512u * MT;
 }
 
 // Two biased int8 values (bytes sel picks, each v + 128) -> their values as an fp16 pair:
@@ -363,13 +370,13 @@ __device__ __forceinline__ void w4a8_block_dp4a(const uint4 (&w)[2], uint32_t me
 
 // One 128-K block of the warp's 16 channels with NT groups of 8 activation rows, by f16
 // mma.sync (m16n8k16): the weights, as int8 values in fp16, are the A fragments (rows g
-// and g + 8 of the tile), the activations the B fragments (row 8t + g of group t).  The
-// block's sums are accumulated in fp32 from zero (exact: every partial sum is an integer
-// below 2^24) and then added to iacc in int32.  a_s: the block's staged activations at
-// this lane's K offset 4i and row g (group t at + 8t rows).
+// and g + 8 of the tile), the activations the B fragments (row 8t + g of group t; xa[t][j]
+// holds its four int8 values at this lane's K offset of step j).  The block's sums are
+// accumulated in fp32 from zero (exact: every partial sum is an integer below 2^24) and
+// then added to iacc in int32.
 template <int NT>
 __device__ __forceinline__ void w4a8_block_mma(const uint4 (&w)[2], uint32_t meta,
-                                               const uint8_t* a_s, int (&iacc)[NT][4]) {
+                                               const uint32_t (&xa)[NT][8], int (&iacc)[NT][4]) {
     const uint32_t s0 = meta & 0xFFu, add0 = ((meta >> 8) & 0xFFu) * 0x01010101u;
     const uint32_t s1 = (meta >> 16) & 0xFFu, add1 = (meta >> 24) * 0x01010101u;
     const uint32_t x[8] = {w[0].x, w[0].y, w[0].z, w[0].w, w[1].x, w[1].y, w[1].z, w[1].w};
@@ -388,8 +395,7 @@ __device__ __forceinline__ void w4a8_block_mma(const uint4 (&w)[2], uint32_t met
         const uint32_t a3 = biased_u8x2_to_f16x2(u1, 0x4342u);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-            const uint32_t av =
-                *reinterpret_cast<const uint32_t*>(a_s + 8 * t * kW4a8ARow + 16 * j) ^ 0x80808080u;
+            const uint32_t av = xa[t][j] ^ 0x80808080u;
             mma_f16_16x8x16(f[t], a0, a1, a2, a3, biased_u8x2_to_f16x2(av, 0x4140u),
                             biased_u8x2_to_f16x2(av, 0x4342u));
         }
@@ -407,12 +413,12 @@ __device__ __forceinline__ uint16_t w4a8_f32_to_dtype(float v) {
 }
 
 // Work split.  A CTA owns one 16-channel tile over the whole K range; its 8 warps are K
-// slots taking the 128-K blocks in rounds (round r: block 8r + warp).  Each lane keeps
-// its 32 bytes of codes of two rounds in flight in registers (the loads of round r + 2
-// are issued as soon as round r is multiplied); the CTA stages each round's int8
-// activations in shared memory with cp.async, one round ahead, rows M..MT-1 zero.  MT
-// is 1 or 2 (dp4a) or 8 or 16 (f16 mma.sync, one or two groups of 8 rows).  The warps'
-// int32 partials are summed in shared memory (exact, so the order does not matter).
+// slots taking the 128-K blocks slot, slot + 8, ...  Each lane keeps the codes (32
+// bytes) of two blocks in flight in registers: the loads for block b + 2 are issued as
+// soon as block b is multiplied.  The activations travel the same way (up to 8 rows) or
+// are staged per round of 8 blocks in shared memory (16 rows).  MT is 1 or 2 (dp4a) or 8 or
+// 16 (f16 mma.sync, one or two groups of 8 rows).  The warps' int32 partials are summed
+// in shared memory (exact, so the order does not matter).
 // Epilogue per output element: fp32(acc) * s_a[m] * s_w[n], two fp32 multiplies rounded
 // to nearest even, then one rounding to the output dtype.
 template <int MT, int DT>
@@ -422,9 +428,8 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
     int K) {
     constexpr bool kMma = MT >= 8;
     constexpr int NT = kMma ? MT / 8 : 1;
-    constexpr uint32_t kBuf = MT * kW4a8ARow;
-    constexpr int kPieces = static_cast<int>(kW4a8Warps * kW4a8Group / 16);  // per row and round
     extern __shared__ __align__(16) uint8_t a_smem[];
+    int* red = reinterpret_cast<int*>(a_smem);  // the warps' partials, after the main loop
     __shared__ int s_ok;
     const int tid = static_cast<int>(threadIdx.x);
     const int slot = tid >> 5, l = tid & 31;
@@ -441,7 +446,6 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
     if (tid == 0) grid_dep_launch();
 
     const int kblocks = K / kW4a8Group;
-    const int rounds = (kblocks + kW4a8Warps - 1) / kW4a8Warps;
     const uint8_t* tile_p = packed + 128 + static_cast<size_t>(tile) * kblocks * kW4a8BlockBytes;
     auto load = [&](int kb, uint4 (&w)[2], uint32_t& meta) {
         const uint8_t* blk = tile_p + static_cast<size_t>(kb) * kW4a8BlockBytes;
@@ -449,28 +453,6 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
         w[1] = ld_stream_v4(blk + 32 * l + 16);
         meta = ld_stream_u32(blk + kW4a8CodeBytes + 4 * g);
     };
-    const uint32_t smem = smem_addr(a_smem);
-    // The activations of round rr into buffer rr & 1 (rows m < M; pieces past K, in the
-    // last round only, are skipped: no block reads them).
-    auto stage = [&](int rr) {
-        const int k0 = rr * kW4a8Warps * kW4a8Group;
-        const uint32_t buf = smem + (rr & 1) * kBuf;
-        for (int e = tid; e < M * kPieces; e += kW4a8Threads) {
-            const int m = e / kPieces, c = e % kPieces;
-            if (k0 + c * 16 < K)
-                cp_async16(buf + m * kW4a8ARow + c * 16,
-                           A_i8 + static_cast<size_t>(m) * K + k0 + c * 16);
-        }
-    };
-    // Rows M..MT-1 of both buffers stay zero for the whole kernel (MMA path).
-    for (int e = tid; kMma && e < (MT - M) * kPieces * 2; e += kW4a8Threads) {
-        const int per_buf = (MT - M) * kPieces;
-        const int bsel = e / per_buf, rem = e % per_buf;
-        const int m = M + rem / kPieces, c = rem % kPieces;
-        *reinterpret_cast<uint4*>(a_smem + bsel * kBuf + m * kW4a8ARow + c * 16) =
-            make_uint4(0, 0, 0, 0);
-    }
-
     int acc[2][kMma ? 1 : MT];   // dp4a: channel g + 8h, row m
     int iacc[NT][4];             // mma: D fragment of group t
 #pragma unroll
@@ -483,12 +465,35 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
         for (int e = 0; e < 4; ++e) iacc[t][e] = 0;
     uint4 wa[2], wb[2];
     uint32_t ma = 0, mb = 0;
-    // The packed weights do not depend on the previous kernel: the first two rounds are
-    // requested before the dependency wait.
+    // The packed weights do not depend on the previous kernel: the codes of the first two
+    // blocks are requested before the dependency wait.
     if (slot < kblocks) load(slot, wa, ma);
     if (slot + kW4a8Warps < kblocks) load(slot + kW4a8Warps, wb, mb);
     grid_dep_wait();  // A_i8 and s_a (and Y) belong to the previous kernel until here
-    if constexpr (kMma) {
+    if constexpr (w4a8_staged<MT>()) {
+        // Rounds of 8 blocks (one per warp); each round's activations are staged by the
+        // whole CTA with cp.async one round ahead, rows M..15 zero.
+        constexpr uint32_t kBuf = MT * kW4a8ARow;
+        constexpr int kPieces = static_cast<int>(kW4a8Warps * kW4a8Group / 16);  // per row
+        const int rounds = (kblocks + kW4a8Warps - 1) / kW4a8Warps;
+        const uint32_t smem = smem_addr(a_smem);
+        auto stage = [&](int rr) {
+            const int k0 = rr * kW4a8Warps * kW4a8Group;
+            const uint32_t buf = smem + (rr & 1) * kBuf;
+            for (int e = tid; e < M * kPieces; e += kW4a8Threads) {
+                const int m = e / kPieces, c = e % kPieces;
+                if (k0 + c * 16 < K)  // pieces past K (last round only) are never read
+                    cp_async16(buf + m * kW4a8ARow + c * 16,
+                               A_i8 + static_cast<size_t>(m) * K + k0 + c * 16);
+            }
+        };
+        for (int e = tid; e < (MT - M) * kPieces * 2; e += kW4a8Threads) {
+            const int per_buf = (MT - M) * kPieces;
+            const int bsel = e / per_buf, rem = e % per_buf;
+            const int m = M + rem / kPieces, c = rem % kPieces;
+            *reinterpret_cast<uint4*>(a_smem + bsel * kBuf + m * kW4a8ARow + c * 16) =
+                make_uint4(0, 0, 0, 0);
+        }
         stage(0);
         cp_async_commit();
         for (int rr = 0; rr < rounds; ++rr) {
@@ -500,11 +505,17 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
             if (kb < kblocks) {
                 const uint8_t* a_s =
                     a_smem + (rr & 1) * kBuf + slot * kW4a8Group + 4 * i + g * kW4a8ARow;
+                uint32_t xs[NT][8];
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        xs[t][j] = *reinterpret_cast<const uint32_t*>(a_s + 8 * t * kW4a8ARow + 16 * j);
                 if (rr & 1) {
-                    w4a8_block_mma<NT>(wb, mb, a_s, iacc);
+                    w4a8_block_mma<NT>(wb, mb, xs, iacc);
                     if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wb, mb);
                 } else {
-                    w4a8_block_mma<NT>(wa, ma, a_s, iacc);
+                    w4a8_block_mma<NT>(wa, ma, xs, iacc);
                     if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wa, ma);
                 }
             }
@@ -512,31 +523,39 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
         }
         cp_async_wait<0>();
     } else {
-        // One or two rows: no shared staging and no barrier in the loop.  Each lane loads
-        // the activation words its blocks need (K values 16j + 4i .. +3 of every row)
-        // from global memory, L1-cached (every CTA reads the same rows), together with the
-        // block's codes and one block ahead; the warps of a CTA run independently.
-        uint32_t xa[MT][8], xb[MT][8];
-        auto load_a = [&](int kb, uint32_t (&xr)[MT][8]) {
-#pragma unroll
-            for (int m = 0; m < MT; ++m)
-#pragma unroll
+        // Each lane loads the activation words its blocks need -- K values 16j + 4i .. +3 of
+        // row r (dp4a: every row; MMA: row 8t + g of group t) -- from global memory, L1-cached
+        // (every CTA reads the same rows), together with the block's codes and one block
+        // ahead; rows past M read as zero.  The warps of a CTA run independently until the
+        // final reduction.
+        constexpr int R = kMma ? NT : MT;
+        uint32_t xa[R][8], xb[R][8];
+        auto load_a = [&](int kb, uint32_t (&xr)[R][8]) {
+    #pragma unroll
+            for (int q = 0; q < R; ++q) {
+                const int row = kMma ? 8 * q + g : q;
+    #pragma unroll
                 for (int j = 0; j < 8; ++j)
-                    xr[m][j] = m < M ? __ldg(reinterpret_cast<const unsigned int*>(
-                                           A_i8 + static_cast<size_t>(m) * K + kb * kW4a8Group +
-                                           16 * j + 4 * i))
-                                     : 0u;
+                    xr[q][j] = row < M ? __ldg(reinterpret_cast<const unsigned int*>(
+                                             A_i8 + static_cast<size_t>(row) * K + kb * kW4a8Group +
+                                             16 * j + 4 * i))
+                                       : 0u;
+            }
+        };
+        auto block = [&](const uint4 (&w)[2], uint32_t meta, const uint32_t (&xr)[R][8]) {
+            if constexpr (kMma) w4a8_block_mma<NT>(w, meta, xr, iacc);
+            else w4a8_block_dp4a<MT>(w, meta, xr, acc);
         };
         if (slot < kblocks) load_a(slot, xa);
         if (slot + kW4a8Warps < kblocks) load_a(slot + kW4a8Warps, xb);
         for (int kb = slot; kb < kblocks; kb += 2 * kW4a8Warps) {
-            w4a8_block_dp4a<MT>(wa, ma, xa, acc);
+            block(wa, ma, xa);
             if (kb + 2 * kW4a8Warps < kblocks) {
                 load(kb + 2 * kW4a8Warps, wa, ma);
                 load_a(kb + 2 * kW4a8Warps, xa);
             }
             if (kb + kW4a8Warps < kblocks) {
-                w4a8_block_dp4a<MT>(wb, mb, xb, acc);
+                block(wb, mb, xb);
                 if (kb + 3 * kW4a8Warps < kblocks) {
                     load(kb + 3 * kW4a8Warps, wb, mb);
                     load_a(kb + 3 * kW4a8Warps, xb);
@@ -544,8 +563,7 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
             }
         }
     }
-    // The activation buffers are reused for the warps' partials: red[slot][channel][row].
-    int* red = reinterpret_cast<int*>(a_smem);
+    // The warps' partials: red[slot][channel][row].
     if constexpr (kMma) {
 #pragma unroll
         for (int t = 0; t < NT; ++t)
@@ -584,7 +602,7 @@ template <int MT, int DT>
 int launch_w4a8_instance(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
                          const void* packed, int M, int N, int K, void* Y, cudaStream_t stream) {
     auto kern = w4a8_gemm_kernel<MT, DT>;
-    constexpr uint32_t smem = w4a8_smem_bytes(MT);
+    constexpr uint32_t smem = w4a8_smem_bytes<MT>();
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(w4a8_tiles(N)), 1, 1);
     cfg.blockDim = dim3(kW4a8Threads, 1, 1);
