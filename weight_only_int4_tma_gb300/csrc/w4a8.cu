@@ -21,21 +21,23 @@
 //   blocks              one per (16-channel tile t, 128-K block kb), tiles in order,
 //                       blocks of one tile contiguous along K; kW4a8BlockBytes each:
 //     [0, 1024)         codes in the mma.sync fragment order: lane l = 4g + i (g = l / 4,
-//                       i = l % 4) owns 32 bytes at 32 l, one word per 16-K step j; byte
-//                       b of word j holds the codes of K value 16 j + 4 i + b of channel
-//                       g (low nibble) and of channel g + 8 (high nibble).  So
+//                       i = l % 4) owns 32 bytes at 32 l, one word per MMA step j; byte b
+//                       of word j holds the codes of K value 32 i + 4 j + b of channel g
+//                       (low nibble) and of channel g + 8 (high nibble).  So
 //                       (x & 0x0F0F0F0F) and ((x >> 4) & 0x0F0F0F0F) are four codes of
-//                       one channel in K order, and a warp reads a block as 1 KB of
-//                       contiguous 32-byte pieces.
+//                       one channel in K order, a lane's eight words cover 32 consecutive
+//                       K values (the activations it needs are 32 contiguous bytes per
+//                       row), and a warp reads a block as 1 KB of contiguous 32-byte
+//                       pieces.
 //     [1024, 1056)      word g: step and offset of channel g (bytes 0, 1) and of
 //                       channel g + 8 (bytes 2, 3).
 //   s_w                 fp32 [Np], the per-channel scale (0 past N).
 // N is padded to Np = a multiple of 16 (padded channels: codes 0, step 1, offset 128, so
 // their int8 weights are exactly 0); K must be a multiple of 128 (one group per block).
 //
-// Within a 16-K step the MMA's K index k' = 2i + e (e = 0, 1) stands for K value 4i + e
-// and k' = 8 + 2i + e for 4i + 2 + e, for the weights and the activations alike; a sum
-// over K does not depend on the order of its terms, and these sums are exact.
+// In MMA step j the MMA's K index k' = 2i + e (e = 0, 1) stands for K value 32i + 4j + e
+// and k' = 8 + 2i + e for 32i + 4j + 2 + e, for the weights and the activations alike; a
+// sum over K does not depend on the order of its terms, and these sums are exact.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -101,7 +103,7 @@ __device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
 // ---- repack ------------------------------------------------------------------------
 
 // One CTA per (tile, block); thread (j, l) = (tid / 32, tid % 32) writes word j of lane
-// l: the codes of K values 16 j + 4 i + (0..3) of channels g and g + 8 (g = l / 4,
+// l: the codes of K values 32 i + 4 j + (0..3) of channels g and g + 8 (g = l / 4,
 // i = l % 4).  Lanes 4g of step 0 also write the step and offset word g, and in block 0
 // of the tile the two channels' s_w.  Codes whose byte value code * s + a would pass
 // 255, and steps outside 1..16, are recorded as W4A16_ERR_INVALID_ARG in the status word
@@ -117,7 +119,7 @@ __global__ void __launch_bounds__(256) w4a8_repack_kernel(
     const int l = static_cast<int>(threadIdx.x) & 31;
     const int g = l >> 2, i = l & 3;
     uint8_t* blk = packed + 128 + static_cast<size_t>(blockIdx.x) * kW4a8BlockBytes;
-    const int k0 = kb * kW4a8Group + 16 * j + 4 * i;  // first of the four K values
+    const int k0 = kb * kW4a8Group + 32 * i + 4 * j;  // first of the four K values
     uint32_t codes[2], sv[2], av[2];
     bool bad = false;
 #pragma unroll
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(256) w4a8_dequant_debug_kernel(
                                     ((meta >> 8) & 0xFFu) * 0x01010101u) ^ 0x80808080u;
     const uint32_t w1 = biased_i8x4((x >> 4) & 0x0F0F0F0Fu, (meta >> 16) & 0xFFu,
                                     (meta >> 24) * 0x01010101u) ^ 0x80808080u;
-    const int k0 = kb * kW4a8Group + 16 * j + 4 * i;
+    const int k0 = kb * kW4a8Group + 32 * i + 4 * j;
     const int n0 = t * kW4a8TileN + g;
     if (n0 < N) *reinterpret_cast<uint32_t*>(W + static_cast<size_t>(n0) * K + k0) = w0;
     if (n0 + 8 < N) *reinterpret_cast<uint32_t*>(W + static_cast<size_t>(n0 + 8) * K + k0) = w1;
@@ -349,7 +351,7 @@ __device__ __forceinline__ void mma_f16_16x8x16(float (&d)[4], uint32_t a0, uint
 
 // One 128-K block of this lane's two channels (g and g + 8) with MT <= 2 activation rows,
 // by dp4a: acc[h][m] += the int8 products of channel g + 8h with row m over the lane's
-// four K values of each 16-K step j; xa[m][j]: those four activations of row m.
+// four K values of each step j; xa[m][j]: those four activations of row m.
 template <int MT>
 __device__ __forceinline__ void w4a8_block_dp4a(const uint4 (&w)[2], uint32_t meta,
                                                 const uint32_t (&xa)[MT][8], int (&acc)[2][MT]) {
@@ -504,13 +506,15 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
             const int kb = rr * kW4a8Warps + slot;
             if (kb < kblocks) {
                 const uint8_t* a_s =
-                    a_smem + (rr & 1) * kBuf + slot * kW4a8Group + 4 * i + g * kW4a8ARow;
+                    a_smem + (rr & 1) * kBuf + slot * kW4a8Group + 32 * i + g * kW4a8ARow;
                 uint32_t xs[NT][8];
 #pragma unroll
-                for (int t = 0; t < NT; ++t)
-#pragma unroll
-                    for (int j = 0; j < 8; ++j)
-                        xs[t][j] = *reinterpret_cast<const uint32_t*>(a_s + 8 * t * kW4a8ARow + 16 * j);
+                for (int t = 0; t < NT; ++t) {
+                    const uint4* p = reinterpret_cast<const uint4*>(a_s + 8 * t * kW4a8ARow);
+                    const uint4 lo = p[0], hi = p[1];
+                    xs[t][0] = lo.x; xs[t][1] = lo.y; xs[t][2] = lo.z; xs[t][3] = lo.w;
+                    xs[t][4] = hi.x; xs[t][5] = hi.y; xs[t][6] = hi.z; xs[t][7] = hi.w;
+                }
                 if (rr & 1) {
                     w4a8_block_mma<NT>(wb, mb, xs, iacc);
                     if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wb, mb);
@@ -523,23 +527,26 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
         }
         cp_async_wait<0>();
     } else {
-        // Each lane loads the activation words its blocks need -- K values 16j + 4i .. +3 of
-        // row r (dp4a: every row; MMA: row 8t + g of group t) -- from global memory, L1-cached
+        // Each lane loads the activation words its blocks need -- K values 32i .. 32i + 31
+        // of row r (dp4a: every row; MMA: row 8t + g of group t) -- from global memory, L1-cached
         // (every CTA reads the same rows), together with the block's codes and one block
         // ahead; rows past M read as zero.  The warps of a CTA run independently until the
         // final reduction.
         constexpr int R = kMma ? NT : MT;
         uint32_t xa[R][8], xb[R][8];
         auto load_a = [&](int kb, uint32_t (&xr)[R][8]) {
-    #pragma unroll
+#pragma unroll
             for (int q = 0; q < R; ++q) {
                 const int row = kMma ? 8 * q + g : q;
-    #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    xr[q][j] = row < M ? __ldg(reinterpret_cast<const unsigned int*>(
-                                             A_i8 + static_cast<size_t>(row) * K + kb * kW4a8Group +
-                                             16 * j + 4 * i))
-                                       : 0u;
+                uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+                if (row < M) {
+                    const uint4* p = reinterpret_cast<const uint4*>(
+                        A_i8 + static_cast<size_t>(row) * K + kb * kW4a8Group + 32 * i);
+                    lo = __ldg(p);
+                    hi = __ldg(p + 1);
+                }
+                xr[q][0] = lo.x; xr[q][1] = lo.y; xr[q][2] = lo.z; xr[q][3] = lo.w;
+                xr[q][4] = hi.x; xr[q][5] = hi.y; xr[q][6] = hi.z; xr[q][7] = hi.w;
             }
         };
         auto block = [&](const uint4 (&w)[2], uint32_t meta, const uint32_t (&xr)[R][8]) {
