@@ -306,31 +306,10 @@ __global__ void __launch_bounds__(kQuantThreads) w4a8_quantize_kernel(
 
 // ---- the GEMM ----------------------------------------------------------------------
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
-// 16 activation rows (two MMA groups) are staged in shared memory instead of being held in
-// registers (their register copies would cost the CTA its third slot on an SM).
+// Dynamic shared memory of a GEMM CTA: the warps' partials, 8 slots x 16 channels x MT
+// rows of int32.
 template <int MT>
-constexpr bool w4a8_staged() { return MT == 16; }
-
-// One round of staged int8 activations per row: the K values of one block per K slot,
-// padded by 16 bytes so that the eight rows an MMA fragment reads fall in distinct banks.
-constexpr uint32_t kW4a8ARow = kW4a8Warps * kW4a8Group + 16;  // 1040
-
-// Dynamic shared memory of a GEMM CTA: two rounds of staged activations (16 rows), else
-// only the warps' partials (8 slots x 16 channels x MT rows of int32), which reuse the
-// staging buffers where there are any.
-template <int MT>
-constexpr uint32_t w4a8_smem_bytes() {
-    return w4a8_staged<MT>() ? 2u * MT * kW4a8ARow : 512u * MT;
-}
+constexpr uint32_t w4a8_smem_bytes() { return 512u * MT; }
 
 // Two biased int8 values (bytes sel picks, each v + 128) -> their values as an fp16 pair:
 // 0x6400 | byte is 1024 + byte exactly, and subtracting 1152 leaves v exactly.
@@ -417,10 +396,10 @@ __device__ __forceinline__ uint16_t w4a8_f32_to_dtype(float v) {
 // Work split.  A CTA owns one 16-channel tile over the whole K range; its 8 warps are K
 // slots taking the 128-K blocks slot, slot + 8, ...  Each lane keeps the codes (32
 // bytes) of two blocks in flight in registers: the loads for block b + 2 are issued as
-// soon as block b is multiplied.  The activations travel the same way (up to 8 rows) or
-// are staged per round of 8 blocks in shared memory (16 rows).  MT is 1 or 2 (dp4a) or 8 or
-// 16 (f16 mma.sync, one or two groups of 8 rows).  The warps' int32 partials are summed
-// in shared memory (exact, so the order does not matter).
+// soon as block b is multiplied.  The activation words a lane needs travel the same way,
+// read through L1, two blocks ahead (one for 16 rows, to keep three CTAs on an SM).  MT
+// is 1 or 2 (dp4a) or 8 or 16 (f16 mma.sync, one or two groups of 8 rows).  The warps'
+// int32 partials are summed in shared memory (exact, so the order does not matter).
 // Epilogue per output element: fp32(acc) * s_a[m] * s_w[n], two fp32 multiplies rounded
 // to nearest even, then one rounding to the output dtype.
 template <int MT, int DT>
@@ -430,8 +409,7 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
     int K) {
     constexpr bool kMma = MT >= 8;
     constexpr int NT = kMma ? MT / 8 : 1;
-    extern __shared__ __align__(16) uint8_t a_smem[];
-    int* red = reinterpret_cast<int*>(a_smem);  // the warps' partials, after the main loop
+    extern __shared__ __align__(16) int red[];  // the warps' partials, after the main loop
     __shared__ int s_ok;
     const int tid = static_cast<int>(threadIdx.x);
     const int slot = tid >> 5, l = tid & 31;
@@ -472,68 +450,14 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
     if (slot < kblocks) load(slot, wa, ma);
     if (slot + kW4a8Warps < kblocks) load(slot + kW4a8Warps, wb, mb);
     grid_dep_wait();  // A_i8 and s_a (and Y) belong to the previous kernel until here
-    if constexpr (w4a8_staged<MT>()) {
-        // Rounds of 8 blocks (one per warp); each round's activations are staged by the
-        // whole CTA with cp.async one round ahead, rows M..15 zero.
-        constexpr uint32_t kBuf = MT * kW4a8ARow;
-        constexpr int kPieces = static_cast<int>(kW4a8Warps * kW4a8Group / 16);  // per row
-        const int rounds = (kblocks + kW4a8Warps - 1) / kW4a8Warps;
-        const uint32_t smem = smem_addr(a_smem);
-        auto stage = [&](int rr) {
-            const int k0 = rr * kW4a8Warps * kW4a8Group;
-            const uint32_t buf = smem + (rr & 1) * kBuf;
-            for (int e = tid; e < M * kPieces; e += kW4a8Threads) {
-                const int m = e / kPieces, c = e % kPieces;
-                if (k0 + c * 16 < K)  // pieces past K (last round only) are never read
-                    cp_async16(buf + m * kW4a8ARow + c * 16,
-                               A_i8 + static_cast<size_t>(m) * K + k0 + c * 16);
-            }
-        };
-        for (int e = tid; e < (MT - M) * kPieces * 2; e += kW4a8Threads) {
-            const int per_buf = (MT - M) * kPieces;
-            const int bsel = e / per_buf, rem = e % per_buf;
-            const int m = M + rem / kPieces, c = rem % kPieces;
-            *reinterpret_cast<uint4*>(a_smem + bsel * kBuf + m * kW4a8ARow + c * 16) =
-                make_uint4(0, 0, 0, 0);
-        }
-        stage(0);
-        cp_async_commit();
-        for (int rr = 0; rr < rounds; ++rr) {
-            if (rr + 1 < rounds) stage(rr + 1);
-            cp_async_commit();      // (an empty group in the last round)
-            cp_async_wait<1>();     // this thread's copies of round rr have landed ...
-            __syncthreads();        // ... and every other thread's
-            const int kb = rr * kW4a8Warps + slot;
-            if (kb < kblocks) {
-                const uint8_t* a_s =
-                    a_smem + (rr & 1) * kBuf + slot * kW4a8Group + 32 * i + g * kW4a8ARow;
-                uint32_t xs[NT][8];
-#pragma unroll
-                for (int t = 0; t < NT; ++t) {
-                    const uint4* p = reinterpret_cast<const uint4*>(a_s + 8 * t * kW4a8ARow);
-                    const uint4 lo = p[0], hi = p[1];
-                    xs[t][0] = lo.x; xs[t][1] = lo.y; xs[t][2] = lo.z; xs[t][3] = lo.w;
-                    xs[t][4] = hi.x; xs[t][5] = hi.y; xs[t][6] = hi.z; xs[t][7] = hi.w;
-                }
-                if (rr & 1) {
-                    w4a8_block_mma<NT>(wb, mb, xs, iacc);
-                    if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wb, mb);
-                } else {
-                    w4a8_block_mma<NT>(wa, ma, xs, iacc);
-                    if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wa, ma);
-                }
-            }
-            __syncthreads();        // buffer rr & 1 is free for round rr + 2
-        }
-        cp_async_wait<0>();
-    } else {
+    {
         // Each lane loads the activation words its blocks need -- K values 32i .. 32i + 31
-        // of row r (dp4a: every row; MMA: row 8t + g of group t) -- from global memory, L1-cached
-        // (every CTA reads the same rows), together with the block's codes and one block
-        // ahead; rows past M read as zero.  The warps of a CTA run independently until the
-        // final reduction.
+        // of row r (dp4a: every row; MMA: row 8t + g of group t) -- from global memory,
+        // L1-cached (every CTA reads the same rows), ahead of the block that uses them;
+        // rows past M read as zero.  The warps of a CTA run independently until the final
+        // reduction.
         constexpr int R = kMma ? NT : MT;
-        uint32_t xa[R][8], xb[R][8];
+        uint32_t xa[R][8], xb[(R <= 1 || !kMma) ? R : 1][8];
         auto load_a = [&](int kb, uint32_t (&xr)[R][8]) {
 #pragma unroll
             for (int q = 0; q < R; ++q) {
@@ -553,19 +477,36 @@ __global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kerne
             if constexpr (kMma) w4a8_block_mma<NT>(w, meta, xr, iacc);
             else w4a8_block_dp4a<MT>(w, meta, xr, acc);
         };
-        if (slot < kblocks) load_a(slot, xa);
-        if (slot + kW4a8Warps < kblocks) load_a(slot + kW4a8Warps, xb);
-        for (int kb = slot; kb < kblocks; kb += 2 * kW4a8Warps) {
-            block(wa, ma, xa);
-            if (kb + 2 * kW4a8Warps < kblocks) {
-                load(kb + 2 * kW4a8Warps, wa, ma);
-                load_a(kb + 2 * kW4a8Warps, xa);
+        if constexpr (R <= 1 || !kMma) {
+            // activations two blocks ahead, like the codes
+            if (slot < kblocks) load_a(slot, xa);
+            if (slot + kW4a8Warps < kblocks) load_a(slot + kW4a8Warps, xb);
+            for (int kb = slot; kb < kblocks; kb += 2 * kW4a8Warps) {
+                block(wa, ma, xa);
+                if (kb + 2 * kW4a8Warps < kblocks) {
+                    load(kb + 2 * kW4a8Warps, wa, ma);
+                    load_a(kb + 2 * kW4a8Warps, xa);
+                }
+                if (kb + kW4a8Warps < kblocks) {
+                    block(wb, mb, xb);
+                    if (kb + 3 * kW4a8Warps < kblocks) {
+                        load(kb + 3 * kW4a8Warps, wb, mb);
+                        load_a(kb + 3 * kW4a8Warps, xb);
+                    }
+                }
             }
-            if (kb + kW4a8Warps < kblocks) {
-                block(wb, mb, xb);
-                if (kb + 3 * kW4a8Warps < kblocks) {
-                    load(kb + 3 * kW4a8Warps, wb, mb);
-                    load_a(kb + 3 * kW4a8Warps, xb);
+        } else {
+            // 16 rows: activations one block ahead in one set of registers (a second set
+            // would cost the CTA its third slot on an SM)
+            if (slot < kblocks) load_a(slot, xa);
+            for (int kb = slot; kb < kblocks; kb += 2 * kW4a8Warps) {
+                block(wa, ma, xa);
+                if (kb + kW4a8Warps < kblocks) load_a(kb + kW4a8Warps, xa);
+                if (kb + 2 * kW4a8Warps < kblocks) load(kb + 2 * kW4a8Warps, wa, ma);
+                if (kb + kW4a8Warps < kblocks) {
+                    block(wb, mb, xa);
+                    if (kb + 2 * kW4a8Warps < kblocks) load_a(kb + 2 * kW4a8Warps, xa);
+                    if (kb + 3 * kW4a8Warps < kblocks) load(kb + 3 * kW4a8Warps, wb, mb);
                 }
             }
         }
