@@ -246,12 +246,20 @@ class ClockSampler:
                 "sm_max_mhz": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel)}
 
 
-def kernel_source_hash():
+# Device-code sources of each kernel family: a traffic record applies only while these
+# are byte-for-byte the ones it was captured with.
+_KERNEL_SOURCES = {
+    "w4a8_gemm_kernel": ["w4a8.cu", "ptx.cuh"],
+}
+_W4A16_SOURCES = ["gemm_tc.cu", "gemv_simt.cu", "repack.cu", "dequant.cuh", "epilogue.cuh",
+                  "format.cuh", "ptx.cuh"]
+
+
+def kernel_source_hash(kernel="w4a16_tc_kernel"):
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "weight_only_int4_tma_gb300", "csrc")
-    for p in sorted(glob.glob(os.path.join(csrc, "*"))):
-        if p.endswith((".cu", ".cuh", ".h")):
-            h.update(open(p, "rb").read())
+    for name in _KERNEL_SOURCES.get(kernel, _W4A16_SOURCES):
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -262,7 +270,7 @@ def profiled_traffic(workload, kernel):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(workload)
-    if not d or d.get("kernel_source_hash") != kernel_source_hash() or d.get("kernel") != kernel:
+    if not d or d.get("kernel_source_hash") != kernel_source_hash(kernel) or d.get("kernel") != kernel:
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -811,7 +819,8 @@ def measure_w4a8(a, w4, device, stream, sampler, workload, steps, warmup):
     dom_s = sum(per_shape_us) * 1e-6 / len(per_shape_us)
     achieved = dom_bytes / dom_s / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                "frac": achieved / hbm_peak,
+                "traffic": profiled_traffic(workload, "w4a8_gemm_kernel"), "peak_kind": peak_kind,
                 "kernel": "w4a8_gemm_kernel", "launches_per_step": len(cases),
                 "algorithmic_bytes_per_launch": dom_bytes}
     value = step_bytes * steps * ws / (elapsed_ms * 1e-3) / 1e12
