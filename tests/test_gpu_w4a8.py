@@ -250,3 +250,32 @@ def test_repack_flags_codes_outside_a_byte():
     packed = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     w4.w4a8_repack(_dev(c.qweight), _dev(c.s_u8), _dev(c.a), _dev(c.s_w), c.N, c.K, packed)
     assert w4.w4a16_get_device_status() == w4.W4A16_ERR_INVALID_ARG
+
+
+def _random_configs(n=40, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        M = int(rng.integers(1, 17))
+        N = int(rng.integers(1, 400)) * 8
+        K = int(rng.integers(1, 49)) * 128
+        dt = int(rng.integers(0, 2))
+        zero = (int(rng.integers(0, M)),) if M > 1 and rng.random() < 0.3 else ()
+        steps = (1, int(rng.integers(1, 17)))
+        out.append((M, N, K, dt, zero, steps, int(rng.integers(0, 1 << 30))))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K,dt,zero,steps,seed", _random_configs(),
+                         ids=[f"m{m}_n{n}_k{k}_{si.DTYPE_NAMES[d]}" for m, n, k, d, *_ in
+                              _random_configs()])
+def test_gemm_random_configs_bitexact(M, N, K, dt, zero, steps, seed):
+    """Seeded random shapes (M 1..16, ragged N, K up to 6144), both dtypes, optional
+    all-zero rows and narrower step ranges: every element bit for bit."""
+    c = si.make_w4a8_case(M, N, K, dtype=dt, seed=seed, zero_rows=zero, steps=steps)
+    packed = _repack(c)
+    A_i8, s_a = _quantize(c)
+    Y = _gemm(c, packed, A_i8, s_a)
+    qa, sa = _oracle_act(c)
+    assert np.array_equal(A_i8.cpu().numpy().astype(np.int64), qa)
+    _assert_bits(Y, _oracle_y(c, qa, sa), "Y")
