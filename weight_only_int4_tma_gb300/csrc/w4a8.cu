@@ -221,12 +221,14 @@ __device__ __forceinline__ float dtype_bits_to_f32(uint32_t b) {
     else return __bfloat162float(__ushort_as_bfloat16(static_cast<unsigned short>(b)));
 }
 
-// One CTA of kQuantThreads threads per row m: amax = max |A[m, :]| (exact), s_a =
-// amax / 127 (1 for an all-zero row), A_i8 = rint(A / s_a) clipped to [-127, 127];
-// division and rounding in fp32, round to nearest even, as the oracle states them.
-// Rows of up to kQuantThreads * kQuantVec * 8 values are read once into registers (all
-// loads issued before the first is used); longer rows are read twice.
-constexpr int kQuantThreads = 512;
+// One thread-block cluster of kQuantCluster CTAs per row m, each CTA a slice of K/8
+// values: amax = max |A[m, :]| (exact; the CTAs' partial maxima are combined through
+// distributed shared memory), s_a = amax / 127 (1 for an all-zero row), A_i8 = rint(A /
+// s_a) clipped to [-127, 127]; division and rounding in fp32, round to nearest even, as
+// the oracle states them.  A slice is at most kQuantThreads * kQuantVec 16-byte pieces
+// (K <= 131072), read once into registers with every load issued before the first use.
+constexpr int kQuantCluster = 8;
+constexpr int kQuantThreads = 256;
 constexpr int kQuantVec = 8;  // 16-byte pieces per thread held in registers
 
 template <int DT>
@@ -258,27 +260,24 @@ template <int DT>
 __global__ void __launch_bounds__(kQuantThreads) w4a8_quantize_kernel(
     const uint16_t* __restrict__ A, int K, int8_t* __restrict__ A_i8, float* __restrict__ s_a) {
     __shared__ float wmax[kQuantThreads / 32];
+    __shared__ float part;   // this CTA's maximum, read by the whole cluster
     __shared__ float s_row;
     grid_dep_wait();  // A belongs to the previous kernel until here
-    const int m = static_cast<int>(blockIdx.x);
+    const int m = static_cast<int>(blockIdx.x) / kQuantCluster;
+    const uint32_t c = cluster_ctarank();
     const int tid = static_cast<int>(threadIdx.x);
-    const uint4* row = reinterpret_cast<const uint4*>(A + static_cast<size_t>(m) * K);
-    uint2* out = reinterpret_cast<uint2*>(A_i8 + static_cast<size_t>(m) * K);
-    const int nv = K / 8;
-    const bool in_regs = nv <= kQuantThreads * kQuantVec;
+    const int per = K / 8 / kQuantCluster;  // 16-byte pieces of this CTA's slice
+    const uint4* row = reinterpret_cast<const uint4*>(A + static_cast<size_t>(m) * K) + c * per;
+    uint2* out = reinterpret_cast<uint2*>(A_i8 + static_cast<size_t>(m) * K) + c * per;
     uint4 v[kQuantVec];
     float amax = 0.0f;
-    if (in_regs) {
 #pragma unroll
-        for (int j = 0; j < kQuantVec; ++j) {
-            const int i = tid + j * kQuantThreads;
-            v[j] = i < nv ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
-        }
-#pragma unroll
-        for (int j = 0; j < kQuantVec; ++j) amax = amax_piece<DT>(v[j], amax);
-    } else {
-        for (int i = tid; i < nv; i += kQuantThreads) amax = amax_piece<DT>(__ldg(row + i), amax);
+    for (int j = 0; j < kQuantVec; ++j) {
+        const int idx = tid + j * kQuantThreads;
+        v[j] = idx < per ? __ldg(row + idx) : make_uint4(0, 0, 0, 0);
     }
+#pragma unroll
+    for (int j = 0; j < kQuantVec; ++j) amax = amax_piece<DT>(v[j], amax);
 #pragma unroll
     for (int d = 16; d > 0; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, d));
     if ((tid & 31) == 0) wmax[tid >> 5] = amax;
@@ -286,21 +285,24 @@ __global__ void __launch_bounds__(kQuantThreads) w4a8_quantize_kernel(
     if (tid == 0) {
         float mx = wmax[0];
         for (int w = 1; w < kQuantThreads / 32; ++w) mx = fmaxf(mx, wmax[w]);
+        part = mx;
+    }
+    cluster_sync_all();  // every CTA's maximum is in place
+    if (tid == 0) {
+        float mx = 0.0f;
+        for (uint32_t r = 0; r < kQuantCluster; ++r)
+            mx = fmaxf(mx, ld_dsmem_f32(map_to_rank(smem_addr(&part), r)));
         const float s = mx > 0.0f ? __fdiv_rn(mx, 127.0f) : 1.0f;
         s_row = s;
-        s_a[m] = s;
+        if (c == 0) s_a[m] = s;
     }
-    __syncthreads();
+    cluster_sync_all();  // no CTA leaves while another may still read its maximum
     grid_dep_launch();
     const float s = s_row;
-    if (in_regs) {
 #pragma unroll
-        for (int j = 0; j < kQuantVec; ++j) {
-            const int i = tid + j * kQuantThreads;
-            if (i < nv) out[i] = quantize_piece<DT>(v[j], s);
-        }
-    } else {
-        for (int i = tid; i < nv; i += kQuantThreads) out[i] = quantize_piece<DT>(__ldg(row + i), s);
+    for (int j = 0; j < kQuantVec; ++j) {
+        const int idx = tid + j * kQuantThreads;
+        if (idx < per) out[idx] = quantize_piece<DT>(v[j], s);
     }
 }
 
@@ -604,14 +606,18 @@ int launch_w4a8_quantize(const DeviceCtx& ctx, const void* A, int M, int K, int 
                          int8_t* A_i8, float* s_a, cudaStream_t stream) {
     (void)ctx;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(M), 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(M) * kQuantCluster, 1, 1);
     cfg.blockDim = dim3(kQuantThreads, 1, 1);
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = kQuantCluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     const uint16_t* a = static_cast<const uint16_t*>(A);
     const cudaError_t e =
         dtype == 0 ? cudaLaunchKernelEx(&cfg, w4a8_quantize_kernel<0>, a, K, A_i8, s_a)
