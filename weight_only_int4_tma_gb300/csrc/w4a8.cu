@@ -405,7 +405,7 @@ __device__ __forceinline__ uint16_t w4a8_f32_to_dtype(float v) {
 // Epilogue per output element: fp32(acc) * s_a[m] * s_w[n], two fp32 multiplies rounded
 // to nearest even, then one rounding to the output dtype.
 template <int MT, int DT>
-__global__ void __launch_bounds__(kW4a8Threads, MT == 1 ? 4 : 3) w4a8_gemm_kernel(
+__global__ void __launch_bounds__(kW4a8Threads, MT == 16 ? 3 : 4) w4a8_gemm_kernel(
     const int8_t* __restrict__ A_i8, const float* __restrict__ s_a,
     const uint8_t* __restrict__ packed, uint16_t* __restrict__ Y, int* status, int M, int N,
     int K) {
