@@ -123,6 +123,8 @@ def parse():
                          "groups of 128; unrounded weights)")
     ap.add_argument("--shape", action="append", default=[],
                     help="restrict the workload to this shape tag (repeatable; profiling)")
+    ap.add_argument("--mx-only", action="store_true",
+                    help="time only the MX block-scaled decode workload (mx_ffn70b_decode)")
     ap.add_argument("--w4a8-only", action="store_true",
                     help="time only the W4A8 decode workload (w4a8_ffn70b_decode_bf16) and "
                          "print its line")
@@ -894,6 +896,144 @@ def measure_w4a8(a, w4, device, stream, sampler, workload, steps, warmup):
     return out
 
 
+def measure_mx(a, w4, device, stream, sampler, workload, steps, warmup):
+    """The MX block-scaled decode GEMM (MXFP4 weights x MXFP8 activations): per shape one
+    mx_gemm per step, activations given as codes.  Value and roofline over the GEMM's
+    algorithmic bytes (codes, scales, activations, Y)."""
+    import torch
+
+    ws, rank, _ = dist_info()
+    shapes = si.MX_WORKLOADS[workload]
+    cases = [si.make_mx_case(**p) for p in shapes]
+    gemm_bytes = [si.mx_algorithmic_bytes(c.M, c.N, c.K) for c in cases]
+    shape_packed = [w4.mx_packed_bytes(c.N, c.K) for c in cases]
+    copies = max(2, -(-3 * L2_BYTES // max(1, sum(shape_packed))))
+    bufs = []
+    for c, nb in zip(cases, shape_packed):
+        first = torch.empty(nb, dtype=torch.uint8, device=device)
+        w4.mx_repack(torch.from_numpy(c.w_codes).to(device), torch.from_numpy(c.w_scales).to(device),
+                     c.N, c.K, first)
+        reps = [first] + [first.clone() for _ in range(copies - 1)]
+        ac = torch.from_numpy(c.a_codes).to(device)
+        asc = torch.from_numpy(c.a_scales).to(device)
+        Y = torch.empty((c.M, c.N), dtype=torch.int16, device=device)
+        bufs.append((c, reps, ac, asc, Y))
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"{workload}: device status after repack: {w4.status_string(st)}")
+
+    def launch_step(i):
+        for c, reps, ac, asc, Y in bufs:
+            w4.mx_gemm(ac, asc, reps[i % copies], c.M, c.N, c.K, c.dtype, Y, stream)
+
+    with torch.cuda.stream(stream):
+        for i in range(max(3, warmup)):
+            launch_step(i)
+    per_shape_us = []
+    for j, (c, reps, ac, asc, Y) in enumerate(bufs):
+        cs = max(3, -(-3 * L2_BYTES // max(1, shape_packed[j])))
+        own = list(reps[:cs]) + [reps[0].clone() for _ in range(cs - len(reps))]
+        nl = max(20, cs)
+        gj = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(gj, stream=stream):
+                for i in range(nl):
+                    w4.mx_gemm(ac, asc, own[i % cs], c.M, c.N, c.K, c.dtype, Y, stream)
+            gj.replay()
+            f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            f0.record(stream)
+            for _ in range(3):
+                gj.replay()
+            f1.record(stream)
+        stream.synchronize()
+        per_shape_us.append(f0.elapsed_time(f1) * 1e3 / (3 * nl))
+        del gj, own
+    G = max(1, min(a.graph_steps, steps))
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(graph, stream=stream):
+            for g in range(G):
+                launch_step(g)
+        graph.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(steps // G):
+            graph.replay()
+        for i in range(steps % G):
+            launch_step(i)
+        e1.record(stream)
+    stream.synchronize()
+    t_wall1 = time.time()
+    st = w4.w4a16_get_device_status(stream)
+    if st != 0:
+        raise SystemExit(f"{workload}: device status after timed region: {w4.status_string(st)}")
+    elapsed_ms = max_over_ranks(e0.elapsed_time(e1), device)
+    del graph
+    peaks, peak_kind = measured_peaks()
+    hbm_peak = float(peaks["hbm_gbs"])
+    dom_bytes = sum(gemm_bytes) / len(gemm_bytes)
+    achieved = dom_bytes / (sum(per_shape_us) * 1e-6 / len(per_shape_us)) / 1e9
+    step_bytes = sum(gemm_bytes)
+    # end to end: per step one pinned-host copy of all shapes' activation codes and scales
+    # in, one mx_gemm per shape, one copy of all Y out, on one stream
+    host_in = [(torch.from_numpy(c.a_codes).pin_memory(), torch.from_numpy(c.a_scales).pin_memory())
+               for c in cases]
+    host_y = [torch.empty((c.M, c.N), dtype=torch.int16).pin_memory() for c in cases]
+    h2d = sum(x.numel() + y.numel() for x, y in host_in)
+    d2h = sum(2 * y.numel() for y in host_y)
+
+    def e2e_step(i):
+        for (c, reps, ac, asc, Y), (hx, hs), hy in zip(bufs, host_in, host_y):
+            ac.copy_(hx, non_blocking=True)
+            asc.copy_(hs, non_blocking=True)
+            w4.mx_gemm(ac, asc, reps[i % copies], c.M, c.N, c.K, c.dtype, Y, stream)
+            hy.copy_(Y, non_blocking=True)
+
+    e2e_steps = max(1, min(a.e2e_steps, steps))
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            e2e_step(i)
+        stream.synchronize()
+        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        f0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        f1.record(stream)
+    stream.synchronize()
+    e2e_ms = max_over_ranks(f0.elapsed_time(f1), device)
+    out = {
+        "workload": workload, "metric": f"MX block-scaled GEMM achieved HBM TB/s ({workload})",
+        "value": step_bytes * steps * ws / (elapsed_ms * 1e-3) / 1e12, "unit": "TB/s",
+        "ms_per_step": elapsed_ms / steps, "steps": steps, "shapes": len(shapes),
+        "step_bytes": step_bytes,
+        "l2": f"inputs larger than L2: {copies} rotating copies of the packed weights "
+              f"({copies * sum(shape_packed) / 2**20:.0f} MiB per rotation)",
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None, "peak_kind": peak_kind,
+                     "kernel": "mx_gemm_kernel", "launches_per_step": len(cases),
+                     "algorithmic_bytes_per_launch": dom_bytes},
+        "per_shape": [{"shape": si.mx_shape_tag(p), "kernel": "mx_gemm_kernel",
+                       "us": round(us, 3), "gbs": round(b / (us * 1e-6) / 1e9, 1),
+                       "hbm_frac": round(b / (us * 1e-6) / 1e9 / hbm_peak, 4)}
+                      for p, us, b in zip(shapes, per_shape_us, gemm_bytes)],
+        "e2e": {"value": step_bytes * e2e_steps * ws / (e2e_ms * 1e-3) / 1e12, "unit": "TB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "kernels_per_step": {"mx_gemm_kernel": len(cases)},
+        "gpu_launches": len(cases) * steps,
+        "clocks": sampler.summary(t_wall0, t_wall1),
+        "note": "E2M1 / E4M3 decoded by cvt into the f16 mma.sync, E8M0 block scales on each "
+                "32-value partial sum; not the native block-scaled MMA"}
+    del bufs
+    torch.cuda.synchronize(device)
+    torch.cuda.empty_cache()
+    return out
+
+
 # Workloads timed beside the headline in a default run (M <= 16 decode at 70B scale, the
 # batch transition and prefill: the rest of the metric), each with its own roofline.
 EXTRA_WORKLOADS = ["ffn70b_decode_bf16", "transition_k8192_n8192",
@@ -923,20 +1063,21 @@ def run_ours(a):
     sampler.start()
     time.sleep(0.3)
 
-    if a.w4a8_only:
-        name = next(iter(si.W4A8_WORKLOADS))
-        x = measure_w4a8(a, w4, device, stream, sampler, name, a.steps, a.warmup)
+    if a.w4a8_only or a.mx_only:
+        name = next(iter(si.MX_WORKLOADS if a.mx_only else si.W4A8_WORKLOADS))
+        meas = measure_mx if a.mx_only else measure_w4a8
+        x = meas(a, w4, device, stream, sampler, name, a.steps, a.warmup)
         sampler.stop()
         if rank == 0:
             print(json.dumps({
                 "metric": x["metric"], "value": x["value"], "unit": x["unit"], "n_gpus": ws,
                 "steps": a.steps, "warmup": a.warmup, "ms_per_step": x["ms_per_step"],
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-                "dtype": "i8", "data": "synthetic",
+                "dtype": "fp4xfp8" if a.mx_only else "i8", "data": "synthetic",
                 "config": {"workload": name, "shapes": x["shapes"], "step_bytes": x["step_bytes"],
                            "l2": x["l2"], "parallelism": f"replicas{ws}"},
                 "roofline": x["roofline"], "per_shape": x["per_shape"], "cpu_baseline": None,
-                "e2e": x["e2e"], "kernel": "w4a8_gemm_kernel",
+                "e2e": x["e2e"], "kernel": x["roofline"]["kernel"],
                 "kernels_per_step": x["kernels_per_step"], "gpu_launches": x["gpu_launches"],
                 "clocks": x["clocks"], "note": x["note"]}), flush=True)
         return

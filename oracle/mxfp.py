@@ -131,6 +131,16 @@ def dequant_mx(codes, exps, fmt: str) -> np.ndarray:
     return vals[c] * scale
 
 
+def unpack_e2m1_bytes(w_bytes, N: int, K: int) -> np.ndarray:
+    """Canonical weight bytes [N, K/2] (K value k in the low nibble of byte k/2 for even k,
+    the high nibble for odd k) -> codes [N, K] int64."""
+    b = np.asarray(w_bytes, dtype=np.int64).reshape(N, K // 2)
+    out = np.empty((N, K), dtype=np.int64)
+    out[:, 0::2] = b & 0xF
+    out[:, 1::2] = b >> 4
+    return out
+
+
 def gemm_mx(a_codes, a_exps, w_codes, w_exps) -> np.ndarray:
     """Y[m, n] = sum_k a[m, k] w[n, k] of MXFP8 (E4M3) activations and MXFP4 (E2M1)
     weights, accumulated in fp64.  Also returns sum_k |a w| for a rounding bound."""

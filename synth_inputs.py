@@ -135,6 +135,51 @@ def make_w4a8_case(M: int, N: int, K: int, dtype: int = FP16, seed: int = 0, *,
     return W4A8Case(M, N, K, dtype, A, qweight, s_u8, off, s_w, meta={"seed": seed})
 
 
+@dataclass
+class MXCase:
+    M: int
+    N: int
+    K: int
+    dtype: int
+    a_codes: np.ndarray   # uint8 [M, K] E4M3 codes
+    a_scales: np.ndarray  # uint8 [M, K/32] E8M0 codes
+    w_codes: np.ndarray   # uint8 [N, K/2], two E2M1 codes per byte (even K in the low nibble)
+    w_scales: np.ndarray  # uint8 [N, K/32] E8M0 codes
+    meta: dict = field(default_factory=dict)
+
+
+def make_mx_case(M: int, N: int, K: int, dtype: int = FP16, seed: int = 0, *,
+                 w_exp: tuple[int, int] = (119, 123), a_exp: tuple[int, int] = (122, 126)
+                 ) -> MXCase:
+    """MXFP4 weights and MXFP8 activations drawn directly as codes: uniform E2M1 codes,
+    uniform E4M3 codes except the two NaN patterns, E8M0 scale codes uniform in the given
+    inclusive ranges (2^-8..2^-4 for weights, 2^-5..2^-1 for activations by default)."""
+    assert K % 128 == 0
+    a_codes = _rng(seed, _STREAM_A).integers(0, 254, size=(M, K)).astype(np.uint8)
+    a_codes[a_codes >= 0x7F] += 1  # skip 0x7F; 0xFF is never drawn (0..253 -> 0..254)
+    a_scales = _rng(seed, _STREAM_S).integers(a_exp[0], a_exp[1] + 1, size=(M, K // 32)).astype(np.uint8)
+    w_codes = _rng(seed, _STREAM_Q).integers(0, 256, size=(N, K // 2)).astype(np.uint8)
+    w_scales = _rng(seed, _STREAM_STEP).integers(w_exp[0], w_exp[1] + 1, size=(N, K // 32)).astype(np.uint8)
+    return MXCase(M, N, K, dtype, a_codes, a_scales, w_codes, w_scales, meta={"seed": seed})
+
+
+def mx_algorithmic_bytes(M: int, N: int, K: int) -> int:
+    """Bytes an MX decode GEMM moves at least once: E2M1 codes and weight scales, E4M3
+    activations and their scales, and Y (16-bit)."""
+    return K * N // 2 + (K // 32) * N + M * K + M * (K // 32) + 2 * M * N
+
+
+# MX workloads (make_mx_case arguments): the 70B-shaped decode FFN shapes, M in {1, 8, 16}.
+MX_WORKLOADS = {
+    "mx_ffn70b_decode": [dict(M=m, N=n, K=k, dtype=BF16, seed=2)
+                         for (k, n) in ((8192, 28672), (28672, 8192)) for m in (1, 8, 16)],
+}
+
+
+def mx_shape_tag(p: dict) -> str:
+    return f"MX_M{p['M']}_N{p['N']}_K{p['K']}_{DTYPE_NAMES[p['dtype']]}"
+
+
 def w4a8_algorithmic_bytes(M: int, N: int, K: int) -> int:
     """Bytes a W4A8 GEMM moves at least once: codes, steps and offsets, channel scales,
     int8 A with its row scales, and Y (16-bit)."""

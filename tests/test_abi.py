@@ -128,3 +128,23 @@ def test_w4a8_host_validation(L):
     assert L.w4a8_gemm(fake + 4, fake, fake, 4, 32, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG
     assert L.w4a8_gemm(fake, fake, fake, 4, 32, 128, 0, fake + 1, None) == w4.W4A16_ERR_INVALID_ARG
     assert L.w4a8_dequant_debug(None, 32, 128, fake, None) == w4.W4A16_ERR_INVALID_ARG
+
+
+# ---- MX block-scaled decode GEMM (include/mxfp.h) ------------------------------------------
+
+@pytest.mark.parametrize("N,K", [(16, 128), (40, 256), (28672, 8192)])
+def test_mx_packed_bytes_formula(L, N, K):
+    Np = -(-N // 16) * 16
+    assert w4.mx_packed_bytes(N, K) == 128 + (Np // 16) * (K // 128) * 1088
+
+
+def test_mx_host_validation(L):
+    fake = 1 << 20
+    assert w4.mx_packed_bytes(16, 100) == 0 and w4.mx_packed_bytes(0, 128) == 0
+    assert L.mx_repack(None, fake, 16, 128, fake, 1 << 20, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.mx_repack(fake, fake, 16, 192, fake, 1 << 20, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.mx_repack(fake, fake, 16, 128, fake, 10, None) == w4.W4A16_ERR_INVALID_ARG
+    assert L.mx_gemm(None, None, None, 0, 16, 128, 0, None, None) == w4.W4A16_OK
+    assert L.mx_gemm(fake, fake, fake, 17, 16, 128, 0, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.mx_gemm(fake, fake, fake, 4, 16, 128, 2, fake, None) == w4.W4A16_ERR_UNSUPPORTED
+    assert L.mx_gemm(fake + 4, fake, fake, 4, 16, 128, 0, fake, None) == w4.W4A16_ERR_INVALID_ARG

@@ -136,3 +136,8 @@ def test_e4m3_rounding_against_torch():
     mine = np.array([mxfp._values(mxfp.E4M3)[mxfp.round_to_element(float(x), mxfp.E4M3)]
                      for x in xs])
     assert np.array_equal(np.abs(lib), np.abs(mine))
+
+
+def test_unpack_e2m1_bytes_nibble_order():
+    b = np.array([[0x21, 0xF0]], dtype=np.uint8)  # K 0 = 1, K 1 = 2, K 2 = 0, K 3 = 15
+    assert mxfp.unpack_e2m1_bytes(b, 1, 4).tolist() == [[1, 2, 0, 15]]

@@ -16,7 +16,8 @@ import threading
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libw4a16.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "w4a16.h")
-HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "w4a8.h")]
+HEADERS = [HEADER, os.path.join(os.path.dirname(HERE), "include", "w4a8.h"),
+           os.path.join(os.path.dirname(HERE), "include", "mxfp.h")]
 
 W4A16_OK = 0
 W4A16_ERR_INVALID_ARG = -1
@@ -102,16 +103,22 @@ def lib() -> ctypes.CDLL:
             L.w4a8_gemm.restype = I
             L.w4a8_dequant_debug.argtypes = [P, I, I, P, P]
             L.w4a8_dequant_debug.restype = I
+            L.mx_packed_bytes.argtypes = [I, I]
+            L.mx_packed_bytes.restype = Z
+            L.mx_repack.argtypes = [P, P, I, I, P, Z, P]
+            L.mx_repack.restype = I
+            L.mx_gemm.argtypes = [P, P, P, I, I, I, I, P, P]
+            L.mx_gemm.restype = I
             _lib = L
     return _lib
 
 
 def header_functions() -> list[str]:
-    """Names of the functions the public headers (include/w4a16.h, include/w4a8.h) declare."""
+    """Names of the functions the public headers (include/w4a16.h, w4a8.h, mxfp.h) declare."""
     names = set()
     for h in HEADERS:
         src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        names.update(re.findall(r"\b(w4a(?:16|8)_[a-z_0-9]+)\s*\(", src))
+        names.update(re.findall(r"\b((?:w4a16|w4a8|mx)_[a-z_0-9]+)\s*\(", src))
     return sorted(names)
 
 
@@ -246,6 +253,24 @@ def w4a8_gemm(A_i8, s_a, packed, M: int, N: int, K: int, dtype: int, Y, stream=N
 def w4a8_dequant_debug(packed, N: int, K: int, W_out, stream=None) -> None:
     _check(lib().w4a8_dequant_debug(_ptr(packed), N, K, _ptr(W_out), _stream(stream)),
            "w4a8_dequant_debug")
+
+
+def mx_packed_bytes(N: int, K: int) -> int:
+    return int(lib().mx_packed_bytes(N, K))
+
+
+def mx_repack(w_codes, w_scales, N: int, K: int, packed, packed_bytes: int | None = None,
+              stream=None) -> None:
+    if packed_bytes is None:
+        packed_bytes = packed.numel() * packed.element_size()
+    _check(lib().mx_repack(_ptr(w_codes), _ptr(w_scales), N, K, _ptr(packed), packed_bytes,
+                           _stream(stream)), "mx_repack")
+
+
+def mx_gemm(a_codes, a_scales, packed, M: int, N: int, K: int, dtype: int, Y,
+            stream=None) -> None:
+    _check(lib().mx_gemm(_ptr(a_codes), _ptr(a_scales), _ptr(packed), M, N, K, dtype, _ptr(Y),
+                         _stream(stream)), "mx_gemm")
 
 
 # ---- torch-friendly helpers (allocation + the calls above) ---------------------------

@@ -7,6 +7,7 @@
 
 #include "w4a16.h"
 #include "w4a8.h"
+#include "mxfp.h"
 #include "format.cuh"
 #include "launch.h"
 
@@ -486,6 +487,43 @@ int w4a8_dequant_debug(const void* packed, int N, int K, int8_t* W_out, void* st
     if ((rc = get_ctx(&ctx)) != W4A16_OK) return rc;
     return launch_w4a8_dequant_debug(*ctx, packed, N, K, W_out,
                                      static_cast<cudaStream_t>(stream));
+}
+
+// ---- MX block-scaled decode GEMM (include/mxfp.h) ---------------------------------------
+
+size_t mx_packed_bytes(int N, int K) {
+    if (N < 1 || K < 128 || K % 128 != 0) return 0;
+    return mx_blob_bytes(N, K);
+}
+
+int mx_repack(const uint8_t* w_codes, const uint8_t* w_scales, int N, int K, void* packed,
+              size_t packed_bytes, void* stream) {
+    if (!w_codes || !w_scales || !packed) return W4A16_ERR_INVALID_ARG;
+    if (N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
+    if (K % 128 != 0) return W4A16_ERR_UNSUPPORTED;
+    if (!aligned(packed, 16) || packed_bytes < mx_blob_bytes(N, K)) return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    int rc = get_ctx(&ctx);
+    if (rc != W4A16_OK) return rc;
+    return launch_mx_repack(*ctx, w_codes, w_scales, N, K, packed,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int mx_gemm(const uint8_t* a_codes, const uint8_t* a_scales, const void* packed, int M, int N,
+            int K, int dtype, void* Y, void* stream) {
+    if (M < 0 || N < 1 || K < 1) return W4A16_ERR_INVALID_ARG;
+    if (K % 128 != 0) return W4A16_ERR_UNSUPPORTED;
+    if (dtype != W4A16_FP16 && dtype != W4A16_BF16) return W4A16_ERR_UNSUPPORTED;
+    if (M > 16) return W4A16_ERR_UNSUPPORTED;
+    if (M == 0) return W4A16_OK;
+    if (!a_codes || !a_scales || !packed || !Y) return W4A16_ERR_INVALID_ARG;
+    if (!aligned(a_codes, 16) || !aligned(a_scales, 4) || !aligned(packed, 16) || !aligned(Y, 2))
+        return W4A16_ERR_INVALID_ARG;
+    const DeviceCtx* ctx = nullptr;
+    int rc = get_ctx(&ctx);
+    if (rc != W4A16_OK) return rc;
+    return launch_mx_gemm(*ctx, a_codes, a_scales, packed, M, N, K, dtype, Y,
+                          static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -70,6 +70,14 @@ int launch_w4a8_gemm(const DeviceCtx& ctx, const int8_t* A_i8, const float* s_a,
                      const void* packed, int M, int N, int K, int dtype, void* Y,
                      cudaStream_t stream);
 
+// MX block-scaled decode GEMM (mxfp.cu): blob size, repack, GEMM (M <= 16; -2 beyond).
+size_t mx_blob_bytes(int N, int K);
+int launch_mx_repack(const DeviceCtx& ctx, const uint8_t* w_codes, const uint8_t* w_scales,
+                     int N, int K, void* packed, cudaStream_t stream);
+int launch_mx_gemm(const DeviceCtx& ctx, const uint8_t* a_codes, const uint8_t* a_scales,
+                   const void* packed, int M, int N, int K, int dtype, void* Y,
+                   cudaStream_t stream);
+
 // Rows of A staged per 64-K chunk (8 or 16 for decode tiles, else the tile height).
 int tc_a_rows(int tile_m, int M);
 // 128-K weight blocks per ring stage (one bulk copy each stage).
