@@ -5,13 +5,14 @@ K = 4096, N in {4096, 11008}, group 128, fp16 activations, asymmetric int4 weigh
 (10 launches).  The repack is offline and not timed.  The headline metric is achieved
 HBM TB/s over algorithmic bytes (packed weights + scales + zeros + A + Y).  A default run
 also times, with the same step count, the 70B-shaped decode FFN (HBM TB/s), the batch
-transition sweep and the prefill GEMM (tensor TFLOP/s), each with its own roofline, under
-the line's "per_workload" key.
+transition sweep and the prefill GEMM (tensor TFLOP/s), the W4A8 decode path and the MX
+block-scaled decode path (HBM TB/s), each with its own roofline, under the line's
+"per_workload" key.  `--w4a8-only` / `--mx-only` time just those two.
 
 Prints ONE JSON line (rank 0).  `--impl reference` times the CPU oracle instead, with the
 same metric string, unit and workload.
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                       [--workload NAME] [--no-extra-workloads]
+                       [--workload NAME] [--no-extra-workloads] [--w4a8-only | --mx-only]
 """
 from __future__ import annotations
 
@@ -1104,6 +1105,8 @@ def run_ours(a):
                 "clocks": x.clocks})
         for name in si.W4A8_WORKLOADS:
             extra.append(measure_w4a8(a, w4, device, stream, sampler, name, a.steps, a.warmup))
+        for name in si.MX_WORKLOADS:
+            extra.append(measure_mx(a, w4, device, stream, sampler, name, a.steps, a.warmup))
     time.sleep(0.3)
     sampler.stop()
 
